@@ -1,0 +1,285 @@
+/*
+ * Selective-scan oracle: plain, slow, obviously correct, double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * What it computes (one function per definition on the pages):
+ *
+ *  - oracle_sscan_fwd: the causal selective scan, stepped one timestep at a
+ *    time.  "硬件感知的选择性扫描" page, section 2.3 (the selective_scan
+ *    pseudocode: discretise, update state, contract with C, add D*x) and
+ *    section 7.1 (the PyTorch reference returning (y, h)); the mamba.py
+ *    listing on the "图解Blelloch并行扫描" page, section 3.2 (deltaA =
+ *    exp(delta*A), deltaB*x = delta*B*x, y = h.C + D*x).  Per (b, d):
+ *        h[n] = h0[b,d,n]  (0 when h0 is absent)
+ *        for t:  a = exp(delta[b,d,t]*A[d,n])
+ *                h[n] = a*h[n] + delta[b,d,t]*B[b,n,t]*u[b,d,t]
+ *                y[b,d,t] = sum_n C[b,n,t]*h[n] + D[d]*u[b,d,t]
+ *        final_state[b,d,n] = h[n] after the last step.
+ *    Readings where the pages are loose: B-bar is delta*B (the simplified
+ *    discretisation of section 2.3, not the zero-order-hold form of
+ *    section 1.2); delta is used as given (no softplus inside); y_t uses the
+ *    state after the update at t; the D skip multiplies u, not delta*u.
+ *
+ *  - oracle_pscan_seq: the first-order linear recurrence h_t = a_t*h_{t-1}
+ *    + b_t, one row at a time (the pscan(deltaA, BX) primitive of the
+ *    mamba.py listing, "图解Blelloch并行扫描" section 3.2; with a = 1 it is
+ *    the prefix sum of section 1.1).
+ *
+ *  - oracle_pscan_blelloch: the same recurrence by Blelloch's work-efficient
+ *    up-sweep / down-sweep ("图解Blelloch并行扫描" section 2) applied to the
+ *    pairs (a, b) under the associative operator
+ *        (a1, b1) o (a2, b2) = (a2*a1, a2*b1 + b2)      ("first 1, then 2")
+ *    of the "Mamba的并行扫描" page, section 2.2, and the "硬件感知" page,
+ *    section 3.2.  Each up-sweep level is recorded so that the 8-element
+ *    trace printed on the Blelloch page can be checked.
+ *
+ * The compile flags keep -ffp-contract=off so that x86 and Arm hosts round
+ * identically.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Planted-mistake switch used only by the oracle's own pin tests, which check
+ * that every plausible slip is caught by at least one pin.  0 = the oracle. */
+enum {
+    MUT_NONE = 0,
+    MUT_DROP_D = 1,          /* forget the D*u skip term                     */
+    MUT_NO_DELTA_IN_B = 2,   /* B-bar*x = B*u instead of delta*B*u           */
+    MUT_Y_BEFORE_UPDATE = 3, /* contract C with the state before the update  */
+    MUT_EXP_SIGN = 4,        /* a = exp(-delta*A)                            */
+    MUT_IGNORE_H0 = 5,       /* start from zero even when h0 is given        */
+    MUT_B_NEXT_STEP = 6,     /* read B at t+1 (index slip)                   */
+    MUT_C_FROM_B = 7,        /* contract with B instead of C (operand swap)  */
+    MUT_D_TIMES_DU = 8,      /* skip term D*delta*u instead of D*u           */
+    MUT_COUNT = 9
+};
+
+typedef struct {
+    const double *u, *delta, *A, *B, *C, *D, *h0;
+    double *out, *final_state;
+    int64_t batch, dim, L, N;
+    int64_t first, last; /* channel range [first, last) over batch*dim */
+    int mutation;
+} sscan_job;
+
+static void sscan_channels(const sscan_job *j)
+{
+    const int64_t L = j->L, N = j->N, dim = j->dim;
+    double *h = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    double *hprev = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    for (int64_t ch = j->first; ch < j->last; ++ch) {
+        const int64_t b = ch / dim, d = ch % dim;
+        const double *u = j->u + ch * L;
+        const double *dl = j->delta + ch * L;
+        const double *Ad = j->A + d * N;
+        const double *Bb = j->B + b * N * L;
+        const double *Cb = j->C + b * N * L;
+        double *y = j->out + ch * L;
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = (j->h0 && j->mutation != MUT_IGNORE_H0) ? j->h0[ch * N + n] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const double dt = dl[t];
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                hprev[n] = h[n];
+                double a = exp(dt * Ad[n]);
+                if (j->mutation == MUT_EXP_SIGN) a = exp(-dt * Ad[n]);
+                int64_t tb = t;
+                if (j->mutation == MUT_B_NEXT_STEP && t + 1 < L) tb = t + 1;
+                double bx = dt * Bb[n * L + tb] * u[t];
+                if (j->mutation == MUT_NO_DELTA_IN_B) bx = Bb[n * L + tb] * u[t];
+                h[n] = a * h[n] + bx;
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                double hv = (j->mutation == MUT_Y_BEFORE_UPDATE) ? hprev[n] : h[n];
+                double cv = (j->mutation == MUT_C_FROM_B) ? Bb[n * L + t] : Cb[n * L + t];
+                acc += cv * hv;
+            }
+            if (j->D && j->mutation != MUT_DROP_D) {
+                if (j->mutation == MUT_D_TIMES_DU)
+                    acc += j->D[d] * dt * u[t];
+                else
+                    acc += j->D[d] * u[t];
+            }
+            y[t] = acc;
+        }
+        if (j->final_state)
+            for (int64_t n = 0; n < N; ++n) j->final_state[ch * N + n] = h[n];
+    }
+    free(h);
+    free(hprev);
+}
+
+static void *sscan_thread(void *arg)
+{
+    sscan_channels((const sscan_job *)arg);
+    return NULL;
+}
+
+/* Layouts (row-major, contiguous): u, delta, out [batch, dim, L]; A [dim, N];
+ * B, C [batch, N, L]; D [dim] or NULL; h0, final_state [batch, dim, N] or NULL.
+ * nthreads <= 1 runs on the calling thread.  Returns 0, or -1 on bad sizes. */
+int oracle_sscan_fwd_mutant(const double *u, const double *delta, const double *A,
+                            const double *B, const double *C, const double *D,
+                            const double *h0, double *out, double *final_state,
+                            int64_t batch, int64_t dim, int64_t L, int64_t N,
+                            int nthreads, int mutation)
+{
+    if (batch < 0 || dim < 0 || L < 0 || N < 0) return -1;
+    if (mutation < 0 || mutation >= MUT_COUNT) return -1;
+    const int64_t nch = batch * dim;
+    if (nch == 0) return 0;
+    sscan_job base = {u, delta, A, B, C, D, h0, out, final_state,
+                      batch, dim, L, N, 0, nch, mutation};
+    if (nthreads <= 1 || nch == 1) {
+        sscan_channels(&base);
+        return 0;
+    }
+    if (nthreads > nch) nthreads = (int)nch;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    sscan_job *jobs = (sscan_job *)malloc(sizeof(sscan_job) * (size_t)nthreads);
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = base;
+        jobs[i].first = nch * i / nthreads;
+        jobs[i].last = nch * (i + 1) / nthreads;
+        if (pthread_create(&tid[i], NULL, sscan_thread, &jobs[i]) == 0)
+            started = i + 1;
+        else
+            break;
+    }
+    /* channels of threads that failed to start run here */
+    if (started < nthreads) {
+        sscan_job rest = base;
+        rest.first = jobs[started].first;
+        sscan_channels(&rest);
+    }
+    for (int i = 0; i < started; ++i) pthread_join(tid[i], NULL);
+    free(tid);
+    free(jobs);
+    return 0;
+}
+
+int oracle_sscan_fwd(const double *u, const double *delta, const double *A,
+                     const double *B, const double *C, const double *D,
+                     const double *h0, double *out, double *final_state,
+                     int64_t batch, int64_t dim, int64_t L, int64_t N, int nthreads)
+{
+    return oracle_sscan_fwd_mutant(u, delta, A, B, C, D, h0, out, final_state,
+                                   batch, dim, L, N, nthreads, MUT_NONE);
+}
+
+int oracle_mutation_count(void) { return MUT_COUNT; }
+
+/* h[r,t] = a[r,t]*h[r,t-1] + b[r,t], h[r,-1] = h0[r] (0 when h0 is NULL).
+ * a, b, h: [rows, len]; h0: [rows] or NULL. */
+int oracle_pscan_seq(const double *a, const double *b, const double *h0, double *h,
+                     int64_t rows, int64_t len)
+{
+    if (rows < 0 || len < 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double s = h0 ? h0[r] : 0.0;
+        for (int64_t t = 0; t < len; ++t) {
+            s = a[r * len + t] * s + b[r * len + t];
+            h[r * len + t] = s;
+        }
+    }
+    return 0;
+}
+
+/* (a1,b1) o (a2,b2): apply step 1, then step 2. */
+static void pair_combine(double a1, double b1, double a2, double b2,
+                         double *ao, double *bo)
+{
+    *ao = a2 * a1;
+    *bo = a2 * b1 + b2;
+}
+
+/* One row by Blelloch's scan over (a, b) pairs.  The row is padded to the next
+ * power of two with identity pairs (1, 0).  trace_a / trace_b, when not NULL,
+ * receive the array after each up-sweep level d = 0 .. log2(P)-1, as
+ * [levels, P] row-major (P = padded length); *levels_out gets the level count.
+ * The down-sweep builds exclusive prefixes; the inclusive state is the
+ * exclusive prefix applied to h0, followed by the element itself.
+ * Returns 0, or -1 on bad sizes / allocation failure. */
+int oracle_pscan_blelloch(const double *a, const double *b, double h0, double *h,
+                          int64_t len, double *trace_a, double *trace_b,
+                          int64_t *levels_out)
+{
+    if (len < 0) return -1;
+    if (len == 0) {
+        if (levels_out) *levels_out = 0;
+        return 0;
+    }
+    int64_t P = 1, levels = 0;
+    while (P < len) {
+        P <<= 1;
+        ++levels;
+    }
+    double *xa = (double *)malloc((size_t)P * sizeof(double));
+    double *xb = (double *)malloc((size_t)P * sizeof(double));
+    if (!xa || !xb) {
+        free(xa);
+        free(xb);
+        return -1;
+    }
+    for (int64_t i = 0; i < P; ++i) {
+        xa[i] = i < len ? a[i] : 1.0;
+        xb[i] = i < len ? b[i] : 0.0;
+    }
+    /* up-sweep: node at k+2^(d+1)-1 absorbs its left sibling at k+2^d-1 */
+    for (int64_t d = 0; d < levels; ++d) {
+        const int64_t half = (int64_t)1 << d, stride = half << 1;
+        for (int64_t k = 0; k < P; k += stride) {
+            const int64_t l = k + half - 1, r = k + stride - 1;
+            pair_combine(xa[l], xb[l], xa[r], xb[r], &xa[r], &xb[r]);
+        }
+        if (trace_a && trace_b) {
+            memcpy(trace_a + d * P, xa, (size_t)P * sizeof(double));
+            memcpy(trace_b + d * P, xb, (size_t)P * sizeof(double));
+        }
+    }
+    if (levels_out) *levels_out = levels;
+    /* down-sweep: the root gets the identity; a right child's prefix is its
+     * parent's prefix followed by the left sibling's subtree */
+    double *ea = (double *)malloc((size_t)P * sizeof(double));
+    double *eb = (double *)malloc((size_t)P * sizeof(double));
+    if (!ea || !eb) {
+        free(xa);
+        free(xb);
+        free(ea);
+        free(eb);
+        return -1;
+    }
+    memcpy(ea, xa, (size_t)P * sizeof(double));
+    memcpy(eb, xb, (size_t)P * sizeof(double));
+    ea[P - 1] = 1.0;
+    eb[P - 1] = 0.0;
+    for (int64_t d = levels - 1; d >= 0; --d) {
+        const int64_t half = (int64_t)1 << d, stride = half << 1;
+        for (int64_t k = 0; k < P; k += stride) {
+            const int64_t l = k + half - 1, r = k + stride - 1;
+            const double la = ea[l], lb = eb[l]; /* left subtree aggregate */
+            const double pa = ea[r], pb = eb[r]; /* parent's prefix        */
+            ea[l] = pa;
+            eb[l] = pb;
+            pair_combine(pa, pb, la, lb, &ea[r], &eb[r]);
+        }
+    }
+    for (int64_t i = 0; i < len; ++i) {
+        const double before = ea[i] * h0 + eb[i]; /* state entering step i */
+        h[i] = a[i] * before + b[i];
+    }
+    free(xa);
+    free(xb);
+    free(ea);
+    free(eb);
+    return 0;
+}
