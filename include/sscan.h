@@ -1,0 +1,128 @@
+/*
+ * sscan.h -- C ABI of libsscan.so: the selective-scan forward pass and the
+ * first-order linear-recurrence primitive on one GB300 (sm_103a).
+ *
+ * Every entry point takes plain pointers and sizes; no framework types cross
+ * this boundary.  Device pointers are caller-owned (the library keeps none
+ * after a call returns).  Calls are asynchronous on the caller's stream; the
+ * return code reports argument validation and launch status only.  Kernel
+ * faults surface through sscan_get_last_error() or any later synchronisation.
+ *
+ * Layouts are contiguous and row-major:
+ *   u, delta, out        [batch, dim, seqlen]    (the I/O dtype)
+ *   B, C                 [batch, dstate, seqlen] (the I/O dtype)
+ *   A                    [dim, dstate]           float32
+ *   D                    [dim]                   float32, may be NULL
+ *   h0, final_state      [batch, dim, dstate]    float32, may be NULL
+ */
+#ifndef SSCAN_H
+#define SSCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* I/O dtype of u, delta, B, C and out.  A, D, h0 and final_state are always
+ * float32, and the state and every accumulation are float32 for both (the
+ * pages keep the decay and state at full precision: "为什么Mamba的“并行扫描”不是真并行 (mhpq.cn/news/1057127)" section 4, pitfall 2; "并行扫描与硬件感知优化 (mhpq.cn/news/1077344)" page section 4.3). */
+typedef enum { SSCAN_F32 = 0, SSCAN_BF16 = 1 } sscan_dtype;
+
+/* Status codes.  No entry point aborts or throws. */
+enum {
+    SSCAN_OK = 0,
+    SSCAN_ERR_INVALID = 1, /* a required pointer is NULL, a size is negative or
+                              too large, dstate exceeds sscan_max_dstate(), or
+                              dtype is unknown; nothing was launched          */
+    SSCAN_ERR_CUDA = 2,    /* a CUDA call failed (launch, allocation, or an
+                              asynchronous fault seen by sscan_get_last_error) */
+    SSCAN_ERR_TIMEOUT = 3  /* a bounded device-side wait gave up; reported by
+                              sscan_get_last_error()                          */
+};
+
+/*
+ * sscan_fwd -- selective-scan forward pass, fused in one pass over HBM.
+ *
+ * Defined by the selective_scan pseudocode of "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战" (section
+ * 2.3: discretise with A-bar = exp(delta*A), B-bar = delta*B; h = A-bar*h +
+ * B-bar*x; y = C.h; plus D*x) and its PyTorch reference (section 7.1, which
+ * also takes an initial state and returns the final state), and by the
+ * mamba.py listing of "图解Blelloch并行扫描" (section 3.2).  For every batch b,
+ * channel d and step t, with diagonal A:
+ *
+ *   h_t[n]   = exp(delta[b,d,t]*A[d,n]) * h_{t-1}[n] + delta[b,d,t]*B[b,n,t]*u[b,d,t]
+ *   out[b,d,t] = sum_n C[b,n,t]*h_t[n] + D[d]*u[b,d,t]
+ *
+ * h_{-1} = h0[b,d,:] (zeros when h0 is NULL); final_state[b,d,:] = h after
+ * the last step (not written when NULL).  delta is used as given (no
+ * softplus is applied).  D == NULL means no skip term.
+ *
+ * u, delta, B, C, A: required device pointers.  out: required device pointer
+ * (it must not alias any input).  batch, dim, seqlen >= 0 and
+ * 1 <= dstate <= sscan_max_dstate(); a zero-sized problem returns SSCAN_OK
+ * without launching (final_state, when given, then receives h0 or zeros if
+ * seqlen == 0).  dtype: sscan_dtype.  stream: a cudaStream_t (NULL = legacy
+ * default stream).
+ *
+ * Scratch: long sequences with few channels are split in time; the split
+ * needs batch*dim*segments*(dstate+1) floats of scratch, taken stream-ordered
+ * from CUDA's default memory pool and returned on the same stream.
+ */
+int sscan_fwd(const void *u, const void *delta, const float *A, const void *B,
+              const void *C, const float *D, const float *h0, void *out,
+              float *final_state, int64_t batch, int64_t dim, int64_t seqlen,
+              int64_t dstate, int dtype, void *stream);
+
+/*
+ * sscan_fwd_ex -- sscan_fwd with the launch plan pinned, for testing and
+ * tuning.  segments: number of time segments per channel (0 = automatic; 1 =
+ * no time split); lanes: lanes per channel sharing the state vector (0 =
+ * automatic; 1, 2 or 4, subject to dstate <= 16*lanes).  Results are the same
+ * computation under any plan (up to float32 rounding order).
+ */
+int sscan_fwd_ex(const void *u, const void *delta, const float *A, const void *B,
+                 const void *C, const float *D, const float *h0, void *out,
+                 float *final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                 int64_t dstate, int dtype, int segments, int lanes, void *stream);
+
+/*
+ * pscan -- first-order linear recurrence over rows, the pscan(a, b) primitive
+ * that the mamba.py listing of "图解Blelloch并行扫描" (section 3.2) calls on
+ * (deltaA, BX); with a = 1 it is the prefix sum of that page's section 1.1.
+ *
+ *   h[r,t] = a[r,t]*h[r,t-1] + b[r,t],   h[r,-1] = h0[r] (0 when h0 is NULL)
+ *
+ * a, b, h: device float32 [rows, len], required (h must not alias a or b);
+ * h0: device float32 [rows] or NULL.  rows, len >= 0.  The result is the
+ * same recurrence under any bracketing of the associative operator
+ * (a1,b1) o (a2,b2) = (a2*a1, a2*b1 + b2) ("并行扫描与硬件感知优化 (mhpq.cn/news/1077344)" page, section
+ * 2.2), up to float32 rounding order.
+ */
+int pscan(const float *a, const float *b, float *h, const float *h0,
+          int64_t rows, int64_t len, void *stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *sscan_status_string(int status);
+
+/* Synchronises the stream of this thread's last call and reports any
+ * asynchronous failure since: SSCAN_OK, SSCAN_ERR_CUDA or SSCAN_ERR_TIMEOUT.
+ * Clears the recorded error. */
+int sscan_get_last_error(void);
+
+/* Largest dstate that sscan_fwd accepts. */
+int sscan_max_dstate(void);
+
+/* Number of kernels the calling thread's last sscan_fwd / pscan call
+ * launched (0 for zero-sized problems or rejected calls). */
+int sscan_last_launch_count(void);
+
+/* Text description of the calling thread's last launch plan (kernel
+ * variant, grid, segments, lanes); static per-thread storage. */
+const char *sscan_last_plan(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSCAN_H */

@@ -1,0 +1,196 @@
+"""Selective-scan forward and pscan on GB300 (sm_103a): the Python binding.
+
+The computation lives in ``libsscan.so`` (hand-written CUDA kernels behind
+the C ABI of ``include/sscan.h``).  This module only checks tensor shapes,
+dtypes and devices, allocates outputs with torch, and passes raw pointers and
+the current CUDA stream through ctypes.  There is no fallback: if the library
+is missing or fails to load, every call raises.
+
+    y, h_last = sscan_fwd(u, delta, A, B, C, D=None, h0=None)
+    h = pscan(a, b, h0=None)
+
+Shapes: u, delta [batch, dim, L] (float32 or bfloat16); A [dim, N] float32;
+B, C [batch, N, L] (same dtype as u); D [dim] float32; h0 [batch, dim, N]
+float32.  Returns y [batch, dim, L] in the I/O dtype and the final state
+[batch, dim, N] float32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB as LIB_PATH
+
+SSCAN_OK, SSCAN_ERR_INVALID, SSCAN_ERR_CUDA, SSCAN_ERR_TIMEOUT = 0, 1, 2, 3
+SSCAN_F32, SSCAN_BF16 = 0, 1
+
+_vp, _fp, _i64, _int = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+_lock = threading.Lock()
+_lib = None
+
+# name -> (restype, argtypes): every symbol include/sscan.h declares
+SIGNATURES = {
+    "sscan_fwd": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
+                         _i64, _i64, _i64, _i64, _int, _vp]),
+    "sscan_fwd_ex": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
+                            _i64, _i64, _i64, _i64, _int, _int, _int, _vp]),
+    "pscan": (_int, [_fp, _fp, _fp, _fp, _i64, _i64, _vp]),
+    "sscan_status_string": (ctypes.c_char_p, [_int]),
+    "sscan_get_last_error": (_int, []),
+    "sscan_max_dstate": (_int, []),
+    "sscan_last_launch_count": (_int, []),
+    "sscan_last_plan": (ctypes.c_char_p, []),
+}
+
+
+class SscanError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def load_library(path: str | None = None):
+    """Load libsscan.so (building it first if this tree has sources but no
+    library).  Raises if it cannot be loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if path is None and not os.path.exists(p):
+            from ._build import build
+            build()
+        if not os.path.exists(p):
+            raise RuntimeError(f"libsscan.so not found at {p}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def lib():
+    return load_library()
+
+
+def status_string(status: int) -> str:
+    return lib().sscan_status_string(int(status)).decode()
+
+
+def get_last_error() -> int:
+    return int(lib().sscan_get_last_error())
+
+
+def max_dstate() -> int:
+    return int(lib().sscan_max_dstate())
+
+
+def last_launch_count() -> int:
+    return int(lib().sscan_last_launch_count())
+
+
+def last_plan() -> str:
+    return lib().sscan_last_plan().decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, shape, dtype, device):
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, out=None, final_state=None,
+              return_final_state: bool = True, segments: int = 0, lanes: int = 0,
+              stream=None):
+    """Selective-scan forward on the GPU.  See the module docstring.
+
+    ``segments`` / ``lanes`` pin the launch plan (0 = automatic); the result is
+    the same computation under any plan.  Returns ``(y, final_state)``
+    (``final_state`` is None when ``return_final_state`` is False and none was
+    passed).
+    """
+    if u.dim() != 3:
+        raise ValueError("u must be [batch, dim, L]")
+    batch, dim, L = u.shape
+    if A.dim() != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("sscan_fwd runs on CUDA tensors only")
+    io = u.dtype
+    if io not in (torch.float32, torch.bfloat16):
+        raise ValueError("u must be float32 or bfloat16")
+    _check(u, "u", (batch, dim, L), io, dev)
+    _check(delta, "delta", (batch, dim, L), io, dev)
+    _check(A, "A", (dim, N), torch.float32, dev)
+    _check(B, "B", (batch, N, L), io, dev)
+    _check(C, "C", (batch, N, L), io, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (batch, dim, N), torch.float32, dev)
+    if out is None:
+        out = torch.empty((batch, dim, L), dtype=io, device=dev)
+    else:
+        _check(out, "out", (batch, dim, L), io, dev)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _check(final_state, "final_state", (batch, dim, N), torch.float32, dev)
+    dtype = SSCAN_F32 if io == torch.float32 else SSCAN_BF16
+    rc = lib().sscan_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                            _ptr(h0), _ptr(out), _ptr(final_state), batch, dim, L, N,
+                            dtype, int(segments), int(lanes), _stream_handle(stream))
+    if rc != SSCAN_OK:
+        raise SscanError(rc, "sscan_fwd")
+    return out, final_state
+
+
+def pscan(a, b, h0=None, *, out=None, stream=None):
+    """h[r,t] = a[r,t]*h[r,t-1] + b[r,t] with h[r,-1] = h0[r] (0 if None), on
+    float32 CUDA tensors a, b [rows, len].  Returns h [rows, len]."""
+    if a.dim() != 2:
+        raise ValueError("a must be [rows, len]")
+    rows, n = a.shape
+    dev = a.device
+    if dev.type != "cuda":
+        raise ValueError("pscan runs on CUDA tensors only")
+    _check(a, "a", (rows, n), torch.float32, dev)
+    _check(b, "b", (rows, n), torch.float32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (rows,), torch.float32, dev)
+    if out is None:
+        out = torch.empty((rows, n), dtype=torch.float32, device=dev)
+    else:
+        _check(out, "out", (rows, n), torch.float32, dev)
+    rc = lib().pscan(_ptr(a), _ptr(b), _ptr(out), _ptr(h0), rows, n, _stream_handle(stream))
+    if rc != SSCAN_OK:
+        raise SscanError(rc, "pscan")
+    return out
+
+
+__all__ = ["sscan_fwd", "pscan", "status_string", "get_last_error", "max_dstate",
+           "last_launch_count", "last_plan", "load_library", "SscanError",
+           "SIGNATURES", "LIB_PATH"]

@@ -1,0 +1,719 @@
+// Fused selective-scan forward kernels for sm_103a.
+//
+// What is computed (the selective_scan pseudocode of "Mamba 状态空间模型：从理论
+// 到生产级推理的 CUDA 内核优化实战", section 2.3, with the initial/final state of
+// its section 7.1): per batch b, channel d, state n and step t
+//     h_t[n] = exp(delta_t * A[d,n]) * h_{t-1}[n] + (delta_t * u_t) * B[b,n,t]
+//     y_t    = sum_n C[b,n,t] * h_t[n] + D[d] * u_t
+//
+// Work decomposition (diagonal A makes every (b, d, n) an independent chain,
+// "为什么Mamba的“并行扫描”不是真并行" section 1):
+//   * a lane owns one channel and NS of its states (P lanes share a channel;
+//     lane g of the group owns states n = k*P + g), keeping h in registers;
+//   * a warp covers 32/P channels, a CTA of 4 warps covers DT channels and
+//     walks time in chunks of TC steps; u/delta tiles [DT x TC] and the B/C
+//     tile [N x TC] of the chunk are staged in shared memory by cp.async
+//     (multi-stage ring) and the B/C tile is reused by every channel of the CTA
+//     (the fusion of discretisation, scan and C-contraction of "并行扫描与硬件
+//     感知优化 (mhpq.cn/news/1077344)" section 3.2, with the double buffering
+//     of the CUDA page's section 4.3 generalised to a ring);
+//   * the C-contraction's partial sums of the P lanes of a channel are
+//     combined by a shuffle reduce-scatter over 4 steps, so each lane writes
+//     one output; outputs are staged in shared memory and stored as 16-byte
+//     vectors;
+//   * long sequences with few channels are split into S time segments
+//     (the chunked scan of "并行扫描与硬件感知优化" section 2.4).  Segments carry
+//     their aggregate (prod_t exp(delta_t A) = 2^(A log2e * sum_t delta_t),
+//     h_end) -- the chunk-carry identity of "为什么Mamba的“并行扫描”不是真并行"
+//     section 3 -- and the state entering a segment is the fold of the
+//     aggregates before it, i.e. the associative operator
+//     (a1,b1) o (a2,b2) = (a2 a1, a2 b1 + b2) applied in order.
+#pragma once
+
+#include "device_utils.cuh"
+
+namespace sscan {
+
+enum FwdMode : int {
+    MODE_SINGLE = 0,  // one segment: start from h0, write y and final_state
+    MODE_LOCAL = 1,   // segment s starts from h0 (s = 0) or 0; write y and the
+                      // segment aggregate; the correction kernel adds the carry
+    MODE_AGG = 2,     // like MODE_LOCAL but only the aggregate (no y)
+    MODE_FOLD = 3     // segment s starts from the fold of segments < s; write y;
+                      // the last segment writes final_state
+};
+
+struct FwdParams {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const float* h0;
+    void* out;
+    float* final_state;
+    float* seg_state;  // [batch*dim, S, N]  state at the end of each segment
+    float* seg_dsum;   // [batch*dim, S]     sum of delta over each segment
+    long long batch, dim, L, N;
+    long long Tseg;    // steps per segment (multiple of TC)
+    int S;             // segments per channel
+    int tiles_per_batch;
+    int mode;
+    int seg_count;     // segments covered by this grid: grid = tiles * seg_count
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T, int NS_, int P_>
+struct FwdCfg {
+    static constexpr int NS = NS_;
+    static constexpr int P = P_;
+    static constexpr int kWarps = 2;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int PPW = 32 / P;                // channel pairs per warp
+    static constexpr int CPW = 2 * PPW;               // channels per warp
+    static constexpr int DT = kWarps * CPW;           // channels per CTA
+    static constexpr int NSP = NS * P;                // state slots per channel
+    static constexpr int TC = 16;                     // steps per chunk
+    static constexpr int VECE = 16 / (int)sizeof(T);  // elements per 16 bytes
+    static constexpr int RROW = TC + VECE;            // raw smem row (T), padded by 16 B
+    static constexpr int PPR = TC / VECE;             // 16-byte pieces per raw row
+    static constexpr int UROW = 2 * TC + 4;           // interleaved u/delta row (fp32)
+    static constexpr int GS2 = 2 * NS + ((P == 4 && NS >= 16) ? 4 : 0);  // dup state group
+    static constexpr int RB2 = P * GS2;               // floats per duplicated B/C row
+    static constexpr int RAW_ELEMS = (2 * DT + 2 * NSP) * RROW;
+    static constexpr int RAW_BYTES = RAW_ELEMS * (int)sizeof(T);
+    static constexpr int UW_FLOATS = (DT / 2) * UROW;  // one of u, delta
+    static constexpr int BW_FLOATS = TC * RB2;         // one of B, C
+    static constexpr int WORK_FLOATS = 2 * UW_FLOATS + 2 * BW_FLOATS;
+    static constexpr int Y_ELEMS = DT * RROW;
+    static constexpr int FIXED_BYTES = 2 * WORK_FLOATS * 4 + 2 * Y_ELEMS * (int)sizeof(T);
+    static constexpr int STAGES = (RAW_BYTES * 4 + FIXED_BYTES <= 48 * 1024) ? 4
+                                  : (RAW_BYTES * 3 + FIXED_BYTES <= 96 * 1024) ? 3
+                                                                               : 2;
+    static constexpr int SMEM_BYTES = STAGES * RAW_BYTES + FIXED_BYTES;
+    static constexpr int kCorrThreads = 2 * kThreads;  // correction kernel: a lane per (channel, group)
+    static_assert(32 % P == 0, "lanes per channel must divide the warp");
+    static_assert(NS % 2 == 0, "state slots are read 2 at a time");
+    static_assert(TC % VECE == 0 && TC % 4 == 0, "chunk must hold whole vectors");
+    static_assert((RROW * sizeof(T)) % 16 == 0, "smem rows must stay 16-byte aligned");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// State entering segment s (s >= 1) for states n = g*NS + k of one channel: the
+// fold of the aggregates of segments 0 .. s-1 (segment 0's entry holds its true
+// end state because it started from h0).
+template <int NS>
+__device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, int s, int g,
+                                              const float (&Al2)[NS], float (&h)[NS]) {
+    const float* st = p.seg_state + ch * p.S * p.N;
+    const float* ds = p.seg_dsum + ch * p.S;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        const long long n = (long long)g * NS + k;
+        h[k] = n < p.N ? st[n] : 0.f;
+    }
+    for (int sp = 1; sp < s; ++sp) {
+        const float dsum = ds[sp];
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const long long n = (long long)g * NS + k;
+            const float bagg = n < p.N ? st[(long long)sp * p.N + n] : 0.f;
+            h[k] = fmaf(ex2(Al2[k] * dsum), h[k], bagg);
+        }
+    }
+}
+
+// Shared-memory layout of the chunked kernel:
+//   raw ring [STAGES]: u [DT][RROW], delta [DT][RROW], B [NSP][RROW], C [NSP][RROW]
+//                      (type T, copied verbatim from global by cp.async)
+//   work [2]:          u, delta [DT/2][UROW]: the two channels of a pair interleaved
+//                        per step (u0[t], u1[t], u0[t+1], ...), fp32;
+//                      B, C [TC][RB2]: per step, every state value twice
+//                        (B[n], B[n], B[n+1], B[n+1], ...), group g at g*GS2, fp32
+//   ybuf [2]:          y [DT][RROW] (type T)
+template <typename T, int NS, int P>
+struct Smem {
+    using Cfg = FwdCfg<T, NS, P>;
+    T* raw;
+    float* work;
+    T* ybuf;
+    __device__ __forceinline__ explicit Smem(unsigned char* base)
+        : raw(reinterpret_cast<T*>(base)),
+          work(reinterpret_cast<float*>(base + Cfg::STAGES * Cfg::RAW_BYTES)),
+          ybuf(reinterpret_cast<T*>(base + Cfg::STAGES * Cfg::RAW_BYTES + 2 * Cfg::WORK_FLOATS * 4)) {}
+    __device__ __forceinline__ T* stage(int i) const { return raw + (i % Cfg::STAGES) * Cfg::RAW_ELEMS; }
+    __device__ __forceinline__ float* wk(int i) const { return work + (i & 1) * Cfg::WORK_FLOATS; }
+    __device__ __forceinline__ T* yb(int i) const { return ybuf + (i & 1) * Cfg::Y_ELEMS; }
+};
+
+// Duplicated-B/C column of state n: group n / NS, slot n % NS, two floats each.
+template <int NS, int GS2>
+__device__ __forceinline__ int dup_col(int n) { return (n / NS) * GS2 + 2 * (n % NS); }
+
+// VEC path, step 1: issue this thread's 16-byte cp.async pieces of chunk [t0, t0+TC).
+// A thread owns the same piece of both rows of a channel pair, and whole B/C
+// pieces.  Out-of-range pieces are zero-filled (delta = 0 keeps the state).
+template <typename T, int NS, int P, bool LOAD_C>
+__device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long b, long long d0,
+                                            long long t0, long long t_end, int tid) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
+    const T* gu = static_cast<const T*>(p.u);
+    const T* gd = static_cast<const T*>(p.delta);
+    const T* gB = static_cast<const T*>(p.B);
+    const T* gC = static_cast<const T*>(p.C);
+    T* su = st;
+    T* sd = st + DT * RROW;
+    T* sB = st + 2 * DT * RROW;
+    T* sC = sB + NSP * RROW;
+    for (int q = tid; q < (DT / 2) * PPR; q += Cfg::kThreads) {
+        const int pr = q / PPR, pc = q % PPR;
+        const long long t = t0 + (long long)pc * VE;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int r = 2 * pr + e;
+            const long long dd = d0 + r;
+            const bool ok = dd < p.dim && t < t_end;
+            const long long off = (b * p.dim + (ok ? dd : 0)) * p.L + (ok ? t : 0);
+            cp_async16(su + r * RROW + pc * VE, gu + off, ok ? 16 : 0);
+            cp_async16(sd + r * RROW + pc * VE, gd + off, ok ? 16 : 0);
+        }
+    }
+    const int N = (int)p.N;
+    for (int q = tid; q < N * PPR; q += Cfg::kThreads) {
+        const int n = q / PPR, pc = q % PPR;
+        const long long t = t0 + (long long)pc * VE;
+        const bool ok = t < t_end;
+        const long long off = (b * p.N + n) * p.L + (ok ? t : 0);
+        cp_async16(sB + n * RROW + pc * VE, gB + off, ok ? 16 : 0);
+        if (LOAD_C) cp_async16(sC + n * RROW + pc * VE, gC + off, ok ? 16 : 0);
+    }
+}
+
+// VEC path, step 2 (after this thread's copies of the chunk landed): widen the
+// pieces this same thread copied into the fp32 work tiles (u/delta interleaved
+// by channel pair, B/C transposed and duplicated).  Only own pieces are
+// touched, so no barrier is needed between the copy and the conversion.
+template <typename T, int NS, int P, bool LOAD_C>
+__device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* st, float* wk, int tid) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
+    constexpr int UROW = Cfg::UROW, RB2 = Cfg::RB2, GS2 = Cfg::GS2;
+    const T* su = st;
+    const T* sd = st + DT * RROW;
+    const T* sB = st + 2 * DT * RROW;
+    const T* sC = sB + NSP * RROW;
+    float* wu = wk;
+    float* wd = wk + Cfg::UW_FLOATS;
+    float* wB = wk + 2 * Cfg::UW_FLOATS;
+    float* wC = wB + Cfg::BW_FLOATS;
+    for (int q = tid; q < (DT / 2) * PPR; q += Cfg::kThreads) {
+        const int pr = q / PPR, pc = q % PPR;
+#pragma unroll
+        for (int e = 0; e < VE; e += 2) {
+            // two steps of both channels -> one 16-byte store per array
+            float a0[4], a1[4];
+            load4_smem(su + (2 * pr) * RROW + pc * VE + (e & ~3), a0);
+            load4_smem(su + (2 * pr + 1) * RROW + pc * VE + (e & ~3), a1);
+            const int o = e & 3;
+            *reinterpret_cast<float4*>(wu + pr * UROW + 2 * (pc * VE + e)) =
+                make_float4(a0[o], a1[o], a0[o + 1], a1[o + 1]);
+            load4_smem(sd + (2 * pr) * RROW + pc * VE + (e & ~3), a0);
+            load4_smem(sd + (2 * pr + 1) * RROW + pc * VE + (e & ~3), a1);
+            *reinterpret_cast<float4*>(wd + pr * UROW + 2 * (pc * VE + e)) =
+                make_float4(a0[o], a1[o], a0[o + 1], a1[o + 1]);
+        }
+    }
+    const int N = (int)p.N;
+    for (int q = tid; q < N * PPR; q += Cfg::kThreads) {
+        const int n = q / PPR, pc = q % PPR;
+        const int col = dup_col<NS, GS2>(n);
+#pragma unroll
+        for (int e = 0; e < VE; e += 4) {
+            float v[4];
+            load4_smem(sB + n * RROW + pc * VE + e, v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float2*>(wB + (pc * VE + e + j) * RB2 + col) = make_float2(v[j], v[j]);
+            if (LOAD_C) {
+                load4_smem(sC + n * RROW + pc * VE + e, v);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<float2*>(wC + (pc * VE + e + j) * RB2 + col) = make_float2(v[j], v[j]);
+            }
+        }
+    }
+}
+
+// Non-VEC path (rows not 16-byte aligned): synchronous element loads with bounds
+// checks straight into the fp32 work tiles.
+template <typename T, int NS, int P, bool LOAD_C>
+__device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* wk, long long b,
+                                                  long long d0, long long t0, long long t_end, int tid) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, UROW = Cfg::UROW, RB2 = Cfg::RB2, GS2 = Cfg::GS2;
+    const T* gu = static_cast<const T*>(p.u);
+    const T* gd = static_cast<const T*>(p.delta);
+    const T* gB = static_cast<const T*>(p.B);
+    const T* gC = static_cast<const T*>(p.C);
+    float* wu = wk;
+    float* wd = wk + Cfg::UW_FLOATS;
+    float* wB = wk + 2 * Cfg::UW_FLOATS;
+    float* wC = wB + Cfg::BW_FLOATS;
+    for (int q = tid; q < DT * TC; q += Cfg::kThreads) {
+        const int r = q / TC, tt = q % TC;
+        const long long dd = d0 + r, t = t0 + tt;
+        const bool ok = dd < p.dim && t < t_end;
+        const long long off = (b * p.dim + dd) * p.L + t;
+        wu[(r / 2) * UROW + 2 * tt + (r & 1)] = ok ? to_f32(gu[off]) : 0.f;
+        wd[(r / 2) * UROW + 2 * tt + (r & 1)] = ok ? to_f32(gd[off]) : 0.f;
+    }
+    const int N = (int)p.N;
+    for (int q = tid; q < N * TC; q += Cfg::kThreads) {
+        const int n = q % N, tt = q / N;
+        const long long t = t0 + tt;
+        const bool ok = t < t_end;
+        const long long off = (b * p.N + n) * p.L + t;
+        const int col = dup_col<NS, GS2>(n);
+        const float vb = ok ? to_f32(gB[off]) : 0.f;
+        *reinterpret_cast<float2*>(wB + tt * RB2 + col) = make_float2(vb, vb);
+        if (LOAD_C) {
+            const float vc = ok ? to_f32(gC[off]) : 0.f;
+            *reinterpret_cast<float2*>(wC + tt * RB2 + col) = make_float2(vc, vc);
+        }
+    }
+}
+
+// Write a staged output chunk [DT x TC] to global memory.
+template <typename T, int NS, int P, bool VEC>
+__device__ __forceinline__ void store_chunk(const FwdParams& p, const T* ys, long long b,
+                                            long long d0, long long t0, long long t_end, int tid) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, RROW = Cfg::RROW;
+    T* go = static_cast<T*>(p.out);
+    if constexpr (VEC) {
+        constexpr int PPR = Cfg::PPR, VE = Cfg::VECE;
+        for (int q = tid; q < DT * PPR; q += Cfg::kThreads) {
+            const int r = q / PPR, pc = q % PPR;
+            const long long dd = d0 + r, t = t0 + (long long)pc * VE;
+            if (dd < p.dim && t < t_end)
+                *reinterpret_cast<uint4*>(go + (b * p.dim + dd) * p.L + t) =
+                    *reinterpret_cast<const uint4*>(ys + r * RROW + pc * VE);
+        }
+    } else {
+        constexpr int TC = Cfg::TC;
+        for (int q = tid; q < DT * TC; q += Cfg::kThreads) {
+            const int r = q / TC, tt = q % TC;
+            const long long dd = d0 + r, t = t0 + tt;
+            if (dd < p.dim && t < t_end) go[(b * p.dim + dd) * p.L + t] = ys[r * RROW + tt];
+        }
+    }
+}
+
+// Combine the P lanes' partial outputs of 4 consecutive steps (a shuffle
+// reduce-scatter).  Afterwards lane g of a 4-lane group holds step g in v[0];
+// lane g of a 2-lane group holds steps 2g, 2g+1 in v[0], v[1]; a lone lane
+// holds all four.
+template <int P>
+__device__ __forceinline__ void reduce4(const float (&y)[4], int g, float (&v)[4]) {
+    constexpr unsigned FULL = 0xffffffffu;
+    if constexpr (P == 4) {
+        const bool hi = (g & 2) != 0;
+        const float k0 = hi ? y[2] : y[0], k1 = hi ? y[3] : y[1];
+        const float s0 = hi ? y[0] : y[2], s1 = hi ? y[1] : y[3];
+        const float r0 = k0 + __shfl_xor_sync(FULL, s0, 2);
+        const float r1 = k1 + __shfl_xor_sync(FULL, s1, 2);
+        const bool odd = (g & 1) != 0;
+        const float kv = odd ? r1 : r0;
+        const float sv = odd ? r0 : r1;
+        v[0] = kv + __shfl_xor_sync(FULL, sv, 1);
+    } else if constexpr (P == 2) {
+        const bool hi = (g & 1) != 0;
+        const float k0 = hi ? y[2] : y[0], k1 = hi ? y[3] : y[1];
+        const float s0 = hi ? y[0] : y[2], s1 = hi ? y[1] : y[3];
+        v[0] = k0 + __shfl_xor_sync(FULL, s0, 1);
+        v[1] = k1 + __shfl_xor_sync(FULL, s1, 1);
+    } else {
+        v[0] = y[0]; v[1] = y[1]; v[2] = y[2]; v[3] = y[3];
+    }
+}
+
+// Reduce-scatter one channel's 4 partial outputs and write the lane's share
+// into its staged output row (yrow points at the first of the 4 steps).
+template <typename T, int P>
+__device__ __forceinline__ void reduce_write4(const float (&y)[4], int g, T* yrow) {
+    float v[4];
+    reduce4<P>(y, g, v);
+    if constexpr (P == 4) {
+        yrow[g] = from_f32<T>(v[0]);
+    } else if constexpr (P == 2) {
+        yrow[2 * g] = from_f32<T>(v[0]);
+        yrow[2 * g + 1] = from_f32<T>(v[1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) yrow[j] = from_f32<T>(v[j]);
+    }
+}
+
+// One chunk of the recurrence for the calling lane: channel pair pr (rows 2pr,
+// 2pr+1 of the tile), states n = g*NS + k; each float2 holds the two channels.
+// SCALAR: every state of a channel shares one decay rate (one exponent per
+// channel and step).  Returns the chunk's sum of delta (both channels) when DSUM.
+template <typename T, int NS, int P, bool WRITE_Y, bool SCALAR, bool DSUM>
+__device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, int g,
+                                                const float2 (&A2)[NS], float2 As2,
+                                                float2 (&h2)[NS], float2 D2) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int TC = Cfg::TC, UROW = Cfg::UROW, RB2 = Cfg::RB2, GS2 = Cfg::GS2, RROW = Cfg::RROW;
+    const float* wu = wk + pr * UROW;
+    const float* wd = wk + Cfg::UW_FLOATS + pr * UROW;
+    const float* wB = wk + 2 * Cfg::UW_FLOATS + g * GS2;
+    const float* wC = wB + Cfg::BW_FLOATS;
+    T* yrow0 = yb + (2 * pr) * RROW;
+    T* yrow1 = yrow0 + RROW;
+    float2 csum = make_float2(0.f, 0.f);
+#pragma unroll 1
+    for (int t4 = 0; t4 < TC; t4 += 4) {
+        float y0[4], y1[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; jj += 2) {
+            const float4 u4 = *reinterpret_cast<const float4*>(wu + 2 * (t4 + jj));
+            const float4 d4 = *reinterpret_cast<const float4*>(wd + 2 * (t4 + jj));
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int t = t4 + jj + hf;
+                const float2 u2 = hf ? make_float2(u4.z, u4.w) : make_float2(u4.x, u4.y);
+                const float2 d2 = hf ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+                if (DSUM) csum = __fadd2_rn(csum, d2);
+                const float2 du2 = __fmul2_rn(d2, u2);
+                float2 a2s;
+                if (SCALAR) {
+                    const float2 xs = __fmul2_rn(d2, As2);
+                    a2s = make_float2(ex2(xs.x), ex2(xs.y));
+                }
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                if (WRITE_Y && g == 0) acc0 = __fmul2_rn(D2, u2);
+                const float* brow = wB + t * RB2;
+                const float* crow = wC + t * RB2;
+#pragma unroll
+                for (int kq = 0; kq < NS / 2; ++kq) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(brow + 4 * kq);
+                    float4 c4;
+                    if (WRITE_Y) c4 = *reinterpret_cast<const float4*>(crow + 4 * kq);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * kq + e;
+                        float2 a2;
+                        if (SCALAR) {
+                            a2 = a2s;
+                        } else {
+                            const float2 x2 = __fmul2_rn(d2, A2[k]);
+                            a2 = make_float2(ex2(x2.x), ex2(x2.y));
+                        }
+                        const float2 bb = e ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+                        h2[k] = __ffma2_rn(a2, h2[k], __fmul2_rn(du2, bb));
+                        if (WRITE_Y) {
+                            const float2 cc = e ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                            if (e) acc1 = __ffma2_rn(cc, h2[k], acc1);
+                            else acc0 = __ffma2_rn(cc, h2[k], acc0);
+                        }
+                    }
+                }
+                if (WRITE_Y) {
+                    const float2 yy = __fadd2_rn(acc0, acc1);
+                    y0[jj + hf] = yy.x;
+                    y1[jj + hf] = yy.y;
+                }
+            }
+        }
+        if (WRITE_Y) {
+            reduce_write4<T, P>(y0, g, yrow0 + t4);
+            reduce_write4<T, P>(y1, g, yrow1 + t4);
+        }
+    }
+    return csum;
+}
+
+template <typename T, int NS, int P, bool VEC>
+__global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(const FwdParams p) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, RB2 = Cfg::RB2, GS2 = Cfg::GS2, NSP = Cfg::NSP;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const Smem<T, NS, P> sm(smem_raw);
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int g = lane % P;
+    const int pr = w * Cfg::PPW + lane / P;  // channel pair within the tile
+    const int tile = blockIdx.x / p.seg_count;
+    const int s = blockIdx.x % p.seg_count;
+    const long long b = tile / p.tiles_per_batch;
+    const long long d0 = (long long)(tile % p.tiles_per_batch) * DT;
+    const long long t_begin = (long long)s * p.Tseg;
+    const long long t_end = min(p.L, t_begin + p.Tseg);
+    const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + TC - 1) / TC) : 0;
+    const bool write_y = p.mode != MODE_AGG;
+    const bool dsum_on = p.mode == MODE_LOCAL || p.mode == MODE_AGG;
+
+    // the lane's two channels and their decay rates (A * log2 e); a warp whose
+    // channels each have a single rate takes the one-exponent-per-step path
+    long long dch[2], ch[2];
+    bool dval[2];
+    float Al2[2][NS];
+    float2 As2, D2;
+    bool uniform_rate = true;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        dch[e] = d0 + 2 * pr + e;
+        dval[e] = dch[e] < p.dim;
+        ch[e] = b * p.dim + (dval[e] ? dch[e] : 0);
+        const float a_first = dval[e] ? p.A[dch[e] * p.N] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const long long n = (long long)g * NS + k;
+            const bool nv = dval[e] && n < p.N;
+            const float a = nv ? p.A[dch[e] * p.N + n] : a_first;
+            uniform_rate &= (a == a_first);
+            Al2[e][k] = nv ? a * kLog2e : 0.f;
+        }
+        const float as = a_first * kLog2e;
+        const float dd = (p.D != nullptr && dval[e]) ? p.D[dch[e]] : 0.f;
+        if (e == 0) { As2.x = as; D2.x = dd; } else { As2.y = as; D2.y = dd; }
+    }
+    const bool scalar = __all_sync(FULL, uniform_rate);
+    float2 A2[NS], h2[NS];
+    {
+        float hs[2][NS];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (p.mode == MODE_FOLD && s > 0) {
+                fold_segments<NS>(p, ch[e], s, g, Al2[e], hs[e]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NS; ++k) {
+                    const long long n = (long long)g * NS + k;
+                    hs[e][k] = (s == 0 && p.h0 != nullptr && dval[e] && n < p.N) ? p.h0[ch[e] * p.N + n] : 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            A2[k] = make_float2(Al2[0][k], Al2[1][k]);
+            h2[k] = make_float2(hs[0][k], hs[1][k]);
+        }
+    }
+
+    // duplicated B/C columns of state slots >= N stay zero for the whole kernel
+    if ((int)p.N < NSP) {
+        const int nz = NSP - (int)p.N;
+        for (int q = tid; q < 2 * 2 * TC * nz; q += Cfg::kThreads) {
+            const int n = (int)p.N + q % nz;
+            const int row = q / nz;  // [buf][B|C][t]
+            const int buf = row / (2 * TC), rr = row % (2 * TC);
+            float* wbase = sm.work + buf * Cfg::WORK_FLOATS + 2 * Cfg::UW_FLOATS;
+            *reinterpret_cast<float2*>(wbase + rr * RB2 + dup_col<NS, GS2>(n)) = make_float2(0.f, 0.f);
+        }
+    }
+
+    // prologue: chunks 0 .. STAGES-2 in flight, chunk 0 converted
+    if constexpr (VEC) {
+#pragma unroll
+        for (int j = 0; j < STAGES - 1; ++j) {
+            if (j < nchunks) {
+                if (write_y) issue_chunk<T, NS, P, true>(p, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
+                else issue_chunk<T, NS, P, false>(p, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
+            }
+            cp_async_commit();
+        }
+        cp_async_wait<STAGES - 2>();
+        if (nchunks > 0) {
+            if (write_y) convert_own_pieces<T, NS, P, true>(p, sm.stage(0), sm.wk(0), tid);
+            else convert_own_pieces<T, NS, P, false>(p, sm.stage(0), sm.wk(0), tid);
+        }
+    } else {
+        if (nchunks > 0) {
+            if (write_y) load_chunk_scalar<T, NS, P, true>(p, sm.wk(0), b, d0, t_begin, t_end, tid);
+            else load_chunk_scalar<T, NS, P, false>(p, sm.wk(0), b, d0, t_begin, t_end, tid);
+        }
+    }
+
+    float2 dsum = make_float2(0.f, 0.f), dcomp = make_float2(0.f, 0.f);  // Kahan sums of delta
+    for (int i = 0; i < nchunks; ++i) {
+        __syncthreads();
+        const long long t0 = t_begin + (long long)i * TC;
+        if (write_y && i > 0) store_chunk<T, NS, P, VEC>(p, sm.yb(i - 1), b, d0, t0 - TC, t_end, tid);
+        if constexpr (VEC) {
+            const int nx = i + STAGES - 1;
+            if (nx < nchunks) {
+                if (write_y) issue_chunk<T, NS, P, true>(p, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
+                else issue_chunk<T, NS, P, false>(p, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
+            }
+            cp_async_commit();
+        }
+        float2 csum = make_float2(0.f, 0.f);
+        if (write_y) {
+            if (scalar) {
+                if (dsum_on) csum = compute_chunk<T, NS, P, true, true, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+                else compute_chunk<T, NS, P, true, true, false>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+            } else {
+                if (dsum_on) csum = compute_chunk<T, NS, P, true, false, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+                else compute_chunk<T, NS, P, true, false, false>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+            }
+        } else {
+            if (scalar) csum = compute_chunk<T, NS, P, false, true, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+            else csum = compute_chunk<T, NS, P, false, false, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+        }
+        if (dsum_on) {
+            const float2 yk = make_float2(csum.x - dcomp.x, csum.y - dcomp.y);
+            const float2 tk = make_float2(dsum.x + yk.x, dsum.y + yk.y);
+            dcomp = make_float2((tk.x - dsum.x) - yk.x, (tk.y - dsum.y) - yk.y);
+            dsum = tk;
+        }
+        if (i + 1 < nchunks) {
+            if constexpr (VEC) {
+                cp_async_wait<STAGES - 2>();
+                if (write_y) convert_own_pieces<T, NS, P, true>(p, sm.stage(i + 1), sm.wk(i + 1), tid);
+                else convert_own_pieces<T, NS, P, false>(p, sm.stage(i + 1), sm.wk(i + 1), tid);
+            } else {
+                if (write_y) load_chunk_scalar<T, NS, P, true>(p, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
+                else load_chunk_scalar<T, NS, P, false>(p, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    if (write_y && nchunks > 0)
+        store_chunk<T, NS, P, VEC>(p, sm.yb(nchunks - 1), b, d0, t_begin + (long long)(nchunks - 1) * TC, t_end, tid);
+
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        if (!dval[e]) continue;
+        const float dse = e ? dsum.y : dsum.x;
+        if (p.mode == MODE_LOCAL || p.mode == MODE_AGG) {
+            float* sst = p.seg_state + (ch[e] * p.S + s) * p.N;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const long long n = (long long)g * NS + k;
+                if (n < p.N) sst[n] = e ? h2[k].y : h2[k].x;
+            }
+            if (g == 0) p.seg_dsum[ch[e] * p.S + s] = dse;
+        } else if (p.final_state != nullptr && (p.mode == MODE_SINGLE || s == p.S - 1)) {
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const long long n = (long long)g * NS + k;
+                if (n < p.N) p.final_state[ch[e] * p.N + n] = e ? h2[k].y : h2[k].x;
+            }
+        }
+    }
+}
+
+// Global loads of 4 consecutive elements [t, t+4) of a row, widened to fp32;
+// elements at or beyond t_end read as zero.
+template <typename T, bool VEC>
+__device__ __forceinline__ void gload4(const T* row, long long t, long long t_end, float (&v)[4]) {
+    if constexpr (VEC) {
+        if constexpr (sizeof(T) == 4) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(row + t));
+            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        } else {
+            const uint2 q = __ldg(reinterpret_cast<const uint2*>(row + t));
+            v[0] = __uint_as_float(q.x << 16);
+            v[1] = __uint_as_float(q.x & 0xffff0000u);
+            v[2] = __uint_as_float(q.y << 16);
+            v[3] = __uint_as_float(q.y & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = (t + j < t_end) ? to_f32(row[t + j]) : 0.f;
+    }
+}
+
+// Carry correction for segments s >= 1 after a MODE_LOCAL pass: with h_in the
+// state entering the segment, h_t = P_t h_in + h_t(local) where P_t is the
+// running product of the decays, so y_t gains sum_n C[b,n,t] P_t[n] h_in[n].
+// The homogeneous state g = P_t h_in is advanced step by step until every
+// lane's g has decayed to exactly zero (or the segment ends), and the last
+// segment writes final_state = 2^(A log2e sum(delta)) h_in + h_end(local).
+template <typename T, int NS, int P, bool VEC>
+__global__ void __launch_bounds__(FwdCfg<T, NS, P>::kCorrThreads) sscan_fwd_correct(const FwdParams p) {
+    using Cfg = FwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC;
+    constexpr unsigned FULL = 0xffffffffu;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int c = lane / P, g = lane % P;
+    const int crow = w * (32 / P) + c;  // kCorrThreads lanes cover the DT channels of a tile
+    const int segs = p.S - 1;
+    const int tile = blockIdx.x / segs;
+    const int s = 1 + blockIdx.x % segs;
+    const long long b = tile / p.tiles_per_batch;
+    const long long d = (long long)(tile % p.tiles_per_batch) * DT + crow;
+    const bool dval = d < p.dim;
+    const long long ch = b * p.dim + (dval ? d : 0);
+    const long long t_begin = (long long)s * p.Tseg;
+    const long long t_end = min(p.L, t_begin + p.Tseg);
+
+    float Al2[NS], gst[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        const long long n = (long long)g * NS + k;
+        Al2[k] = (dval && n < p.N) ? p.A[d * p.N + n] * kLog2e : 0.f;
+    }
+    fold_segments<NS>(p, ch, s, g, Al2, gst);
+    if (!dval) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k) gst[k] = 0.f;
+    }
+    if (dval && s == p.S - 1 && p.final_state != nullptr) {
+        const float dsum = p.seg_dsum[ch * p.S + s];
+        const float* sst = p.seg_state + (ch * p.S + s) * p.N;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const long long n = (long long)g * NS + k;
+            if (n < p.N) p.final_state[ch * p.N + n] = fmaf(ex2(Al2[k] * dsum), gst[k], sst[n]);
+        }
+    }
+
+    const T* drow = static_cast<const T*>(p.delta) + ch * p.L;
+    const T* Cb = static_cast<const T*>(p.C) + b * p.N * p.L;
+    T* orow = static_cast<T*>(p.out) + ch * p.L;
+    for (long long tc = t_begin; tc < t_end; tc += TC) {
+        bool live = false;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) live |= (gst[k] != 0.f);
+        if (!__any_sync(FULL, live)) break;
+        for (long long t = tc; t < min(tc + TC, t_end); t += 4) {
+            float dd[4];
+            gload4<T, VEC>(drow, t, t_end, dd);
+            float yv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const long long n = (long long)g * NS + k;
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (n < p.N) gload4<T, VEC>(Cb + n * p.L, t, t_end, cc);
+                float gv = gst[k];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    gv *= ex2(dd[j] * Al2[k]);
+                    yv[j] = fmaf(cc[j], gv, yv[j]);
+                }
+                gst[k] = gv;
+            }
+            float v[4];
+            reduce4<P>(yv, g, v);
+            if (dval) {
+                constexpr int NOWN = (P == 4) ? 1 : ((P == 2) ? 2 : 4);
+                const long long tt0 = t + (P == 4 ? g : (P == 2 ? 2 * g : 0));
+#pragma unroll
+                for (int j = 0; j < NOWN; ++j) {
+                    const long long tt = tt0 + j;
+                    if (tt < t_end) orow[tt] = from_f32<T>(to_f32(orow[tt]) + v[j]);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace sscan

@@ -11,14 +11,14 @@ The arithmetic lives in ``sscan_oracle.c`` (plain C, double precision,
 ctypes and converts arrays to float64.  Each function cites the passage it
 follows:
 
-* :func:`sscan_fwd` -- the sequential selective scan of the "硬件感知的选择性扫描"
+* :func:`sscan_fwd` -- the sequential selective scan of the "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战"
   page, section 2.3 (pseudocode) and section 7.1 (PyTorch reference), and of
   the mamba.py listing on the "图解Blelloch并行扫描" page, section 3.2.
 * :func:`pscan_seq` -- h_t = a_t*h_{t-1} + b_t row by row (the ``pscan``
   primitive of that listing; with a = 1 the prefix sum of its section 1.1).
 * :func:`pscan_blelloch` -- the same recurrence by Blelloch up-sweep /
   down-sweep over (a, b) pairs ("图解Blelloch并行扫描", section 2), with the
-  combine (a1,b1) o (a2,b2) = (a2*a1, a2*b1+b2) of the "Mamba的并行扫描" page,
+  combine (a1,b1) o (a2,b2) = (a2*a1, a2*b1+b2) of the "并行扫描与硬件感知优化 (mhpq.cn/news/1077344)" page,
   section 2.2.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` to values the pages

@@ -9,7 +9,7 @@
  * What it computes (one function per definition on the pages):
  *
  *  - oracle_sscan_fwd: the causal selective scan, stepped one timestep at a
- *    time.  "硬件感知的选择性扫描" page, section 2.3 (the selective_scan
+ *    time.  "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战" page, section 2.3 (the selective_scan
  *    pseudocode: discretise, update state, contract with C, add D*x) and
  *    section 7.1 (the PyTorch reference returning (y, h)); the mamba.py
  *    listing on the "图解Blelloch并行扫描" page, section 3.2 (deltaA =
@@ -33,7 +33,8 @@
  *    up-sweep / down-sweep ("图解Blelloch并行扫描" section 2) applied to the
  *    pairs (a, b) under the associative operator
  *        (a1, b1) o (a2, b2) = (a2*a1, a2*b1 + b2)      ("first 1, then 2")
- *    of the "Mamba的并行扫描" page, section 2.2, and the "硬件感知" page,
+ *    of the "并行扫描与硬件感知优化 (mhpq.cn/news/1077344)" page, section 2.2, and the
+ *    "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战" page,
  *    section 3.2.  Each up-sweep level is recorded so that the 8-element
  *    trace printed on the Blelloch page can be checked.
  *

@@ -152,7 +152,7 @@ def _rand_problem(seed, batch=2, dim=3, L=17, N=4, h0=True, D=True):
 def pin_lti_convolution(sscan):
     """Constant delta, B, C over t: y_k = sum_{i<=k} C Abar^i Bbar u_{k-i}
     + C Abar^{k+1} h0 + D u_k, with Abar = exp(delta A), Bbar = delta B
-    ("硬件感知的选择性扫描", section 1.3), by brute-force convolution."""
+    ("Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战", section 1.3), by brute-force convolution."""
     r = _rng(11)
     batch, dim, L, N = 2, 3, 40, 5
     dval = r.uniform(0.05, 0.6, size=(batch, dim))
@@ -185,7 +185,7 @@ def pin_lti_convolution(sscan):
 def pin_chunk_identity_page_example(sscan):
     """The chunk-carry identity with the page's diagonal A-bar and chunk 3:
     h_{3k} = Abar^3 h_{3(k-1)} + sum_{i=0}^{2} Abar^{2-i} Bbar x_{3(k-1)+i+1}
-    ("Mamba的并行扫描与硬件感知优化", section 3; the index is read as in the
+    ("为什么Mamba的“并行扫描”不是真并行 (mhpq.cn/news/1057127)", section 3; the index is read as in the
     page's own simulation, h3 = A^3 h0 + A^2 Bx1 + A Bx2 + Bx3)."""
     g = read_golden("chunk_carry_diag.txt")
     abar = np.array(g["abar"][0])
