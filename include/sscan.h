@@ -102,6 +102,42 @@ int sscan_fwd_ex(const void *u, const void *delta, const float *A, const void *B
 int pscan(const float *a, const float *b, float *h, const float *h0,
           int64_t rows, int64_t len, void *stream);
 
+/* Bytes of device memory that sscan_fwd_noalloc keeps, per GPU, for the
+ * carry of time-split launches (a fixed array, held until the process exits). */
+#define SSCAN_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * sscan_fwd_noalloc -- sscan_fwd for callers that cannot allocate device
+ * memory while they run.  The pages have no counterpart: this is a deployment
+ * variant of the same computation.
+ *
+ * Some callers must never allocate on their execution path -- an inference
+ * engine's per-request plugin hook running under a fixed memory budget, a
+ * real-time loop in which an allocation could synchronise the device or wait
+ * on the allocator, a runtime that hands out all memory up front.  sscan_fwd
+ * takes the scratch of a time-split launch from CUDA's stream-ordered pool;
+ * this entry point keeps that scratch in a fixed device array of
+ * SSCAN_NOALLOC_SCRATCH_BYTES instead and calls no allocating routine.  The
+ * caller still passes every input and output.
+ *
+ * Arguments are those of sscan_fwd plus segments: 0 picks the time split
+ * automatically, shrunk so that its carry (batch*dim*segments*(dstate+1)
+ * floats) fits the array; a positive value pins it, and a pinned split whose
+ * carry does not fit is rejected with SSCAN_ERR_INVALID before anything is
+ * launched.  The result equals sscan_fwd's under the same plan.
+ *
+ * The first call on each device looks up the array's address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the array and each
+ * call writes everything it reads from it, so no clearing is needed, but
+ * calls whose kernels may overlap on the GPU (unordered streams) race on it.
+ * sscan_last_launch_count() and sscan_last_plan() do not describe these calls.
+ */
+int sscan_fwd_noalloc(const void *u, const void *delta, const float *A, const void *B,
+                      const void *C, const float *D, const float *h0, void *out,
+                      float *final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                      int64_t dstate, int dtype, int segments, void *stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *sscan_status_string(int status);
 

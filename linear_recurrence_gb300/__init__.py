@@ -37,6 +37,8 @@ SIGNATURES = {
                          _i64, _i64, _i64, _i64, _int, _vp]),
     "sscan_fwd_ex": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
                             _i64, _i64, _i64, _i64, _int, _int, _int, _vp]),
+    "sscan_fwd_noalloc": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
+                                 _i64, _i64, _i64, _i64, _int, _int, _vp]),
     "pscan": (_int, [_fp, _fp, _fp, _fp, _i64, _i64, _vp]),
     "sscan_status_string": (ctypes.c_char_p, [_int]),
     "sscan_get_last_error": (_int, []),

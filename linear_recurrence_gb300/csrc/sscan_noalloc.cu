@@ -1,0 +1,167 @@
+// sscan_fwd_noalloc: the selective-scan forward pass without any device
+// allocation, for callers that cannot allocate device memory while they run.
+//
+// Some hosts must never allocate during their own execution path: an
+// inference engine calling a plugin's per-request hook under a fixed memory
+// budget, a real-time loop where an allocation may synchronise the device or
+// stall on the allocator, or an embedding runtime whose memory is handed out
+// up front.  sscan_fwd may need a little scratch (the per-segment carry of a
+// time-split launch) and takes it from CUDA's stream-ordered pool; this entry
+// point instead keeps that scratch in a fixed array in device memory that
+// every GPU which loads libsscan.so holds until the process exits.
+//
+// Setup: the first call on each device looks up the array's device address
+// with cudaGetSymbolAddress (with that device current) and caches it.  That
+// lookup may load the module, so make the first call on a device before any
+// stream capture.
+//
+// Sharing: every call uses the same array.  Everything a call reads from it
+// is written earlier in the same call, so nothing needs clearing between
+// calls, but two calls whose kernels overlap on the GPU (different streams,
+// no ordering between them) race on the array and may corrupt each other's
+// results.  Order such calls on one stream, or use sscan_fwd.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/sscan.h"
+#include "sscan_dispatch.cuh"
+
+namespace {
+
+constexpr size_t kScratchBytes = SSCAN_NOALLOC_SCRATCH_BYTES;  // carry scratch per GPU
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[64] = {nullptr};  // per device ordinal
+
+// Device address of the scratch array on the current device (set up once).
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+inline bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaError_t launch(int dtype, sscan::FwdKernel k, const sscan::FwdParams& p, sscan::Shape sh,
+                   bool vec, long long grid, cudaStream_t st) {
+    if (grid <= 0) return cudaSuccess;
+    return dtype == SSCAN_F32 ? sscan::fwd_launch_f32(k, p, sh, vec, (int)grid, st)
+                              : sscan::fwd_launch_bf16(k, p, sh, vec, (int)grid, st);
+}
+
+}  // namespace
+
+extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
+                                 const void* C, const float* D, const float* h0, void* out,
+                                 float* final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                                 int64_t dstate, int dtype, int segments, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype != SSCAN_F32 && dtype != SSCAN_BF16) return SSCAN_ERR_INVALID;
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > sscan::kMaxDstate ||
+        segments < 0)
+        return SSCAN_ERR_INVALID;
+    const long long big = (long long)1 << 46;
+    if (batch > big || dim > big || seqlen > big || (batch && dim > big / batch) ||
+        (batch * dim && seqlen > big / (batch * dim)))
+        return SSCAN_ERR_INVALID;
+    sscan::Shape sh{0, 0};
+    {
+        const int lanes = dstate <= 4 ? 1 : (dstate <= 8 ? 2 : 4);
+        bool found = false;
+        for (const sscan::Shape& s : sscan::kShapes)
+            if (s.P == lanes && (long long)s.NS * s.P >= dstate) { sh = s; found = true; break; }
+        if (!found) return SSCAN_ERR_INVALID;
+    }
+    if (batch == 0 || dim == 0) return SSCAN_OK;
+    if (seqlen == 0) {
+        if (final_state) {
+            const size_t bytes = (size_t)(batch * dim * dstate) * sizeof(float);
+            cudaError_t e = h0 ? cudaMemcpyAsync(final_state, h0, bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(final_state, 0, bytes, st);
+            if (e != cudaSuccess) return SSCAN_ERR_CUDA;
+        }
+        return SSCAN_OK;
+    }
+    if (!u || !delta || !A || !B || !C || !out) return SSCAN_ERR_INVALID;
+
+    const int esz = dtype == SSCAN_F32 ? 4 : 2;
+    const bool vec = (seqlen % (16 / esz)) == 0 && is_aligned16(u) && is_aligned16(delta) &&
+                     is_aligned16(B) && is_aligned16(C) && is_aligned16(out);
+    const int DT = sscan::fwd_channels_per_cta(sh);
+    const int TC = sscan::kChunkSteps;
+    const long long tiles_per_batch = cdiv(dim, DT);
+    const long long tiles = batch * tiles_per_batch;
+    if (tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
+    // carry scratch of a plan with S segments: batch*dim*S*(dstate+1) floats
+    const long long per_segment = batch * dim * (dstate + 1) * (long long)sizeof(float);
+    const long long max_segments = (long long)kScratchBytes / per_segment;  // may be 0 or 1
+
+    long long S = segments;
+    if (S == 0) {
+        int dev = 0, nsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SSCAN_ERR_CUDA;
+        const int occ = dtype == SSCAN_F32 ? sscan::fwd_occupancy_f32(sh, vec)
+                                           : sscan::fwd_occupancy_bf16(sh, vec);
+        const long long target = (long long)std::max(nsm, 1) * std::max(occ, 1);
+        S = tiles >= target ? 1 : cdiv(target, tiles);
+        S = std::min(S, std::max(1LL, seqlen / (8LL * TC)));
+        S = std::min(S, std::max(1LL, max_segments));  // automatic plans shrink to the array
+    }
+    S = std::max(1LL, std::min(S, cdiv(seqlen, TC)));
+    const long long Tseg = cdiv(cdiv(seqlen, S), TC) * TC;
+    S = cdiv(seqlen, Tseg);
+    if (S > 1 && S > max_segments) return SSCAN_ERR_INVALID;  // would overflow the fixed scratch
+    if (tiles * S > (1LL << 30)) return SSCAN_ERR_INVALID;
+
+    sscan::FwdParams p{};
+    p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.h0 = h0;
+    p.out = out; p.final_state = final_state;
+    p.batch = batch; p.dim = dim; p.L = seqlen; p.N = dstate;
+    p.Tseg = Tseg; p.S = (int)S; p.tiles_per_batch = (int)tiles_per_batch;
+
+    cudaError_t e;
+    if (S == 1) {
+        p.mode = sscan::MODE_SINGLE;
+        p.seg_count = 1;
+        e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles, st);
+        return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+    }
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return SSCAN_ERR_CUDA;
+    const size_t nseg = (size_t)(batch * dim) * (size_t)S;
+    p.seg_state = static_cast<float*>(scratch);
+    p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
+    if (dtype == SSCAN_F32) {
+        p.mode = sscan::MODE_LOCAL;
+        p.seg_count = (int)S;
+        e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * S, st);
+        if (e == cudaSuccess) e = launch(dtype, sscan::FwdKernel::Correct, p, sh, vec, tiles * (S - 1), st);
+    } else {
+        p.mode = sscan::MODE_AGG;
+        p.seg_count = (int)(S - 1);
+        e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
+        if (e == cudaSuccess) {
+            p.mode = sscan::MODE_FOLD;
+            p.seg_count = (int)S;
+            e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * S, st);
+        }
+    }
+    return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
+}
