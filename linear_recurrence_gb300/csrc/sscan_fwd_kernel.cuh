@@ -80,12 +80,12 @@ struct FwdCfg {
     static constexpr int RROW = TC + VECE;            // raw smem row (T), padded by 16 B
     static constexpr int PPR = TC / VECE;             // 16-byte pieces per raw row
     static constexpr int UROW = 2 * TC + 4;           // interleaved u/delta row (fp32)
-    static constexpr int GS2 = 2 * NS + ((P == 4 && NS >= 16) ? 4 : 0);  // dup state group
-    static constexpr int RB2 = P * GS2;               // floats per duplicated B/C row
+    static constexpr int GS = NS + ((P == 4 && NS >= 16) ? 4 : 0);  // floats per state group
+    static constexpr int RB = P * GS;                 // floats per B/C work row (one step)
     static constexpr int RAW_ELEMS = (2 * DT + 2 * NSP) * RROW;
     static constexpr int RAW_BYTES = RAW_ELEMS * (int)sizeof(T);
     static constexpr int UW_FLOATS = (DT / 2) * UROW;  // one of u, delta
-    static constexpr int BW_FLOATS = TC * RB2;         // one of B, C
+    static constexpr int BW_FLOATS = TC * RB;          // one of B, C
     static constexpr int WORK_FLOATS = 2 * UW_FLOATS + 2 * BW_FLOATS;
     static constexpr int Y_ELEMS = DT * RROW;
     static constexpr int FIXED_BYTES = 2 * WORK_FLOATS * 4 + 2 * Y_ELEMS * (int)sizeof(T);
@@ -95,7 +95,7 @@ struct FwdCfg {
     static constexpr int SMEM_BYTES = STAGES * RAW_BYTES + FIXED_BYTES;
     static constexpr int kCorrThreads = 2 * kThreads;  // correction kernel: a lane per (channel, group)
     static_assert(32 % P == 0, "lanes per channel must divide the warp");
-    static_assert(NS % 2 == 0, "state slots are read 2 at a time");
+    static_assert(NS % 4 == 0, "state slots are read 4 at a time");
     static_assert(TC % VECE == 0 && TC % 4 == 0, "chunk must hold whole vectors");
     static_assert((RROW * sizeof(T)) % 16 == 0, "smem rows must stay 16-byte aligned");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -130,8 +130,8 @@ __device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, 
 //                      (type T, copied verbatim from global by cp.async)
 //   work [2]:          u, delta [DT/2][UROW]: the two channels of a pair interleaved
 //                        per step (u0[t], u1[t], u0[t+1], ...), fp32;
-//                      B, C [TC][RB2]: per step, every state value twice
-//                        (B[n], B[n], B[n+1], B[n+1], ...), group g at g*GS2, fp32
+//                      B, C [TC][RB]: transposed so that a lane's NS states at
+//                        one step are contiguous, group g at g*GS, fp32
 //   ybuf [2]:          y [DT][RROW] (type T)
 template <typename T, int NS, int P>
 struct Smem {
@@ -148,9 +148,9 @@ struct Smem {
     __device__ __forceinline__ T* yb(int i) const { return ybuf + (i & 1) * Cfg::Y_ELEMS; }
 };
 
-// Duplicated-B/C column of state n: group n / NS, slot n % NS, two floats each.
-template <int NS, int GS2>
-__device__ __forceinline__ int dup_col(int n) { return (n / NS) * GS2 + 2 * (n % NS); }
+// B/C work-tile column of state n: group n / NS, slot n % NS.
+template <int NS, int GS>
+__device__ __forceinline__ int work_col(int n) { return (n / NS) * GS + (n % NS); }
 
 // VEC path, step 1: issue this thread's 16-byte cp.async pieces of chunk [t0, t0+TC).
 // A thread owns the same piece of both rows of a channel pair, and whole B/C
@@ -200,7 +200,7 @@ template <typename T, int NS, int P, bool LOAD_C>
 __device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* st, float* wk, int tid) {
     using Cfg = FwdCfg<T, NS, P>;
     constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
-    constexpr int UROW = Cfg::UROW, RB2 = Cfg::RB2, GS2 = Cfg::GS2;
+    constexpr int UROW = Cfg::UROW, RB = Cfg::RB, GS = Cfg::GS;
     const T* su = st;
     const T* sd = st + DT * RROW;
     const T* sB = st + 2 * DT * RROW;
@@ -229,19 +229,17 @@ __device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* 
     const int N = (int)p.N;
     for (int q = tid; q < N * PPR; q += Cfg::kThreads) {
         const int n = q / PPR, pc = q % PPR;
-        const int col = dup_col<NS, GS2>(n);
+        const int col = work_col<NS, GS>(n);
 #pragma unroll
         for (int e = 0; e < VE; e += 4) {
             float v[4];
             load4_smem(sB + n * RROW + pc * VE + e, v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<float2*>(wB + (pc * VE + e + j) * RB2 + col) = make_float2(v[j], v[j]);
+            for (int j = 0; j < 4; ++j) wB[(pc * VE + e + j) * RB + col] = v[j];
             if (LOAD_C) {
                 load4_smem(sC + n * RROW + pc * VE + e, v);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<float2*>(wC + (pc * VE + e + j) * RB2 + col) = make_float2(v[j], v[j]);
+                for (int j = 0; j < 4; ++j) wC[(pc * VE + e + j) * RB + col] = v[j];
             }
         }
     }
@@ -253,7 +251,7 @@ template <typename T, int NS, int P, bool LOAD_C>
 __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* wk, long long b,
                                                   long long d0, long long t0, long long t_end, int tid) {
     using Cfg = FwdCfg<T, NS, P>;
-    constexpr int DT = Cfg::DT, TC = Cfg::TC, UROW = Cfg::UROW, RB2 = Cfg::RB2, GS2 = Cfg::GS2;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, UROW = Cfg::UROW, RB = Cfg::RB, GS = Cfg::GS;
     const T* gu = static_cast<const T*>(p.u);
     const T* gd = static_cast<const T*>(p.delta);
     const T* gB = static_cast<const T*>(p.B);
@@ -276,13 +274,9 @@ __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* wk,
         const long long t = t0 + tt;
         const bool ok = t < t_end;
         const long long off = (b * p.N + n) * p.L + t;
-        const int col = dup_col<NS, GS2>(n);
-        const float vb = ok ? to_f32(gB[off]) : 0.f;
-        *reinterpret_cast<float2*>(wB + tt * RB2 + col) = make_float2(vb, vb);
-        if (LOAD_C) {
-            const float vc = ok ? to_f32(gC[off]) : 0.f;
-            *reinterpret_cast<float2*>(wC + tt * RB2 + col) = make_float2(vc, vc);
-        }
+        const int col = work_col<NS, GS>(n);
+        wB[tt * RB + col] = ok ? to_f32(gB[off]) : 0.f;
+        if (LOAD_C) wC[tt * RB + col] = ok ? to_f32(gC[off]) : 0.f;
     }
 }
 
@@ -358,18 +352,20 @@ __device__ __forceinline__ void reduce_write4(const float (&y)[4], int g, T* yro
 }
 
 // One chunk of the recurrence for the calling lane: channel pair pr (rows 2pr,
-// 2pr+1 of the tile), states n = g*NS + k; each float2 holds the two channels.
-// SCALAR: every state of a channel shares one decay rate (one exponent per
-// channel and step).  Returns the chunk's sum of delta (both channels) when DSUM.
+// 2pr+1 of the tile), states n = g*NS + k; .x / .y of every float2 hold the
+// two channels.  Arithmetic is scalar FP32 (on this part two scalar FFMAs
+// outrun one packed f32x2 FFMA).  SCALAR: every state of a channel shares one
+// decay rate (one exponent per channel and step).  Returns the chunk's sum of
+// delta (both channels) when DSUM.
 template <typename T, int NS, int P, bool WRITE_Y, bool SCALAR, bool DSUM>
 __device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, int g,
                                                 const float2 (&A2)[NS], float2 As2,
                                                 float2 (&h2)[NS], float2 D2) {
     using Cfg = FwdCfg<T, NS, P>;
-    constexpr int TC = Cfg::TC, UROW = Cfg::UROW, RB2 = Cfg::RB2, GS2 = Cfg::GS2, RROW = Cfg::RROW;
+    constexpr int TC = Cfg::TC, UROW = Cfg::UROW, RB = Cfg::RB, GS = Cfg::GS, RROW = Cfg::RROW;
     const float* wu = wk + pr * UROW;
     const float* wd = wk + Cfg::UW_FLOATS + pr * UROW;
-    const float* wB = wk + 2 * Cfg::UW_FLOATS + g * GS2;
+    const float* wB = wk + 2 * Cfg::UW_FLOATS + g * GS;
     const float* wC = wB + Cfg::BW_FLOATS;
     T* yrow0 = yb + (2 * pr) * RROW;
     T* yrow1 = yrow0 + RROW;
@@ -384,47 +380,41 @@ __device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, 
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int t = t4 + jj + hf;
-                const float2 u2 = hf ? make_float2(u4.z, u4.w) : make_float2(u4.x, u4.y);
-                const float2 d2 = hf ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-                if (DSUM) csum = __fadd2_rn(csum, d2);
-                const float2 du2 = __fmul2_rn(d2, u2);
-                float2 a2s;
-                if (SCALAR) {
-                    const float2 xs = __fmul2_rn(d2, As2);
-                    a2s = make_float2(ex2(xs.x), ex2(xs.y));
-                }
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-                if (WRITE_Y && g == 0) acc0 = __fmul2_rn(D2, u2);
-                const float* brow = wB + t * RB2;
-                const float* crow = wC + t * RB2;
+                const float ux = hf ? u4.z : u4.x, uy = hf ? u4.w : u4.y;
+                const float dx = hf ? d4.z : d4.x, dy = hf ? d4.w : d4.y;
+                if (DSUM) { csum.x += dx; csum.y += dy; }
+                const float dux = dx * ux, duy = dy * uy;
+                float asx = 0.f, asy = 0.f;
+                if (SCALAR) { asx = ex2(dx * As2.x); asy = ex2(dy * As2.y); }
+                float ax0 = 0.f, ay0 = 0.f, ax1 = 0.f, ay1 = 0.f;
+                if (WRITE_Y && g == 0) { ax0 = D2.x * ux; ay0 = D2.y * uy; }
+                const float* brow = wB + t * RB;
+                const float* crw = wC + t * RB;
 #pragma unroll
-                for (int kq = 0; kq < NS / 2; ++kq) {
+                for (int kq = 0; kq < NS / 4; ++kq) {
                     const float4 b4 = *reinterpret_cast<const float4*>(brow + 4 * kq);
-                    float4 c4;
-                    if (WRITE_Y) c4 = *reinterpret_cast<const float4*>(crow + 4 * kq);
+                    const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+                    float cv[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (WRITE_Y) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(crw + 4 * kq);
+                        cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
+                    }
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = 2 * kq + e;
-                        float2 a2;
-                        if (SCALAR) {
-                            a2 = a2s;
-                        } else {
-                            const float2 x2 = __fmul2_rn(d2, A2[k]);
-                            a2 = make_float2(ex2(x2.x), ex2(x2.y));
-                        }
-                        const float2 bb = e ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-                        h2[k] = __ffma2_rn(a2, h2[k], __fmul2_rn(du2, bb));
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * kq + e;
+                        const float ex = SCALAR ? asx : ex2(dx * A2[k].x);
+                        const float ey = SCALAR ? asy : ex2(dy * A2[k].y);
+                        h2[k].x = fmaf(ex, h2[k].x, dux * bv[e]);
+                        h2[k].y = fmaf(ey, h2[k].y, duy * bv[e]);
                         if (WRITE_Y) {
-                            const float2 cc = e ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
-                            if (e) acc1 = __ffma2_rn(cc, h2[k], acc1);
-                            else acc0 = __ffma2_rn(cc, h2[k], acc0);
+                            if (e & 1) { ax1 = fmaf(cv[e], h2[k].x, ax1); ay1 = fmaf(cv[e], h2[k].y, ay1); }
+                            else { ax0 = fmaf(cv[e], h2[k].x, ax0); ay0 = fmaf(cv[e], h2[k].y, ay0); }
                         }
                     }
                 }
                 if (WRITE_Y) {
-                    const float2 yy = __fadd2_rn(acc0, acc1);
-                    y0[jj + hf] = yy.x;
-                    y1[jj + hf] = yy.y;
+                    y0[jj + hf] = ax0 + ax1;
+                    y1[jj + hf] = ay0 + ay1;
                 }
             }
         }
@@ -439,7 +429,7 @@ __device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, 
 template <typename T, int NS, int P, bool VEC>
 __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(const FwdParams p) {
     using Cfg = FwdCfg<T, NS, P>;
-    constexpr int DT = Cfg::DT, TC = Cfg::TC, RB2 = Cfg::RB2, GS2 = Cfg::GS2, NSP = Cfg::NSP;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, RB = Cfg::RB, GS = Cfg::GS, NSP = Cfg::NSP;
     constexpr int STAGES = Cfg::STAGES;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -506,7 +496,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
         }
     }
 
-    // duplicated B/C columns of state slots >= N stay zero for the whole kernel
+    // B/C columns of state slots >= N stay zero for the whole kernel
     if ((int)p.N < NSP) {
         const int nz = NSP - (int)p.N;
         for (int q = tid; q < 2 * 2 * TC * nz; q += Cfg::kThreads) {
@@ -514,7 +504,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
             const int row = q / nz;  // [buf][B|C][t]
             const int buf = row / (2 * TC), rr = row % (2 * TC);
             float* wbase = sm.work + buf * Cfg::WORK_FLOATS + 2 * Cfg::UW_FLOATS;
-            *reinterpret_cast<float2*>(wbase + rr * RB2 + dup_col<NS, GS2>(n)) = make_float2(0.f, 0.f);
+            wbase[rr * RB + work_col<NS, GS>(n)] = 0.f;
         }
     }
 
