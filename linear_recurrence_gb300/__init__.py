@@ -56,13 +56,14 @@ class SscanError(RuntimeError):
 
 def load_library(path: str | None = None):
     """Load libsscan.so (building it first if this tree has sources but no
-    library).  Raises if it cannot be loaded."""
+    library).  ``path``, else the SSCAN_LIBRARY environment variable, selects
+    another build of the library.  Raises if it cannot be loaded."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or LIB_PATH
-        if path is None and not os.path.exists(p):
+        p = path or os.environ.get("SSCAN_LIBRARY") or LIB_PATH
+        if p == LIB_PATH and not os.path.exists(p):
             from ._build import build
             build()
         if not os.path.exists(p):

@@ -149,14 +149,18 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     const long long tiles = batch * tiles_per_batch;
     if (tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
 
-    // time split: enough CTAs to fill every SM, each segment >= 8 chunks
+    // time split: about two CTAs per SM (measured best on GB300 for the
+    // few-channel workloads), each segment at least 8 chunks long
     long long S = segments;
     if (S == 0) {
         const int nsm = sm_count();
         const int occ = dtype == SSCAN_F32 ? sscan::fwd_occupancy_f32(sh, vec)
                                            : sscan::fwd_occupancy_bf16(sh, vec);
-        const long long target = (long long)std::max(nsm, 1) * std::max(occ, 1);
-        S = tiles >= target ? 1 : ceil_div(target, tiles);
+        // fp32 splits cost a short carry pass; bf16 splits re-run every segment,
+        // so bf16 splits only when there are fewer tiles than SMs
+        const long long per_sm = dtype == SSCAN_F32 ? std::min(std::max(occ, 1), 2) : 1;
+        const long long target = (long long)std::max(nsm, 1) * per_sm;
+        S = tiles >= target ? 1 : ceil_div((long long)std::max(nsm, 1) * std::min(std::max(occ, 1), 2), tiles);
         S = std::min(S, std::max(1LL, seqlen / (8LL * TC)));
     }
     S = std::max(1LL, std::min(S, ceil_div(seqlen, TC)));
@@ -197,7 +201,11 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
         p.mode = sscan::MODE_LOCAL;
         p.seg_count = (int)S;
         e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles * S, st);
-        if (e == cudaSuccess) e = launch_fwd(dtype, FwdKernel::Correct, p, sh, vec, tiles * (S - 1), st);
+        if (e == cudaSuccess) {
+            p.mode = sscan::MODE_CORR;
+            p.seg_count = (int)(S - 1);
+            e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
+        }
     } else {
         // bf16 output is written once: aggregates first, then every segment from
         // its exact entry state

@@ -17,7 +17,7 @@ struct Shape {
 constexpr Shape kShapes[] = {{1, 4}, {1, 8}, {1, 16}, {2, 4}, {2, 8}, {4, 4}, {4, 8}, {4, 16}};
 constexpr int kMaxDstate = 64;
 
-enum class FwdKernel { Chunked, Correct };
+enum class FwdKernel { Chunked };
 
 // Per-dtype entry points (defined in sscan_fwd_f32.cu / sscan_fwd_bf16.cu).
 // launch: enqueue one kernel on `stream`; returns the launch error, or
@@ -31,17 +31,15 @@ int fwd_occupancy_f32(Shape sh, bool vec);
 int fwd_occupancy_bf16(Shape sh, bool vec);
 // Channels per CTA and steps per chunk of a shape.
 inline int fwd_channels_per_cta(Shape sh) { return 2 * 2 * (32 / sh.P); }
-constexpr int kChunkSteps = 16;
+// Time segments are multiples of this many steps (a multiple of every shape's chunk).
+constexpr int kChunkSteps = 32;
 
 // Shared implementation, included by the per-dtype translation units only.
 #ifdef SSCAN_DISPATCH_IMPL
 template <typename T, int NS, int P, bool VEC>
 static cudaError_t launch_variant(FwdKernel k, const FwdParams& p, int grid, cudaStream_t stream) {
     using Cfg = FwdCfg<T, NS, P>;
-    if (k == FwdKernel::Correct) {
-        sscan_fwd_correct<T, NS, P, VEC><<<grid, Cfg::kCorrThreads, 0, stream>>>(p);
-        return cudaGetLastError();
-    }
+    (void)k;
     auto kern = sscan_fwd_chunked<T, NS, P, VEC>;
     // opting in to more than 48 KB of dynamic shared memory is per device
     static unsigned long long configured = 0;  // bit per device ordinal (< 64)

@@ -37,10 +37,15 @@ namespace sscan {
 enum FwdMode : int {
     MODE_SINGLE = 0,  // one segment: start from h0, write y and final_state
     MODE_LOCAL = 1,   // segment s starts from h0 (s = 0) or 0; write y and the
-                      // segment aggregate; the correction kernel adds the carry
+                      // segment aggregate; a MODE_CORR launch adds the carry
     MODE_AGG = 2,     // like MODE_LOCAL but only the aggregate (no y)
-    MODE_FOLD = 3     // segment s starts from the fold of segments < s; write y;
+    MODE_FOLD = 3,    // segment s starts from the fold of segments < s; write y;
                       // the last segment writes final_state
+    MODE_CORR = 4     // after MODE_LOCAL: segment s >= 1 adds the decaying carry of
+                      // its entry state to the outputs already written (read back
+                      // through the u slot), until the carry has decayed below
+                      // 2^-24 of its entry magnitude; the last segment writes
+                      // final_state
 };
 
 struct FwdParams {
@@ -65,6 +70,12 @@ struct FwdParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+#ifndef SSCAN_STEP_UNROLL
+#define SSCAN_STEP_UNROLL 8
+#endif
+// Steps per unrolled iteration of the inner loop (a multiple of 4).
+constexpr int kStepUnroll = SSCAN_STEP_UNROLL;
+
 template <typename T, int NS_, int P_>
 struct FwdCfg {
     static constexpr int NS = NS_;
@@ -75,11 +86,11 @@ struct FwdCfg {
     static constexpr int CPW = 2 * PPW;               // channels per warp
     static constexpr int DT = kWarps * CPW;           // channels per CTA
     static constexpr int NSP = NS * P;                // state slots per channel
-    static constexpr int TC = 16;                     // steps per chunk
+    static constexpr int TC = (DT > 64) ? 16 : 32;    // steps per chunk
     static constexpr int VECE = 16 / (int)sizeof(T);  // elements per 16 bytes
     static constexpr int RROW = TC + VECE;            // raw smem row (T), padded by 16 B
     static constexpr int PPR = TC / VECE;             // 16-byte pieces per raw row
-    static constexpr int UROW = 2 * TC + 4;           // interleaved u/delta row (fp32)
+    static constexpr int UROW = 2 * TC + 4;           // interleaved u/delta row of a channel pair
     static constexpr int GS = NS + ((P == 4 && NS >= 16) ? 4 : 0);  // floats per state group
     static constexpr int RB = P * GS;                 // floats per B/C work row (one step)
     static constexpr int RAW_ELEMS = (2 * DT + 2 * NSP) * RROW;
@@ -90,10 +101,9 @@ struct FwdCfg {
     static constexpr int Y_ELEMS = DT * RROW;
     static constexpr int FIXED_BYTES = 2 * WORK_FLOATS * 4 + 2 * Y_ELEMS * (int)sizeof(T);
     static constexpr int STAGES = (RAW_BYTES * 4 + FIXED_BYTES <= 48 * 1024) ? 4
-                                  : (RAW_BYTES * 3 + FIXED_BYTES <= 96 * 1024) ? 3
+                                  : (RAW_BYTES * 3 + FIXED_BYTES <= 72 * 1024) ? 3
                                                                                : 2;
     static constexpr int SMEM_BYTES = STAGES * RAW_BYTES + FIXED_BYTES;
-    static constexpr int kCorrThreads = 2 * kThreads;  // correction kernel: a lane per (channel, group)
     static_assert(32 % P == 0, "lanes per channel must divide the warp");
     static_assert(NS % 4 == 0, "state slots are read 4 at a time");
     static_assert(TC % VECE == 0 && TC % 4 == 0, "chunk must hold whole vectors");
@@ -130,8 +140,8 @@ __device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, 
 //                      (type T, copied verbatim from global by cp.async)
 //   work [2]:          u, delta [DT/2][UROW]: the two channels of a pair interleaved
 //                        per step (u0[t], u1[t], u0[t+1], ...), fp32;
-//                      B, C [TC][RB]: transposed so that a lane's NS states at
-//                        one step are contiguous, group g at g*GS, fp32
+//                      B, C [TC][RB]: fp32, transposed so that a lane's NS states at
+//                        one step are contiguous, group g at g*GS
 //   ybuf [2]:          y [DT][RROW] (type T)
 template <typename T, int NS, int P>
 struct Smem {
@@ -155,7 +165,7 @@ __device__ __forceinline__ int work_col(int n) { return (n / NS) * GS + (n % NS)
 // VEC path, step 1: issue this thread's 16-byte cp.async pieces of chunk [t0, t0+TC).
 // A thread owns the same piece of both rows of a channel pair, and whole B/C
 // pieces.  Out-of-range pieces are zero-filled (delta = 0 keeps the state).
-template <typename T, int NS, int P, bool LOAD_C>
+template <typename T, int NS, int P, bool LOAD_C, bool LOAD_B = true>
 __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long b, long long d0,
                                             long long t0, long long t_end, int tid) {
     using Cfg = FwdCfg<T, NS, P>;
@@ -187,16 +197,16 @@ __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long
         const long long t = t0 + (long long)pc * VE;
         const bool ok = t < t_end;
         const long long off = (b * p.N + n) * p.L + (ok ? t : 0);
-        cp_async16(sB + n * RROW + pc * VE, gB + off, ok ? 16 : 0);
+        if (LOAD_B) cp_async16(sB + n * RROW + pc * VE, gB + off, ok ? 16 : 0);
         if (LOAD_C) cp_async16(sC + n * RROW + pc * VE, gC + off, ok ? 16 : 0);
     }
 }
 
 // VEC path, step 2 (after this thread's copies of the chunk landed): widen the
 // pieces this same thread copied into the fp32 work tiles (u/delta interleaved
-// by channel pair, B/C transposed and duplicated).  Only own pieces are
-// touched, so no barrier is needed between the copy and the conversion.
-template <typename T, int NS, int P, bool LOAD_C>
+// by channel pair, B/C transposed).  Only own pieces are touched, so no barrier
+// is needed between the copy and the conversion.
+template <typename T, int NS, int P, bool LOAD_C, bool LOAD_B = true>
 __device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* st, float* wk, int tid) {
     using Cfg = FwdCfg<T, NS, P>;
     constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
@@ -212,18 +222,18 @@ __device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* 
     for (int q = tid; q < (DT / 2) * PPR; q += Cfg::kThreads) {
         const int pr = q / PPR, pc = q % PPR;
 #pragma unroll
-        for (int e = 0; e < VE; e += 2) {
-            // two steps of both channels -> one 16-byte store per array
+        for (int e = 0; e < VE; e += 4) {
             float a0[4], a1[4];
-            load4_smem(su + (2 * pr) * RROW + pc * VE + (e & ~3), a0);
-            load4_smem(su + (2 * pr + 1) * RROW + pc * VE + (e & ~3), a1);
-            const int o = e & 3;
-            *reinterpret_cast<float4*>(wu + pr * UROW + 2 * (pc * VE + e)) =
-                make_float4(a0[o], a1[o], a0[o + 1], a1[o + 1]);
-            load4_smem(sd + (2 * pr) * RROW + pc * VE + (e & ~3), a0);
-            load4_smem(sd + (2 * pr + 1) * RROW + pc * VE + (e & ~3), a1);
-            *reinterpret_cast<float4*>(wd + pr * UROW + 2 * (pc * VE + e)) =
-                make_float4(a0[o], a1[o], a0[o + 1], a1[o + 1]);
+            load4_smem(su + (2 * pr) * RROW + pc * VE + e, a0);
+            load4_smem(su + (2 * pr + 1) * RROW + pc * VE + e, a1);
+            float* o = wu + pr * UROW + 2 * (pc * VE + e);
+            *reinterpret_cast<float4*>(o) = make_float4(a0[0], a1[0], a0[1], a1[1]);
+            *reinterpret_cast<float4*>(o + 4) = make_float4(a0[2], a1[2], a0[3], a1[3]);
+            load4_smem(sd + (2 * pr) * RROW + pc * VE + e, a0);
+            load4_smem(sd + (2 * pr + 1) * RROW + pc * VE + e, a1);
+            o = wd + pr * UROW + 2 * (pc * VE + e);
+            *reinterpret_cast<float4*>(o) = make_float4(a0[0], a1[0], a0[1], a1[1]);
+            *reinterpret_cast<float4*>(o + 4) = make_float4(a0[2], a1[2], a0[3], a1[3]);
         }
     }
     const int N = (int)p.N;
@@ -233,9 +243,11 @@ __device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* 
 #pragma unroll
         for (int e = 0; e < VE; e += 4) {
             float v[4];
-            load4_smem(sB + n * RROW + pc * VE + e, v);
+            if (LOAD_B) {
+                load4_smem(sB + n * RROW + pc * VE + e, v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wB[(pc * VE + e + j) * RB + col] = v[j];
+                for (int j = 0; j < 4; ++j) wB[(pc * VE + e + j) * RB + col] = v[j];
+            }
             if (LOAD_C) {
                 load4_smem(sC + n * RROW + pc * VE + e, v);
 #pragma unroll
@@ -247,7 +259,7 @@ __device__ __forceinline__ void convert_own_pieces(const FwdParams& p, const T* 
 
 // Non-VEC path (rows not 16-byte aligned): synchronous element loads with bounds
 // checks straight into the fp32 work tiles.
-template <typename T, int NS, int P, bool LOAD_C>
+template <typename T, int NS, int P, bool LOAD_C, bool LOAD_B = true>
 __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* wk, long long b,
                                                   long long d0, long long t0, long long t_end, int tid) {
     using Cfg = FwdCfg<T, NS, P>;
@@ -275,7 +287,7 @@ __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* wk,
         const bool ok = t < t_end;
         const long long off = (b * p.N + n) * p.L + t;
         const int col = work_col<NS, GS>(n);
-        wB[tt * RB + col] = ok ? to_f32(gB[off]) : 0.f;
+        if (LOAD_B) wB[tt * RB + col] = ok ? to_f32(gB[off]) : 0.f;
         if (LOAD_C) wC[tt * RB + col] = ok ? to_f32(gC[off]) : 0.f;
     }
 }
@@ -334,93 +346,119 @@ __device__ __forceinline__ void reduce4(const float (&y)[4], int g, float (&v)[4
     }
 }
 
-// Reduce-scatter one channel's 4 partial outputs and write the lane's share
-// into its staged output row (yrow points at the first of the 4 steps).
+// Reduce-scatter one channel's 4 partial outputs, add the skip term D*u once
+// (by the lane that owns each step), and write the lane's share of the staged
+// output row (yrow points at the first of the 4 steps).
 template <typename T, int P>
-__device__ __forceinline__ void reduce_write4(const float (&y)[4], int g, T* yrow) {
+__device__ __forceinline__ void reduce_write4(const float (&y)[4], const float (&u)[4], float Dd, int g,
+                                              T* yrow) {
     float v[4];
     reduce4<P>(y, g, v);
     if constexpr (P == 4) {
-        yrow[g] = from_f32<T>(v[0]);
+        const float ug = (g & 2) ? ((g & 1) ? u[3] : u[2]) : ((g & 1) ? u[1] : u[0]);
+        yrow[g] = from_f32<T>(fmaf(Dd, ug, v[0]));
     } else if constexpr (P == 2) {
-        yrow[2 * g] = from_f32<T>(v[0]);
-        yrow[2 * g + 1] = from_f32<T>(v[1]);
+        const float u0 = g ? u[2] : u[0], u1 = g ? u[3] : u[1];
+        yrow[2 * g] = from_f32<T>(fmaf(Dd, u0, v[0]));
+        yrow[2 * g + 1] = from_f32<T>(fmaf(Dd, u1, v[1]));
     } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) yrow[j] = from_f32<T>(v[j]);
+        for (int j = 0; j < 4; ++j) yrow[j] = from_f32<T>(fmaf(Dd, u[j], v[j]));
     }
 }
 
 // One chunk of the recurrence for the calling lane: channel pair pr (rows 2pr,
-// 2pr+1 of the tile), states n = g*NS + k; .x / .y of every float2 hold the
-// two channels.  Arithmetic is scalar FP32 (on this part two scalar FFMAs
-// outrun one packed f32x2 FFMA).  SCALAR: every state of a channel shares one
-// decay rate (one exponent per channel and step).  Returns the chunk's sum of
-// delta (both channels) when DSUM.
-template <typename T, int NS, int P, bool WRITE_Y, bool SCALAR, bool DSUM>
+// 2pr+1 of the tile; index e below), states n = g*NS + k.  Each B/C value read
+// from shared memory serves both channels of the pair.  Software-pipelined:
+// step t+1's loads and exponentials are issued before step t's state updates,
+// so the dependent FMA chain overlaps independent work.  Arithmetic is scalar
+// FP32 (on this part two scalar FFMAs outrun one packed f32x2 FFMA).  SCALAR:
+// every state of a channel shares its decay rate (one exponent per channel and
+// step).  Returns the chunk's sum of delta per channel when DSUM.  NO_B: the
+// homogeneous recurrence h = a*h (the carry correction), B is not read.
+template <typename T, int NS, int P, bool WRITE_Y, bool SCALAR, bool DSUM, bool NO_B = false>
 __device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, int g,
-                                                const float2 (&A2)[NS], float2 As2,
-                                                float2 (&h2)[NS], float2 D2) {
+                                                const float (&A)[2][NS], const float (&As)[2],
+                                                float (&h)[2][NS], const float (&Dd)[2]) {
     using Cfg = FwdCfg<T, NS, P>;
     constexpr int TC = Cfg::TC, UROW = Cfg::UROW, RB = Cfg::RB, GS = Cfg::GS, RROW = Cfg::RROW;
-    const float* wu = wk + pr * UROW;
-    const float* wd = wk + Cfg::UW_FLOATS + pr * UROW;
-    const float* wB = wk + 2 * Cfg::UW_FLOATS + g * GS;
-    const float* wC = wB + Cfg::BW_FLOATS;
+    const float* ur = wk + pr * UROW;
+    const float* dr = wk + Cfg::UW_FLOATS + pr * UROW;
+    const float* bb = wk + 2 * Cfg::UW_FLOATS + g * GS;
+    const float* cb = bb + Cfg::BW_FLOATS;
     T* yrow0 = yb + (2 * pr) * RROW;
     T* yrow1 = yrow0 + RROW;
+
+    float a_n[2][NS], du_n[2], u_n[2];
+    float4 b_n[NS / 4], c_n[NS / 4];
     float2 csum = make_float2(0.f, 0.f);
-#pragma unroll 1
-    for (int t4 = 0; t4 < TC; t4 += 4) {
-        float y0[4], y1[4];
+    auto fetch = [&](int t) {
+        const float2 u2 = *reinterpret_cast<const float2*>(ur + 2 * t);
+        const float2 d2 = *reinterpret_cast<const float2*>(dr + 2 * t);
+        if (DSUM) { csum.x += d2.x; csum.y += d2.y; }
+        u_n[0] = u2.x; u_n[1] = u2.y;
+        du_n[0] = d2.x * u2.x; du_n[1] = d2.y * u2.y;
 #pragma unroll
-        for (int jj = 0; jj < 4; jj += 2) {
-            const float4 u4 = *reinterpret_cast<const float4*>(wu + 2 * (t4 + jj));
-            const float4 d4 = *reinterpret_cast<const float4*>(wd + 2 * (t4 + jj));
+        for (int q = 0; q < NS / 4; ++q) {
+            if (!NO_B) b_n[q] = *reinterpret_cast<const float4*>(bb + t * RB + 4 * q);
+            if (WRITE_Y) c_n[q] = *reinterpret_cast<const float4*>(cb + t * RB + 4 * q);
+        }
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int t = t4 + jj + hf;
-                const float ux = hf ? u4.z : u4.x, uy = hf ? u4.w : u4.y;
-                const float dx = hf ? d4.z : d4.x, dy = hf ? d4.w : d4.y;
-                if (DSUM) { csum.x += dx; csum.y += dy; }
-                const float dux = dx * ux, duy = dy * uy;
-                float asx = 0.f, asy = 0.f;
-                if (SCALAR) { asx = ex2(dx * As2.x); asy = ex2(dy * As2.y); }
-                float ax0 = 0.f, ay0 = 0.f, ax1 = 0.f, ay1 = 0.f;
-                if (WRITE_Y && g == 0) { ax0 = D2.x * ux; ay0 = D2.y * uy; }
-                const float* brow = wB + t * RB;
-                const float* crw = wC + t * RB;
+        for (int e = 0; e < 2; ++e) {
+            const float dt = e ? d2.y : d2.x;
+            if (SCALAR) {
+                const float a = ex2(dt * As[e]);
 #pragma unroll
-                for (int kq = 0; kq < NS / 4; ++kq) {
-                    const float4 b4 = *reinterpret_cast<const float4*>(brow + 4 * kq);
-                    const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-                    float cv[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (WRITE_Y) {
-                        const float4 c4 = *reinterpret_cast<const float4*>(crw + 4 * kq);
-                        cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
-                    }
+                for (int k = 0; k < NS; ++k) a_n[e][k] = a;
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 4 * kq + e;
-                        const float ex = SCALAR ? asx : ex2(dx * A2[k].x);
-                        const float ey = SCALAR ? asy : ex2(dy * A2[k].y);
-                        h2[k].x = fmaf(ex, h2[k].x, dux * bv[e]);
-                        h2[k].y = fmaf(ey, h2[k].y, duy * bv[e]);
-                        if (WRITE_Y) {
-                            if (e & 1) { ax1 = fmaf(cv[e], h2[k].x, ax1); ay1 = fmaf(cv[e], h2[k].y, ay1); }
-                            else { ax0 = fmaf(cv[e], h2[k].x, ax0); ay0 = fmaf(cv[e], h2[k].y, ay0); }
-                        }
-                    }
-                }
-                if (WRITE_Y) {
-                    y0[jj + hf] = ax0 + ax1;
-                    y1[jj + hf] = ay0 + ay1;
-                }
+                for (int k = 0; k < NS; ++k) a_n[e][k] = ex2(dt * A[e][k]);
             }
         }
+    };
+    fetch(0);
+    float y[2][4], uu[2][4];
+#pragma unroll kStepUnroll
+    for (int t = 0; t < TC; ++t) {
+        float a_c[2][NS], du_c[2];
+        float4 b_c[NS / 4], c_c[NS / 4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            du_c[e] = du_n[e];
+            uu[e][t & 3] = u_n[e];
+#pragma unroll
+            for (int k = 0; k < NS; ++k) a_c[e][k] = a_n[e][k];
+        }
+#pragma unroll
+        for (int q = 0; q < NS / 4; ++q) {
+            if (!NO_B) b_c[q] = b_n[q];
+            if (WRITE_Y) c_c[q] = c_n[q];
+        }
+        if (t + 1 < TC) fetch(t + 1);
+        float acc[2] = {0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < NS / 4; ++q) {
+            float bv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (!NO_B) { bv[0] = b_c[q].x; bv[1] = b_c[q].y; bv[2] = b_c[q].z; bv[3] = b_c[q].w; }
+            float cv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (WRITE_Y) { cv[0] = c_c[q].x; cv[1] = c_c[q].y; cv[2] = c_c[q].z; cv[3] = c_c[q].w; }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 4 * q + j;
+                    if (NO_B) h[e][k] = a_c[e][k] * h[e][k];
+                    else h[e][k] = fmaf(a_c[e][k], h[e][k], du_c[e] * bv[j]);
+                    if (WRITE_Y) acc[e] = fmaf(cv[j], h[e][k], acc[e]);
+                }
+        }
         if (WRITE_Y) {
-            reduce_write4<T, P>(y0, g, yrow0 + t4);
-            reduce_write4<T, P>(y1, g, yrow1 + t4);
+            y[0][t & 3] = acc[0];
+            y[1][t & 3] = acc[1];
+            if ((t & 3) == 3) {
+                reduce_write4<T, P>(y[0], uu[0], Dd[0], g, yrow0 + (t & ~3));
+                reduce_write4<T, P>(y[1], uu[1], Dd[1], g, yrow1 + (t & ~3));
+            }
         }
     }
     return csum;
@@ -438,8 +476,9 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane % P;
     const int pr = w * Cfg::PPW + lane / P;  // channel pair within the tile
+    const bool corr = p.mode == MODE_CORR;
     const int tile = blockIdx.x / p.seg_count;
-    const int s = blockIdx.x % p.seg_count;
+    const int s = (corr ? 1 : 0) + blockIdx.x % p.seg_count;
     const long long b = tile / p.tiles_per_batch;
     const long long d0 = (long long)(tile % p.tiles_per_batch) * DT;
     const long long t_begin = (long long)s * p.Tseg;
@@ -447,13 +486,15 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
     const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + TC - 1) / TC) : 0;
     const bool write_y = p.mode != MODE_AGG;
     const bool dsum_on = p.mode == MODE_LOCAL || p.mode == MODE_AGG;
+    // the correction reads back the local outputs through the u slot
+    FwdParams q = p;
+    if (corr) q.u = p.out;
 
     // the lane's two channels and their decay rates (A * log2 e); a warp whose
     // channels each have a single rate takes the one-exponent-per-step path
     long long dch[2], ch[2];
     bool dval[2];
-    float Al2[2][NS];
-    float2 As2, D2;
+    float A[2][NS], As[2], Dd[2], h[2][NS];
     bool uniform_rate = true;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -467,32 +508,46 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
             const bool nv = dval[e] && n < p.N;
             const float a = nv ? p.A[dch[e] * p.N + n] : a_first;
             uniform_rate &= (a == a_first);
-            Al2[e][k] = nv ? a * kLog2e : 0.f;
+            A[e][k] = nv ? a * kLog2e : 0.f;
         }
-        const float as = a_first * kLog2e;
-        const float dd = (p.D != nullptr && dval[e]) ? p.D[dch[e]] : 0.f;
-        if (e == 0) { As2.x = as; D2.x = dd; } else { As2.y = as; D2.y = dd; }
+        As[e] = a_first * kLog2e;
+        Dd[e] = corr ? 1.f : ((p.D != nullptr && dval[e]) ? p.D[dch[e]] : 0.f);
+        if ((p.mode == MODE_FOLD || corr) && s > 0) {
+            fold_segments<NS>(p, ch[e], s, g, A[e], h[e]);
+            if (!dval[e]) {
+#pragma unroll
+                for (int k = 0; k < NS; ++k) h[e][k] = 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const long long n = (long long)g * NS + k;
+                h[e][k] = (s == 0 && p.h0 != nullptr && dval[e] && n < p.N) ? p.h0[ch[e] * p.N + n] : 0.f;
+            }
+        }
     }
     const bool scalar = __all_sync(FULL, uniform_rate);
-    float2 A2[NS], h2[NS];
-    {
-        float hs[2][NS];
+
+    // correction: the last segment's final state is the carry decayed over the
+    // segment plus its local end state; the carry is followed until every
+    // state of the CTA has fallen below 2^-24 of its entry magnitude
+    float thr[2] = {0.f, 0.f};
+    if (corr) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            if (p.mode == MODE_FOLD && s > 0) {
-                fold_segments<NS>(p, ch[e], s, g, Al2[e], hs[e]);
-            } else {
+            float m = 0.f;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) m = fmaxf(m, fabsf(h[e][k]));
+            thr[e] = m * 0x1p-24f;
+            if (dval[e] && s == p.S - 1 && p.final_state != nullptr) {
+                const float ds = p.seg_dsum[ch[e] * p.S + s];
+                const float* sst = p.seg_state + (ch[e] * p.S + s) * p.N;
 #pragma unroll
                 for (int k = 0; k < NS; ++k) {
                     const long long n = (long long)g * NS + k;
-                    hs[e][k] = (s == 0 && p.h0 != nullptr && dval[e] && n < p.N) ? p.h0[ch[e] * p.N + n] : 0.f;
+                    if (n < p.N) p.final_state[ch[e] * p.N + n] = fmaf(ex2(A[e][k] * ds), h[e][k], sst[n]);
                 }
             }
-        }
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            A2[k] = make_float2(Al2[0][k], Al2[1][k]);
-            h2[k] = make_float2(hs[0][k], hs[1][k]);
         }
     }
 
@@ -513,48 +568,65 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
 #pragma unroll
         for (int j = 0; j < STAGES - 1; ++j) {
             if (j < nchunks) {
-                if (write_y) issue_chunk<T, NS, P, true>(p, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
-                else issue_chunk<T, NS, P, false>(p, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
+                if (corr) issue_chunk<T, NS, P, true, false>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
+                else if (write_y) issue_chunk<T, NS, P, true>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
+                else issue_chunk<T, NS, P, false>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid);
             }
             cp_async_commit();
         }
         cp_async_wait<STAGES - 2>();
         if (nchunks > 0) {
-            if (write_y) convert_own_pieces<T, NS, P, true>(p, sm.stage(0), sm.wk(0), tid);
-            else convert_own_pieces<T, NS, P, false>(p, sm.stage(0), sm.wk(0), tid);
+            if (corr) convert_own_pieces<T, NS, P, true, false>(q, sm.stage(0), sm.wk(0), tid);
+            else if (write_y) convert_own_pieces<T, NS, P, true>(q, sm.stage(0), sm.wk(0), tid);
+            else convert_own_pieces<T, NS, P, false>(q, sm.stage(0), sm.wk(0), tid);
         }
     } else {
         if (nchunks > 0) {
-            if (write_y) load_chunk_scalar<T, NS, P, true>(p, sm.wk(0), b, d0, t_begin, t_end, tid);
-            else load_chunk_scalar<T, NS, P, false>(p, sm.wk(0), b, d0, t_begin, t_end, tid);
+            if (corr) load_chunk_scalar<T, NS, P, true, false>(q, sm.wk(0), b, d0, t_begin, t_end, tid);
+            else if (write_y) load_chunk_scalar<T, NS, P, true>(q, sm.wk(0), b, d0, t_begin, t_end, tid);
+            else load_chunk_scalar<T, NS, P, false>(q, sm.wk(0), b, d0, t_begin, t_end, tid);
         }
     }
 
     float2 dsum = make_float2(0.f, 0.f), dcomp = make_float2(0.f, 0.f);  // Kahan sums of delta
+    int done = 0;  // chunks computed (the correction may stop early)
     for (int i = 0; i < nchunks; ++i) {
-        __syncthreads();
+        if (corr) {
+            bool live = false;
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int k = 0; k < NS; ++k) live |= fabsf(h[e][k]) > thr[e];
+            if (!__syncthreads_or(live)) break;
+        } else {
+            __syncthreads();
+        }
         const long long t0 = t_begin + (long long)i * TC;
         if (write_y && i > 0) store_chunk<T, NS, P, VEC>(p, sm.yb(i - 1), b, d0, t0 - TC, t_end, tid);
         if constexpr (VEC) {
             const int nx = i + STAGES - 1;
             if (nx < nchunks) {
-                if (write_y) issue_chunk<T, NS, P, true>(p, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
-                else issue_chunk<T, NS, P, false>(p, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
+                if (corr) issue_chunk<T, NS, P, true, false>(q, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
+                else if (write_y) issue_chunk<T, NS, P, true>(q, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
+                else issue_chunk<T, NS, P, false>(q, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid);
             }
             cp_async_commit();
         }
         float2 csum = make_float2(0.f, 0.f);
-        if (write_y) {
+        if (corr) {
+            if (scalar) compute_chunk<T, NS, P, true, true, false, true>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
+            else compute_chunk<T, NS, P, true, false, false, true>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
+        } else if (write_y) {
             if (scalar) {
-                if (dsum_on) csum = compute_chunk<T, NS, P, true, true, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
-                else compute_chunk<T, NS, P, true, true, false>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+                if (dsum_on) csum = compute_chunk<T, NS, P, true, true, true>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
+                else compute_chunk<T, NS, P, true, true, false>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
             } else {
-                if (dsum_on) csum = compute_chunk<T, NS, P, true, false, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
-                else compute_chunk<T, NS, P, true, false, false>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+                if (dsum_on) csum = compute_chunk<T, NS, P, true, false, true>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
+                else compute_chunk<T, NS, P, true, false, false>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
             }
         } else {
-            if (scalar) csum = compute_chunk<T, NS, P, false, true, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
-            else csum = compute_chunk<T, NS, P, false, false, true>(sm.wk(i), sm.yb(i), pr, g, A2, As2, h2, D2);
+            if (scalar) csum = compute_chunk<T, NS, P, false, true, true>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
+            else csum = compute_chunk<T, NS, P, false, false, true>(sm.wk(i), sm.yb(i), pr, g, A, As, h, Dd);
         }
         if (dsum_on) {
             const float2 yk = make_float2(csum.x - dcomp.x, csum.y - dcomp.y);
@@ -562,145 +634,42 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P>::kThreads) sscan_fwd_chunked(
             dcomp = make_float2((tk.x - dsum.x) - yk.x, (tk.y - dsum.y) - yk.y);
             dsum = tk;
         }
+        done = i + 1;
         if (i + 1 < nchunks) {
             if constexpr (VEC) {
                 cp_async_wait<STAGES - 2>();
-                if (write_y) convert_own_pieces<T, NS, P, true>(p, sm.stage(i + 1), sm.wk(i + 1), tid);
-                else convert_own_pieces<T, NS, P, false>(p, sm.stage(i + 1), sm.wk(i + 1), tid);
+                if (corr) convert_own_pieces<T, NS, P, true, false>(q, sm.stage(i + 1), sm.wk(i + 1), tid);
+                else if (write_y) convert_own_pieces<T, NS, P, true>(q, sm.stage(i + 1), sm.wk(i + 1), tid);
+                else convert_own_pieces<T, NS, P, false>(q, sm.stage(i + 1), sm.wk(i + 1), tid);
             } else {
-                if (write_y) load_chunk_scalar<T, NS, P, true>(p, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
-                else load_chunk_scalar<T, NS, P, false>(p, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
+                if (corr) load_chunk_scalar<T, NS, P, true, false>(q, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
+                else if (write_y) load_chunk_scalar<T, NS, P, true>(q, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
+                else load_chunk_scalar<T, NS, P, false>(q, sm.wk(i + 1), b, d0, t0 + TC, t_end, tid);
             }
         }
     }
     cp_async_wait<0>();
     __syncthreads();
-    if (write_y && nchunks > 0)
-        store_chunk<T, NS, P, VEC>(p, sm.yb(nchunks - 1), b, d0, t_begin + (long long)(nchunks - 1) * TC, t_end, tid);
+    if (write_y && done > 0)
+        store_chunk<T, NS, P, VEC>(p, sm.yb(done - 1), b, d0, t_begin + (long long)(done - 1) * TC, t_end, tid);
+    if (corr) return;
 
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         if (!dval[e]) continue;
-        const float dse = e ? dsum.y : dsum.x;
         if (p.mode == MODE_LOCAL || p.mode == MODE_AGG) {
             float* sst = p.seg_state + (ch[e] * p.S + s) * p.N;
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
                 const long long n = (long long)g * NS + k;
-                if (n < p.N) sst[n] = e ? h2[k].y : h2[k].x;
+                if (n < p.N) sst[n] = h[e][k];
             }
-            if (g == 0) p.seg_dsum[ch[e] * p.S + s] = dse;
+            if (g == 0) p.seg_dsum[ch[e] * p.S + s] = e ? dsum.y : dsum.x;
         } else if (p.final_state != nullptr && (p.mode == MODE_SINGLE || s == p.S - 1)) {
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
                 const long long n = (long long)g * NS + k;
-                if (n < p.N) p.final_state[ch[e] * p.N + n] = e ? h2[k].y : h2[k].x;
-            }
-        }
-    }
-}
-
-// Global loads of 4 consecutive elements [t, t+4) of a row, widened to fp32;
-// elements at or beyond t_end read as zero.
-template <typename T, bool VEC>
-__device__ __forceinline__ void gload4(const T* row, long long t, long long t_end, float (&v)[4]) {
-    if constexpr (VEC) {
-        if constexpr (sizeof(T) == 4) {
-            const float4 q = __ldg(reinterpret_cast<const float4*>(row + t));
-            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-        } else {
-            const uint2 q = __ldg(reinterpret_cast<const uint2*>(row + t));
-            v[0] = __uint_as_float(q.x << 16);
-            v[1] = __uint_as_float(q.x & 0xffff0000u);
-            v[2] = __uint_as_float(q.y << 16);
-            v[3] = __uint_as_float(q.y & 0xffff0000u);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = (t + j < t_end) ? to_f32(row[t + j]) : 0.f;
-    }
-}
-
-// Carry correction for segments s >= 1 after a MODE_LOCAL pass: with h_in the
-// state entering the segment, h_t = P_t h_in + h_t(local) where P_t is the
-// running product of the decays, so y_t gains sum_n C[b,n,t] P_t[n] h_in[n].
-// The homogeneous state g = P_t h_in is advanced step by step until every
-// lane's g has decayed to exactly zero (or the segment ends), and the last
-// segment writes final_state = 2^(A log2e sum(delta)) h_in + h_end(local).
-template <typename T, int NS, int P, bool VEC>
-__global__ void __launch_bounds__(FwdCfg<T, NS, P>::kCorrThreads) sscan_fwd_correct(const FwdParams p) {
-    using Cfg = FwdCfg<T, NS, P>;
-    constexpr int DT = Cfg::DT, TC = Cfg::TC;
-    constexpr unsigned FULL = 0xffffffffu;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int c = lane / P, g = lane % P;
-    const int crow = w * (32 / P) + c;  // kCorrThreads lanes cover the DT channels of a tile
-    const int segs = p.S - 1;
-    const int tile = blockIdx.x / segs;
-    const int s = 1 + blockIdx.x % segs;
-    const long long b = tile / p.tiles_per_batch;
-    const long long d = (long long)(tile % p.tiles_per_batch) * DT + crow;
-    const bool dval = d < p.dim;
-    const long long ch = b * p.dim + (dval ? d : 0);
-    const long long t_begin = (long long)s * p.Tseg;
-    const long long t_end = min(p.L, t_begin + p.Tseg);
-
-    float Al2[NS], gst[NS];
-#pragma unroll
-    for (int k = 0; k < NS; ++k) {
-        const long long n = (long long)g * NS + k;
-        Al2[k] = (dval && n < p.N) ? p.A[d * p.N + n] * kLog2e : 0.f;
-    }
-    fold_segments<NS>(p, ch, s, g, Al2, gst);
-    if (!dval) {
-#pragma unroll
-        for (int k = 0; k < NS; ++k) gst[k] = 0.f;
-    }
-    if (dval && s == p.S - 1 && p.final_state != nullptr) {
-        const float dsum = p.seg_dsum[ch * p.S + s];
-        const float* sst = p.seg_state + (ch * p.S + s) * p.N;
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            const long long n = (long long)g * NS + k;
-            if (n < p.N) p.final_state[ch * p.N + n] = fmaf(ex2(Al2[k] * dsum), gst[k], sst[n]);
-        }
-    }
-
-    const T* drow = static_cast<const T*>(p.delta) + ch * p.L;
-    const T* Cb = static_cast<const T*>(p.C) + b * p.N * p.L;
-    T* orow = static_cast<T*>(p.out) + ch * p.L;
-    for (long long tc = t_begin; tc < t_end; tc += TC) {
-        bool live = false;
-#pragma unroll
-        for (int k = 0; k < NS; ++k) live |= (gst[k] != 0.f);
-        if (!__any_sync(FULL, live)) break;
-        for (long long t = tc; t < min(tc + TC, t_end); t += 4) {
-            float dd[4];
-            gload4<T, VEC>(drow, t, t_end, dd);
-            float yv[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < NS; ++k) {
-                const long long n = (long long)g * NS + k;
-                float cc[4] = {0.f, 0.f, 0.f, 0.f};
-                if (n < p.N) gload4<T, VEC>(Cb + n * p.L, t, t_end, cc);
-                float gv = gst[k];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    gv *= ex2(dd[j] * Al2[k]);
-                    yv[j] = fmaf(cc[j], gv, yv[j]);
-                }
-                gst[k] = gv;
-            }
-            float v[4];
-            reduce4<P>(yv, g, v);
-            if (dval) {
-                constexpr int NOWN = (P == 4) ? 1 : ((P == 2) ? 2 : 4);
-                const long long tt0 = t + (P == 4 ? g : (P == 2 ? 2 * g : 0));
-#pragma unroll
-                for (int j = 0; j < NOWN; ++j) {
-                    const long long tt = tt0 + j;
-                    if (tt < t_end) orow[tt] = from_f32<T>(to_f32(orow[tt]) + v[j]);
-                }
+                if (n < p.N) p.final_state[ch[e] * p.N + n] = h[e][k];
             }
         }
     }

@@ -119,8 +119,9 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
             return SSCAN_ERR_CUDA;
         const int occ = dtype == SSCAN_F32 ? sscan::fwd_occupancy_f32(sh, vec)
                                            : sscan::fwd_occupancy_bf16(sh, vec);
-        const long long target = (long long)std::max(nsm, 1) * std::max(occ, 1);
-        S = tiles >= target ? 1 : cdiv(target, tiles);
+        const long long per_sm = dtype == SSCAN_F32 ? std::min(std::max(occ, 1), 2) : 1;
+        const long long target = (long long)std::max(nsm, 1) * per_sm;
+        S = tiles >= target ? 1 : cdiv((long long)std::max(nsm, 1) * std::min(std::max(occ, 1), 2), tiles);
         S = std::min(S, std::max(1LL, seqlen / (8LL * TC)));
         S = std::min(S, std::max(1LL, max_segments));  // automatic plans shrink to the array
     }
@@ -152,7 +153,11 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
         p.mode = sscan::MODE_LOCAL;
         p.seg_count = (int)S;
         e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * S, st);
-        if (e == cudaSuccess) e = launch(dtype, sscan::FwdKernel::Correct, p, sh, vec, tiles * (S - 1), st);
+        if (e == cudaSuccess) {
+            p.mode = sscan::MODE_CORR;
+            p.seg_count = (int)(S - 1);
+            e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
+        }
     } else {
         p.mode = sscan::MODE_AGG;
         p.seg_count = (int)(S - 1);
