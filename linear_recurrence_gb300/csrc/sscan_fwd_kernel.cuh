@@ -75,6 +75,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 #endif
 // Steps per unrolled iteration of the inner loop (a multiple of 4).
 constexpr int kStepUnroll = SSCAN_STEP_UNROLL;
+#ifndef SSCAN_MAX_CHUNK
+#define SSCAN_MAX_CHUNK 32
+#endif
+// Largest number of steps staged per chunk (16 or 32).
+constexpr int kMaxChunk = SSCAN_MAX_CHUNK;
 
 template <typename T, int NS_, int P_>
 struct FwdCfg {
@@ -86,7 +91,7 @@ struct FwdCfg {
     static constexpr int CPW = 2 * PPW;               // channels per warp
     static constexpr int DT = kWarps * CPW;           // channels per CTA
     static constexpr int NSP = NS * P;                // state slots per channel
-    static constexpr int TC = (DT > 64) ? 16 : 32;    // steps per chunk
+    static constexpr int TC = (DT > 64 || kMaxChunk < 32) ? 16 : 32;  // steps per chunk
     static constexpr int VECE = 16 / (int)sizeof(T);  // elements per 16 bytes
     static constexpr int RROW = TC + VECE;            // raw smem row (T), padded by 16 B
     static constexpr int PPR = TC / VECE;             // 16-byte pieces per raw row
@@ -389,19 +394,25 @@ __device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, 
     T* yrow0 = yb + (2 * pr) * RROW;
     T* yrow1 = yrow0 + RROW;
 
-    float a_n[2][NS], du_n[2], u_n[2];
-    float4 b_n[NS / 4], c_n[NS / 4];
+    // Two register sets (ping-pong): while step t is applied from one set, step
+    // t+1 is fetched into the other, so no values are copied between steps.
+    struct StepRegs {
+        float a[2][NS];
+        float du[2], u[2];
+        float4 b[NS / 4], c[NS / 4];
+    };
+    StepRegs r0, r1;
     float2 csum = make_float2(0.f, 0.f);
-    auto fetch = [&](int t) {
+    auto fetch = [&](StepRegs& r, int t) {
         const float2 u2 = *reinterpret_cast<const float2*>(ur + 2 * t);
         const float2 d2 = *reinterpret_cast<const float2*>(dr + 2 * t);
         if (DSUM) { csum.x += d2.x; csum.y += d2.y; }
-        u_n[0] = u2.x; u_n[1] = u2.y;
-        du_n[0] = d2.x * u2.x; du_n[1] = d2.y * u2.y;
+        r.u[0] = u2.x; r.u[1] = u2.y;
+        r.du[0] = d2.x * u2.x; r.du[1] = d2.y * u2.y;
 #pragma unroll
         for (int q = 0; q < NS / 4; ++q) {
-            if (!NO_B) b_n[q] = *reinterpret_cast<const float4*>(bb + t * RB + 4 * q);
-            if (WRITE_Y) c_n[q] = *reinterpret_cast<const float4*>(cb + t * RB + 4 * q);
+            if (!NO_B) r.b[q] = *reinterpret_cast<const float4*>(bb + t * RB + 4 * q);
+            if (WRITE_Y) r.c[q] = *reinterpret_cast<const float4*>(cb + t * RB + 4 * q);
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -409,57 +420,50 @@ __device__ __forceinline__ float2 compute_chunk(const float* wk, T* yb, int pr, 
             if (SCALAR) {
                 const float a = ex2(dt * As[e]);
 #pragma unroll
-                for (int k = 0; k < NS; ++k) a_n[e][k] = a;
+                for (int k = 0; k < NS; ++k) r.a[e][k] = a;
             } else {
 #pragma unroll
-                for (int k = 0; k < NS; ++k) a_n[e][k] = ex2(dt * A[e][k]);
+                for (int k = 0; k < NS; ++k) r.a[e][k] = ex2(dt * A[e][k]);
             }
         }
     };
-    fetch(0);
     float y[2][4], uu[2][4];
-#pragma unroll kStepUnroll
-    for (int t = 0; t < TC; ++t) {
-        float a_c[2][NS], du_c[2];
-        float4 b_c[NS / 4], c_c[NS / 4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            du_c[e] = du_n[e];
-            uu[e][t & 3] = u_n[e];
-#pragma unroll
-            for (int k = 0; k < NS; ++k) a_c[e][k] = a_n[e][k];
-        }
-#pragma unroll
-        for (int q = 0; q < NS / 4; ++q) {
-            if (!NO_B) b_c[q] = b_n[q];
-            if (WRITE_Y) c_c[q] = c_n[q];
-        }
-        if (t + 1 < TC) fetch(t + 1);
+    auto apply = [&](const StepRegs& r, int t) {
         float acc[2] = {0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < NS / 4; ++q) {
             float bv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (!NO_B) { bv[0] = b_c[q].x; bv[1] = b_c[q].y; bv[2] = b_c[q].z; bv[3] = b_c[q].w; }
+            if (!NO_B) { bv[0] = r.b[q].x; bv[1] = r.b[q].y; bv[2] = r.b[q].z; bv[3] = r.b[q].w; }
             float cv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (WRITE_Y) { cv[0] = c_c[q].x; cv[1] = c_c[q].y; cv[2] = c_c[q].z; cv[3] = c_c[q].w; }
+            if (WRITE_Y) { cv[0] = r.c[q].x; cv[1] = r.c[q].y; cv[2] = r.c[q].z; cv[3] = r.c[q].w; }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int k = 4 * q + j;
-                    if (NO_B) h[e][k] = a_c[e][k] * h[e][k];
-                    else h[e][k] = fmaf(a_c[e][k], h[e][k], du_c[e] * bv[j]);
+                    if (NO_B) h[e][k] = r.a[e][k] * h[e][k];
+                    else h[e][k] = fmaf(r.a[e][k], h[e][k], r.du[e] * bv[j]);
                     if (WRITE_Y) acc[e] = fmaf(cv[j], h[e][k], acc[e]);
                 }
         }
         if (WRITE_Y) {
             y[0][t & 3] = acc[0];
             y[1][t & 3] = acc[1];
+            uu[0][t & 3] = r.u[0];
+            uu[1][t & 3] = r.u[1];
             if ((t & 3) == 3) {
                 reduce_write4<T, P>(y[0], uu[0], Dd[0], g, yrow0 + (t & ~3));
                 reduce_write4<T, P>(y[1], uu[1], Dd[1], g, yrow1 + (t & ~3));
             }
         }
+    };
+    fetch(r0, 0);
+#pragma unroll kStepUnroll / 2
+    for (int t = 0; t < TC; t += 2) {
+        fetch(r1, t + 1);  // TC is even
+        apply(r0, t);
+        if (t + 2 < TC) fetch(r0, t + 2);
+        apply(r1, t + 1);
     }
     return csum;
 }
