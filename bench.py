@@ -236,14 +236,16 @@ def time_device(fn, steps, warmup, flush, stream):
     before each call; returns (mean seconds, total kernel launches)."""
     import torch
     for _ in range(warmup):
-        flush.zero_()
+        with torch.cuda.stream(stream):
+            flush.zero_()
         fn()
     torch.cuda.synchronize()
     evs = []
     launches = 0
     import linear_recurrence_gb300 as lr
     for _ in range(steps):
-        flush.zero_()
+        with torch.cuda.stream(stream):   # the flush is ordered before the timed call
+            flush.zero_()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
@@ -291,6 +293,28 @@ def bench_workload(w, steps, warmup, dev, stream, flush, e2e=False):
         te, _, _ = time_device(e2e_step, max(3, steps // 2), 2, flush, stream)
         res.update({"t_e2e": te, "h2d": h2d, "d2h": d2h})
     return res
+
+
+def bench_step(steps, warmup, dev, stream, flush, pk):
+    """The single-step decode update on DECODE_WORKLOAD: HBM-bound on the fp32
+    state (read + write 8 bytes per (b, d, n))."""
+    import torch
+    import linear_recurrence_gb300 as lr
+    w = workloads.DECODE_WORKLOAD
+    x = workloads.make_decode_inputs(w)
+    g = {k: v.to(dev) for k, v in x.items()}
+    out = torch.empty_like(g["u"])
+    st = g["state"]
+    t, launches, _ = time_device(
+        lambda: lr.sscan_step(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], state=st, out=out,
+                              stream=stream), steps, warmup, flush, stream)
+    es = 2 if w.dtype == "bf16" else 4
+    nbytes = (2 * w.batch * w.dim * w.N * 4 + 3 * w.batch * w.dim * es + 2 * w.batch * w.N * es
+              + w.dim * w.N * 4 + w.dim * 4)
+    gbs = nbytes / t / 1e9
+    return {"workload": f"{w.name} (batch={w.batch}, dim={w.dim}, N={w.N}, {w.dtype} I/O, fp32 state)",
+            "us": t * 1e6, "hbm_gbs": gbs, "bound": "hbm", "frac": gbs / pk["hbm_gbs"],
+            "launches_per_call": launches / steps}
 
 
 def bench_pscan(steps, warmup, dev, stream, flush):
@@ -422,6 +446,7 @@ def main():
                          "frac": rfx["frac"], "frac_of_roofline": rfx["frac_of_roofline"],
                          "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"]}
         per["pscan_8k"] = bench_pscan(max(5, args.steps // 2), 3, dev, stream, flush)
+        per["decode_step"] = bench_step(max(5, args.steps // 2), 3, dev, stream, flush, pk)
         extra["per_workload"] = per
         rate, cores, sample, _ = oracle_rate(w, budget_s=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}

@@ -102,6 +102,26 @@ int sscan_fwd_ex(const void *u, const void *delta, const float *A, const void *B
 int pscan(const float *a, const float *b, float *h, const float *h0,
           int64_t rows, int64_t len, void *stream);
 
+/*
+ * sscan_step -- one autoregressive decode step: advance the cached state of
+ * every (batch, channel) by one token and read it out (the recurrent
+ * inference step whose state cache "Mamba 状态空间模型：从理论到生产级推理的
+ * CUDA 内核优化实战" describes in section 5.1):
+ *
+ *   state[b,d,n] <- exp(delta[b,d]*A[d,n])*state[b,d,n] + delta[b,d]*B[b,n]*u[b,d]
+ *   out[b,d]      = sum_n C[b,n]*state[b,d,n] + D[d]*u[b,d]    (the updated state)
+ *
+ * It equals sscan_fwd with seqlen = 1, h0 = state and final_state = state.
+ * u, delta, out: [batch, dim] in the I/O dtype; A [dim, N] float32; B, C
+ * [batch, N] in the I/O dtype; D [dim] float32 or NULL; state [batch, dim, N]
+ * float32, updated in place.  All are device pointers; state must not alias
+ * any other argument.  Returns SSCAN_OK, SSCAN_ERR_INVALID (missing pointer,
+ * bad size or dtype, N > sscan_max_dstate()) or SSCAN_ERR_CUDA (launch).
+ */
+int sscan_step(const void *u, const void *delta, const float *A, const void *B,
+               const void *C, const float *D, float *state, void *out, int64_t batch,
+               int64_t dim, int64_t dstate, int dtype, void *stream);
+
 /* Bytes of device memory that sscan_fwd_noalloc keeps, per GPU, for the
  * carry of time-split launches (a fixed array, held until the process exits). */
 #define SSCAN_NOALLOC_SCRATCH_BYTES (4u << 20)

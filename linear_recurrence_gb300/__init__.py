@@ -39,6 +39,7 @@ SIGNATURES = {
                             _i64, _i64, _i64, _i64, _int, _int, _int, _vp]),
     "sscan_fwd_noalloc": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
                                  _i64, _i64, _i64, _i64, _int, _int, _vp]),
+    "sscan_step": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _int, _vp]),
     "pscan": (_int, [_fp, _fp, _fp, _fp, _i64, _i64, _vp]),
     "sscan_status_string": (ctypes.c_char_p, [_int]),
     "sscan_get_last_error": (_int, []),
@@ -171,6 +172,42 @@ def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, out=None, final_state=None,
     return out, final_state
 
 
+def sscan_step(u, delta, A, B, C, D=None, *, state, out=None, stream=None):
+    """One decode step: advances ``state`` [batch, dim, N] (float32, in place)
+    by one token and returns y [batch, dim].  u, delta: [batch, dim]; B, C:
+    [batch, N] (float32 or bfloat16, like u); A [dim, N] and D [dim] float32."""
+    if u.dim() != 2:
+        raise ValueError("u must be [batch, dim]")
+    batch, dim = u.shape
+    if A.dim() != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("sscan_step runs on CUDA tensors only")
+    io = u.dtype
+    if io not in (torch.float32, torch.bfloat16):
+        raise ValueError("u must be float32 or bfloat16")
+    _check(u, "u", (batch, dim), io, dev)
+    _check(delta, "delta", (batch, dim), io, dev)
+    _check(A, "A", (dim, N), torch.float32, dev)
+    _check(B, "B", (batch, N), io, dev)
+    _check(C, "C", (batch, N), io, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    _check(state, "state", (batch, dim, N), torch.float32, dev)
+    if out is None:
+        out = torch.empty((batch, dim), dtype=io, device=dev)
+    else:
+        _check(out, "out", (batch, dim), io, dev)
+    dtype = SSCAN_F32 if io == torch.float32 else SSCAN_BF16
+    rc = lib().sscan_step(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state),
+                          _ptr(out), batch, dim, N, dtype, _stream_handle(stream))
+    if rc != SSCAN_OK:
+        raise SscanError(rc, "sscan_step")
+    return out
+
+
 def pscan(a, b, h0=None, *, out=None, stream=None):
     """h[r,t] = a[r,t]*h[r,t-1] + b[r,t] with h[r,-1] = h0[r] (0 if None), on
     float32 CUDA tensors a, b [rows, len].  Returns h [rows, len]."""
@@ -194,6 +231,6 @@ def pscan(a, b, h0=None, *, out=None, stream=None):
     return out
 
 
-__all__ = ["sscan_fwd", "pscan", "status_string", "get_last_error", "max_dstate",
+__all__ = ["sscan_fwd", "sscan_step", "pscan", "status_string", "get_last_error", "max_dstate",
            "last_launch_count", "last_plan", "load_library", "SscanError",
            "SIGNATURES", "LIB_PATH"]

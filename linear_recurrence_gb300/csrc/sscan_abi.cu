@@ -74,6 +74,16 @@ cudaError_t launch_fwd(int dtype, FwdKernel k, const FwdParams& p, Shape sh, boo
 
 }  // namespace
 
+namespace sscan {
+// Call record of an entry point defined in another translation unit.
+void record_call(int launches, cudaStream_t stream, const char* plan) {
+    g_rec.launches = launches;
+    g_rec.stream = stream;
+    snprintf(g_rec.plan, sizeof(g_rec.plan), "%s", plan);
+}
+void record_error(cudaError_t e) { fail_cuda(e); }
+}  // namespace sscan
+
 extern "C" {
 
 const char* sscan_status_string(int status) {

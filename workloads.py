@@ -145,3 +145,37 @@ def make_pscan_inputs(w: PscanWorkload):
     b = torch.randn((w.rows, w.len), generator=g, dtype=torch.float32)
     h0 = torch.randn((w.rows,), generator=g, dtype=torch.float32)
     return {"a": a.contiguous(), "b": b.contiguous(), "h0": h0.contiguous()}
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    batch: int
+    dim: int
+    N: int
+    dtype: str
+    seed: int
+
+
+# One decode step for a batch of 256 sequences of a d_inner = 5120 layer (the
+# channel count of a 2.8B-parameter Mamba) with N = 16: bf16 activations, an
+# fp32 state cache of 256*5120*16 floats.  Same distributions as the dim512
+# recipe; the cached state ~ N(0, 0.5^2).
+DECODE_WORKLOAD = DecodeWorkload("decode_b256_d5120", 256, 5120, 16, "bf16", 21)
+
+
+def make_decode_inputs(w: DecodeWorkload):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    u = torch.randn((w.batch, w.dim), generator=g, dtype=torch.float32)
+    z = torch.randn((w.batch, w.dim), generator=g, dtype=torch.float32)
+    delta = F.softplus(z * 0.5 - 2.0)
+    A = (-torch.arange(1, w.N + 1, dtype=torch.float32)).repeat(w.dim, 1)
+    B = torch.randn((w.batch, w.N), generator=g, dtype=torch.float32)
+    C = torch.randn((w.batch, w.N), generator=g, dtype=torch.float32)
+    D = torch.randn((w.dim,), generator=g, dtype=torch.float32)
+    state = torch.randn((w.batch, w.dim, w.N), generator=g, dtype=torch.float32) * 0.5
+    dt = io_dtype(w.dtype)
+    return {"u": u.to(dt).contiguous(), "delta": delta.to(dt).contiguous(), "A": A.contiguous(),
+            "B": B.to(dt).contiguous(), "C": C.to(dt).contiguous(), "D": D.contiguous(),
+            "state": state.contiguous()}
