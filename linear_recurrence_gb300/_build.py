@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsscan.so")
-UNITS = ["sscan_abi.cu", "sscan_fwd_f32.cu", "sscan_fwd_bf16.cu", "sscan_noalloc.cu",
+UNITS = ["sscan_abi.cu", "sscan_fwd_f32_a.cu", "sscan_fwd_f32_b.cu", "sscan_fwd_bf16_a.cu",
+         "sscan_fwd_bf16_b.cu", "sscan_noalloc.cu",
          "sscan_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -14,7 +14,6 @@
 
 namespace {
 
-using sscan::FwdKernel;
 using sscan::FwdParams;
 using sscan::Shape;
 
@@ -48,28 +47,10 @@ int fail_cuda(cudaError_t e) {
     return SSCAN_ERR_CUDA;
 }
 
-// Smallest compiled shape for dstate N with the requested lanes per channel
-// (0 = the default for N).
-bool choose_shape(long long N, int lanes, Shape* out) {
-    if (lanes == 0) {
-        if (N <= 4) lanes = 1;
-        else if (N <= 8) lanes = 2;
-        else lanes = 4;
-    }
-    for (const Shape& s : sscan::kShapes)
-        if (s.P == lanes && (long long)s.NS * s.P >= N) {
-            *out = s;
-            return true;
-        }
-    return false;
-}
-
-cudaError_t launch_fwd(int dtype, FwdKernel k, const FwdParams& p, Shape sh, bool vec, long long grid,
-                       cudaStream_t st) {
+cudaError_t launch_fwd(bool f32, const FwdParams& p, Shape sh, long long grid, cudaStream_t st) {
     if (grid <= 0) return cudaSuccess;
     ++g_rec.launches;
-    return dtype == SSCAN_F32 ? sscan::fwd_launch_f32(k, p, sh, vec, (int)grid, st)
-                              : sscan::fwd_launch_bf16(k, p, sh, vec, (int)grid, st);
+    return sscan::fwd_launch(f32, p, sh, (int)grid, st);
 }
 
 }  // namespace
@@ -82,6 +63,95 @@ void record_call(int launches, cudaStream_t stream, const char* plan) {
     snprintf(g_rec.plan, sizeof(g_rec.plan), "%s", plan);
 }
 void record_error(cudaError_t e) { fail_cuda(e); }
+
+// Warps per SM the automatic plan aims for when it splits time: about three
+// per scheduler, enough to cover the FMA/MUFU and shared-memory latencies of
+// the scan loop.
+#ifndef SSCAN_TARGET_WARPS
+#define SSCAN_TARGET_WARPS 12
+#endif
+constexpr long long kTargetWarpsPerSm = SSCAN_TARGET_WARPS;
+// Shortest automatic segment, in chunks.
+constexpr long long kMinSegmentChunks = 8;
+
+// Automatic shape per state count, measured on GB300: two or four states per
+// lane and one channel per lane keep the most warps in flight, which the
+// exponent-bound general case needs; wide states (N > 32) prefer 16 states x 2
+// channels per lane (B/C reuse across channels) when that still gives 3 warps
+// per SM.
+struct ShapePref {
+    long long max_n;
+    Shape sh;
+    long long min_warps_per_sm;
+};
+constexpr ShapePref kPrefs[] = {
+    {4, {1, 4, 1}, 0},  {8, {2, 4, 1}, 0},  {16, {8, 2, 1}, 0},
+    {32, {8, 4, 1}, 0}, {64, {4, 16, 2}, 3}, {64, {8, 8, 1}, 0},
+};
+
+// Resident CTAs per SM of a shape, queried once per device.
+int cached_occupancy(bool f32, Shape sh) {
+    constexpr int kNumShapes = (int)(sizeof(kShapes) / sizeof(kShapes[0]));
+    static int cache[64][2][kNumShapes] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int idx = 0;
+    while (idx < kNumShapes &&
+           !(kShapes[idx].P == sh.P && kShapes[idx].NS == sh.NS && kShapes[idx].CPL == sh.CPL))
+        ++idx;
+    if (idx == kNumShapes) return 0;
+    int& c = cache[dev & 63][f32 ? 0 : 1][idx];
+    if (c == 0) c = fwd_occupancy(f32, sh);
+    return c;
+}
+
+int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
+             int lanes, long long max_segments, FwdPlan* out) {
+    const int nsm = std::max(sm_count(), 1);
+    Shape chosen{0, 0, 0};
+    if (lanes == 0) {
+        for (const ShapePref& pr : kPrefs) {
+            if (N > pr.max_n) continue;
+            const long long warps = batch * ceil_div(dim, shape_channels(pr.sh)) * shape_warps(pr.sh);
+            if (warps >= pr.min_warps_per_sm * nsm) {
+                chosen = pr.sh;
+                break;
+            }
+        }
+    } else {
+        // the compiled shape with P = lanes and the fewest state slots >= N
+        for (const Shape& c : kShapes)
+            if (c.P == lanes && (long long)c.NS * c.P >= N &&
+                (chosen.P == 0 || c.NS * c.P < chosen.NS * chosen.P))
+                chosen = c;
+    }
+    const long long chosen_warps =
+        chosen.P == 0 ? 0 : batch * ceil_div(dim, shape_channels(chosen)) * shape_warps(chosen);
+    const long long target =
+        chosen.P == 0 ? 0
+                      : std::min((long long)nsm * std::max(cached_occupancy(f32, chosen), 1) * shape_warps(chosen),
+                                 (long long)nsm * kTargetWarpsPerSm);
+    if (chosen.P == 0) return SSCAN_ERR_INVALID;
+    const long long DT = shape_channels(chosen);
+    const long long TC = kChunkSteps;
+    FwdPlan pl;
+    pl.sh = chosen;
+    pl.tiles_per_batch = ceil_div(dim, DT);
+    pl.tiles = batch * pl.tiles_per_batch;
+    if (pl.tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
+    long long S = segments;
+    if (S == 0) {
+        S = chosen_warps >= target ? 1 : ceil_div(target, std::max(chosen_warps, 1LL));
+        S = std::min(S, std::max(1LL, seqlen / (kMinSegmentChunks * TC)));
+        S = std::min(S, std::max(1LL, max_segments));
+    }
+    S = std::max(1LL, std::min(S, ceil_div(seqlen, TC)));
+    pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
+    pl.S = ceil_div(seqlen, pl.Tseg);
+    if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    *out = pl;
+    return SSCAN_OK;
+}
 }  // namespace sscan
 
 extern "C" {
@@ -129,14 +199,13 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     if (batch > big || dim > big || seqlen > big || (batch && dim > big / batch) ||
         (batch * dim && seqlen > big / (batch * dim)))
         return SSCAN_ERR_INVALID;
-    Shape sh;
-    if (!choose_shape(dstate, lanes, &sh)) return SSCAN_ERR_INVALID;
-
     // empty problems: arrays with no elements may be NULL
     if (batch == 0 || dim == 0) {
         snprintf(g_rec.plan, sizeof(g_rec.plan), "empty");
         return SSCAN_OK;
     }
+    if (lanes != 0 && lanes != 1 && lanes != 2 && lanes != 4 && lanes != 8 && lanes != 16)
+        return SSCAN_ERR_INVALID;
     if (seqlen == 0) {
         snprintf(g_rec.plan, sizeof(g_rec.plan), "seqlen 0: final_state = h0");
         if (final_state) {
@@ -149,51 +218,34 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     }
     if (!u || !delta || !A || !B || !C || !out) return SSCAN_ERR_INVALID;
 
-    const int esz = dtype == SSCAN_F32 ? 4 : 2;
+    const bool f32 = dtype == SSCAN_F32;
+    const int esz = f32 ? 4 : 2;
     const int vece = 16 / esz;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
                      aligned16(C) && aligned16(out);
-    const int DT = sscan::fwd_channels_per_cta(sh);
-    const int TC = sscan::kChunkSteps;
-    const long long tiles_per_batch = ceil_div(dim, DT);
-    const long long tiles = batch * tiles_per_batch;
-    if (tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
-
-    // time split: about two CTAs per SM (measured best on GB300 for the
-    // few-channel workloads), each segment at least 8 chunks long
-    long long S = segments;
-    if (S == 0) {
-        const int nsm = sm_count();
-        const int occ = dtype == SSCAN_F32 ? sscan::fwd_occupancy_f32(sh, vec)
-                                           : sscan::fwd_occupancy_bf16(sh, vec);
-        // fp32 splits cost a short carry pass; bf16 splits re-run every segment,
-        // so bf16 splits only when there are fewer tiles than SMs
-        const long long per_sm = dtype == SSCAN_F32 ? std::min(std::max(occ, 1), 2) : 1;
-        const long long target = (long long)std::max(nsm, 1) * per_sm;
-        S = tiles >= target ? 1 : ceil_div((long long)std::max(nsm, 1) * std::min(std::max(occ, 1), 2), tiles);
-        S = std::min(S, std::max(1LL, seqlen / (8LL * TC)));
-    }
-    S = std::max(1LL, std::min(S, ceil_div(seqlen, TC)));
-    const long long Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
-    S = ceil_div(seqlen, Tseg);
-    if (tiles * S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    sscan::FwdPlan pl;
+    const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
+    if (prc != SSCAN_OK) return prc;
+    const Shape sh = pl.sh;
+    const long long S = pl.S, tiles = pl.tiles;
 
     FwdParams p{};
     p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.h0 = h0;
     p.out = out; p.final_state = final_state;
     p.batch = batch; p.dim = dim; p.L = seqlen; p.N = dstate;
-    p.Tseg = Tseg; p.S = (int)S; p.tiles_per_batch = (int)tiles_per_batch;
+    p.Tseg = pl.Tseg; p.S = (int)S; p.tiles_per_batch = (int)pl.tiles_per_batch;
+    p.vec = vec ? 1 : 0;
 
     snprintf(g_rec.plan, sizeof(g_rec.plan),
-             "sscan %s P=%d NS=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s", esz == 4 ? "f32" : "bf16",
-             sh.P, sh.NS, (int)vec, tiles, S, Tseg,
-             S == 1 ? "single" : (dtype == SSCAN_F32 ? "local+correct" : "agg+fold"));
+             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s", f32 ? "f32" : "bf16",
+             sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
+             S == 1 ? "single" : "local+correct");
 
     cudaError_t e;
     if (S == 1) {
         p.mode = sscan::MODE_SINGLE;
         p.seg_count = 1;
-        e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles, st);
+        e = launch_fwd(f32, p, sh, tiles, st);
         if (e != cudaSuccess) return fail_cuda(e);
         return SSCAN_OK;
     }
@@ -205,28 +257,16 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     if (e != cudaSuccess) return fail_cuda(e);
     p.seg_state = static_cast<float*>(scratch);
     p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
-    if (dtype == SSCAN_F32) {
-        // pass 1: every segment from its local start, writing y and its aggregate;
-        // pass 2: add the carried state's decaying contribution
-        p.mode = sscan::MODE_LOCAL;
-        p.seg_count = (int)S;
-        e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles * S, st);
-        if (e == cudaSuccess) {
-            p.mode = sscan::MODE_CORR;
-            p.seg_count = (int)(S - 1);
-            e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
-        }
-    } else {
-        // bf16 output is written once: aggregates first, then every segment from
-        // its exact entry state
-        p.mode = sscan::MODE_AGG;
+    // pass 1: every segment from its local start, writing y and its aggregate;
+    // pass 2: add the carried state's decaying contribution (bf16 outputs are
+    // rounded twice, the second time with the carry added)
+    p.mode = sscan::MODE_LOCAL;
+    p.seg_count = (int)S;
+    e = launch_fwd(f32, p, sh, tiles * S, st);
+    if (e == cudaSuccess) {
+        p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
-        e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
-        if (e == cudaSuccess) {
-            p.mode = sscan::MODE_FOLD;
-            p.seg_count = (int)S;
-            e = launch_fwd(dtype, FwdKernel::Chunked, p, sh, vec, tiles * S, st);
-        }
+        e = launch_fwd(f32, p, sh, tiles * (S - 1), st);
     }
     cudaError_t ef = cudaFreeAsync(scratch, st);
     if (e != cudaSuccess) return fail_cuda(e);

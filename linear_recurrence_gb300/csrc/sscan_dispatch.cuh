@@ -1,6 +1,7 @@
 // Host-side dispatch from a runtime launch plan to the compiled kernel
-// variants.  Each I/O dtype is instantiated in its own translation unit so the
-// variants compile in parallel.
+// variants, and the launch planner shared by the entry points.  The variants
+// are instantiated in four translation units (two per I/O dtype) so they
+// compile in parallel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -9,38 +10,72 @@
 
 namespace sscan {
 
-// (lanes per channel P, state slots per lane NS) combinations that are compiled.
+// (lanes per channel P, state slots per lane NS, channels per lane CPL).
 struct Shape {
     int P;
     int NS;
+    int CPL;
 };
-constexpr Shape kShapes[] = {{1, 4}, {1, 8}, {1, 16}, {2, 4}, {2, 8}, {4, 4}, {4, 8}, {4, 16}};
+// Every compiled shape.  The first group (P <= 4) lives in the *_a units, the
+// second (P >= 8) in the *_b units.
+#ifndef SSCAN_SHAPES_A
+#define SSCAN_SHAPES_A(X) X(1, 4, 1) X(2, 4, 1) X(4, 4, 1) X(4, 16, 2)
+#endif
+#ifndef SSCAN_SHAPES_B
+#define SSCAN_SHAPES_B(X) X(8, 2, 1) X(8, 4, 1) X(8, 8, 1) X(16, 4, 1)
+#endif
+#define SSCAN_SHAPE_INIT(P_, NS_, CPL_) {P_, NS_, CPL_},
+constexpr Shape kShapes[] = {SSCAN_SHAPES_A(SSCAN_SHAPE_INIT) SSCAN_SHAPES_B(SSCAN_SHAPE_INIT)};
 constexpr int kMaxDstate = 64;
 
-enum class FwdKernel { Chunked };
+inline int shape_warps(Shape sh) { return warps_for(sh.P, sh.CPL); }
+inline int shape_channels(Shape sh) { return shape_warps(sh) * (32 / sh.P) * sh.CPL; }
 
-// Per-dtype entry points (defined in sscan_fwd_f32.cu / sscan_fwd_bf16.cu).
-// launch: enqueue one kernel on `stream`; returns the launch error, or
-// cudaErrorInvalidValue for a shape that is not compiled.
-cudaError_t fwd_launch_f32(FwdKernel k, const FwdParams& p, Shape sh, bool vec, int grid,
-                           cudaStream_t stream);
-cudaError_t fwd_launch_bf16(FwdKernel k, const FwdParams& p, Shape sh, bool vec, int grid,
-                            cudaStream_t stream);
-// Resident CTAs per SM of the chunked kernel (0 on error).
-int fwd_occupancy_f32(Shape sh, bool vec);
-int fwd_occupancy_bf16(Shape sh, bool vec);
-// Channels per CTA and steps per chunk of a shape.
-inline int fwd_channels_per_cta(Shape sh) { return 2 * 2 * (32 / sh.P); }
-// Time segments are multiples of this many steps (a multiple of every shape's chunk).
-constexpr int kChunkSteps = 32;
+// Per-unit entry points: enqueue one kernel on `stream` (returns the launch
+// error, or cudaErrorInvalidValue for a shape the unit does not hold), and the
+// resident CTAs per SM of a shape (0 if unknown).
+cudaError_t fwd_launch_f32_a(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+cudaError_t fwd_launch_f32_b(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+cudaError_t fwd_launch_bf16_a(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+cudaError_t fwd_launch_bf16_b(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+int fwd_occupancy_f32_a(Shape sh);
+int fwd_occupancy_f32_b(Shape sh);
+int fwd_occupancy_bf16_a(Shape sh);
+int fwd_occupancy_bf16_b(Shape sh);
 
-// Shared implementation, included by the per-dtype translation units only.
+inline cudaError_t fwd_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream) {
+    if (sh.P <= 4)
+        return f32 ? fwd_launch_f32_a(p, sh, grid, stream) : fwd_launch_bf16_a(p, sh, grid, stream);
+    return f32 ? fwd_launch_f32_b(p, sh, grid, stream) : fwd_launch_bf16_b(p, sh, grid, stream);
+}
+inline int fwd_occupancy(bool f32, Shape sh) {
+    if (sh.P <= 4) return f32 ? fwd_occupancy_f32_a(sh) : fwd_occupancy_bf16_a(sh);
+    return f32 ? fwd_occupancy_f32_b(sh) : fwd_occupancy_bf16_b(sh);
+}
+
+// A launch plan of the forward pass (defined in sscan_abi.cu).
+struct FwdPlan {
+    Shape sh;
+    long long tiles_per_batch;
+    long long tiles;  // channel tiles (CTAs per segment)
+    long long S;      // time segments
+    long long Tseg;   // steps per segment
+};
+// Choose the shape and time split.  lanes: 0 = automatic, else P; segments:
+// 0 = automatic, else S; max_segments (>= 1) caps an automatic split.
+// Returns SSCAN_OK, SSCAN_ERR_INVALID or SSCAN_ERR_CUDA.
+int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
+             int lanes, long long max_segments, FwdPlan* out);
+
+// Shared implementation, included by the per-unit translation units only.
 #ifdef SSCAN_DISPATCH_IMPL
-template <typename T, int NS, int P, bool VEC>
-static cudaError_t launch_variant(FwdKernel k, const FwdParams& p, int grid, cudaStream_t stream) {
-    using Cfg = FwdCfg<T, NS, P>;
-    (void)k;
-    auto kern = sscan_fwd_chunked<T, NS, P, VEC>;
+template <typename T, int NS, int P, int CPL>
+static cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
+    using Cfg = FwdCfg<T, NS, P, CPL>;
+    auto kern = sscan_fwd_chunked<T, NS, P, CPL>;
+    // the state slots of a shape must cover every state: the kernel stages
+    // B/C rows n < N into NSP slots
+    if (p.N < 1 || p.N > (long long)Cfg::NSP) return cudaErrorInvalidValue;
     // opting in to more than 48 KB of dynamic shared memory is per device
     static unsigned long long configured = 0;  // bit per device ordinal (< 64)
     int dev = 0;
@@ -56,10 +91,10 @@ static cudaError_t launch_variant(FwdKernel k, const FwdParams& p, int grid, cud
     return cudaGetLastError();
 }
 
-template <typename T, int NS, int P, bool VEC>
+template <typename T, int NS, int P, int CPL>
 static int occupancy_variant() {
-    using Cfg = FwdCfg<T, NS, P>;
-    auto kern = sscan_fwd_chunked<T, NS, P, VEC>;
+    using Cfg = FwdCfg<T, NS, P, CPL>;
+    auto kern = sscan_fwd_chunked<T, NS, P, CPL>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
         cudaSuccess)
         return 0;
@@ -70,29 +105,22 @@ static int occupancy_variant() {
     return n;
 }
 
-#define SSCAN_FOR_SHAPES(X) X(1, 4) X(1, 8) X(1, 16) X(2, 4) X(2, 8) X(4, 4) X(4, 8) X(4, 16)
-
-template <typename T>
-static cudaError_t launch_dtype(FwdKernel k, const FwdParams& p, Shape sh, bool vec, int grid,
-                                cudaStream_t stream) {
-#define SSCAN_CASE(P_, NS_)                                                        \
-    if (sh.P == P_ && sh.NS == NS_)                                                \
-        return vec ? launch_variant<T, NS_, P_, true>(k, p, grid, stream)          \
-                   : launch_variant<T, NS_, P_, false>(k, p, grid, stream);
-    SSCAN_FOR_SHAPES(SSCAN_CASE)
-#undef SSCAN_CASE
-    return cudaErrorInvalidValue;
-}
-
-template <typename T>
-static int occupancy_dtype(Shape sh, bool vec) {
-#define SSCAN_CASE(P_, NS_)                                                        \
-    if (sh.P == P_ && sh.NS == NS_)                                                \
-        return vec ? occupancy_variant<T, NS_, P_, true>() : occupancy_variant<T, NS_, P_, false>();
-    SSCAN_FOR_SHAPES(SSCAN_CASE)
-#undef SSCAN_CASE
-    return 0;
-}
+// A unit sets `using UnitT = float;` (or bf16) and then expands
+// SSCAN_DEFINE_UNIT(f32_a, SSCAN_SHAPES_A) and so on.
+#define SSCAN_LAUNCH_CASE(P_, NS_, CPL_)                                   \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_)                      \
+        return launch_variant<UnitT, NS_, P_, CPL_>(p, grid, st);
+#define SSCAN_OCC_CASE(P_, NS_, CPL_)                                      \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_variant<UnitT, NS_, P_, CPL_>();
+#define SSCAN_DEFINE_UNIT(SUFFIX, SHAPES)                                                       \
+    cudaError_t fwd_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t st) { \
+        SHAPES(SSCAN_LAUNCH_CASE)                                                               \
+        return cudaErrorInvalidValue;                                                           \
+    }                                                                                           \
+    int fwd_occupancy_##SUFFIX(Shape sh) {                                                      \
+        SHAPES(SSCAN_OCC_CASE)                                                                  \
+        return 0;                                                                               \
+    }
 #endif  // SSCAN_DISPATCH_IMPL
 
 }  // namespace sscan

@@ -1,0 +1,10 @@
+// bfloat16-I/O variants of the selective-scan kernel (lanes per channel >= 8).
+#define SSCAN_DISPATCH_IMPL
+#include "sscan_dispatch.cuh"
+
+namespace sscan {
+
+using UnitT = bf16;
+SSCAN_DEFINE_UNIT(bf16_b, SSCAN_SHAPES_B)
+
+}  // namespace sscan

@@ -1,0 +1,10 @@
+// float32-I/O variants of the selective-scan kernel (lanes per channel <= 4).
+#define SSCAN_DISPATCH_IMPL
+#include "sscan_dispatch.cuh"
+
+namespace sscan {
+
+using UnitT = float;
+SSCAN_DEFINE_UNIT(f32_a, SSCAN_SHAPES_A)
+
+}  // namespace sscan

@@ -1,0 +1,10 @@
+// float32-I/O variants of the selective-scan kernel (lanes per channel >= 8).
+#define SSCAN_DISPATCH_IMPL
+#include "sscan_dispatch.cuh"
+
+namespace sscan {
+
+using UnitT = float;
+SSCAN_DEFINE_UNIT(f32_b, SSCAN_SHAPES_B)
+
+}  // namespace sscan

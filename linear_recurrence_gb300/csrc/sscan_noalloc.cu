@@ -54,14 +54,12 @@ cudaError_t scratch_address(void** out) {
     return cudaSuccess;
 }
 
-inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 inline bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-cudaError_t launch(int dtype, sscan::FwdKernel k, const sscan::FwdParams& p, sscan::Shape sh,
-                   bool vec, long long grid, cudaStream_t st) {
+cudaError_t launch(bool f32, const sscan::FwdParams& p, sscan::Shape sh, long long grid,
+                   cudaStream_t st) {
     if (grid <= 0) return cudaSuccess;
-    return dtype == SSCAN_F32 ? sscan::fwd_launch_f32(k, p, sh, vec, (int)grid, st)
-                              : sscan::fwd_launch_bf16(k, p, sh, vec, (int)grid, st);
+    return sscan::fwd_launch(f32, p, sh, (int)grid, st);
 }
 
 }  // namespace
@@ -79,14 +77,6 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     if (batch > big || dim > big || seqlen > big || (batch && dim > big / batch) ||
         (batch * dim && seqlen > big / (batch * dim)))
         return SSCAN_ERR_INVALID;
-    sscan::Shape sh{0, 0};
-    {
-        const int lanes = dstate <= 4 ? 1 : (dstate <= 8 ? 2 : 4);
-        bool found = false;
-        for (const sscan::Shape& s : sscan::kShapes)
-            if (s.P == lanes && (long long)s.NS * s.P >= dstate) { sh = s; found = true; break; }
-        if (!found) return SSCAN_ERR_INVALID;
-    }
     if (batch == 0 || dim == 0) return SSCAN_OK;
     if (seqlen == 0) {
         if (final_state) {
@@ -99,49 +89,33 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     }
     if (!u || !delta || !A || !B || !C || !out) return SSCAN_ERR_INVALID;
 
-    const int esz = dtype == SSCAN_F32 ? 4 : 2;
+    const bool f32 = dtype == SSCAN_F32;
+    const int esz = f32 ? 4 : 2;
     const bool vec = (seqlen % (16 / esz)) == 0 && is_aligned16(u) && is_aligned16(delta) &&
                      is_aligned16(B) && is_aligned16(C) && is_aligned16(out);
-    const int DT = sscan::fwd_channels_per_cta(sh);
-    const int TC = sscan::kChunkSteps;
-    const long long tiles_per_batch = cdiv(dim, DT);
-    const long long tiles = batch * tiles_per_batch;
-    if (tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
     // carry scratch of a plan with S segments: batch*dim*S*(dstate+1) floats
     const long long per_segment = batch * dim * (dstate + 1) * (long long)sizeof(float);
     const long long max_segments = (long long)kScratchBytes / per_segment;  // may be 0 or 1
-
-    long long S = segments;
-    if (S == 0) {
-        int dev = 0, nsm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return SSCAN_ERR_CUDA;
-        const int occ = dtype == SSCAN_F32 ? sscan::fwd_occupancy_f32(sh, vec)
-                                           : sscan::fwd_occupancy_bf16(sh, vec);
-        const long long per_sm = dtype == SSCAN_F32 ? std::min(std::max(occ, 1), 2) : 1;
-        const long long target = (long long)std::max(nsm, 1) * per_sm;
-        S = tiles >= target ? 1 : cdiv((long long)std::max(nsm, 1) * std::min(std::max(occ, 1), 2), tiles);
-        S = std::min(S, std::max(1LL, seqlen / (8LL * TC)));
-        S = std::min(S, std::max(1LL, max_segments));  // automatic plans shrink to the array
-    }
-    S = std::max(1LL, std::min(S, cdiv(seqlen, TC)));
-    const long long Tseg = cdiv(cdiv(seqlen, S), TC) * TC;
-    S = cdiv(seqlen, Tseg);
+    sscan::FwdPlan pl;
+    const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, 0,
+                                    std::max(1LL, max_segments), &pl);
+    if (prc != SSCAN_OK) return prc;
+    const sscan::Shape sh = pl.sh;
+    const long long S = pl.S, tiles = pl.tiles, Tseg = pl.Tseg, tiles_per_batch = pl.tiles_per_batch;
     if (S > 1 && S > max_segments) return SSCAN_ERR_INVALID;  // would overflow the fixed scratch
-    if (tiles * S > (1LL << 30)) return SSCAN_ERR_INVALID;
 
     sscan::FwdParams p{};
     p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.h0 = h0;
     p.out = out; p.final_state = final_state;
     p.batch = batch; p.dim = dim; p.L = seqlen; p.N = dstate;
     p.Tseg = Tseg; p.S = (int)S; p.tiles_per_batch = (int)tiles_per_batch;
+    p.vec = vec ? 1 : 0;
 
     cudaError_t e;
     if (S == 1) {
         p.mode = sscan::MODE_SINGLE;
         p.seg_count = 1;
-        e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles, st);
+        e = launch(f32, p, sh, tiles, st);
         return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
     }
     void* scratch = nullptr;
@@ -149,24 +123,16 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     const size_t nseg = (size_t)(batch * dim) * (size_t)S;
     p.seg_state = static_cast<float*>(scratch);
     p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
-    if (dtype == SSCAN_F32) {
-        p.mode = sscan::MODE_LOCAL;
-        p.seg_count = (int)S;
-        e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * S, st);
-        if (e == cudaSuccess) {
-            p.mode = sscan::MODE_CORR;
-            p.seg_count = (int)(S - 1);
-            e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
-        }
-    } else {
-        p.mode = sscan::MODE_AGG;
+    // pass 1: every segment from its local start, writing y and its aggregate;
+    // pass 2: add the carried state's decaying contribution (bf16 outputs are
+    // rounded twice, the second time with the carry added)
+    p.mode = sscan::MODE_LOCAL;
+    p.seg_count = (int)S;
+    e = launch(f32, p, sh, tiles * S, st);
+    if (e == cudaSuccess) {
+        p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
-        e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * (S - 1), st);
-        if (e == cudaSuccess) {
-            p.mode = sscan::MODE_FOLD;
-            p.seg_count = (int)S;
-            e = launch(dtype, sscan::FwdKernel::Chunked, p, sh, vec, tiles * S, st);
-        }
+        e = launch(f32, p, sh, tiles * (S - 1), st);
     }
     return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }

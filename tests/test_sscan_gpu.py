@@ -95,14 +95,22 @@ def test_workload_small_time_split(lr, name, kw, segments):
         assert "single" not in plan
 
 
-@pytest.mark.parametrize("lanes", [1, 2, 4])
+# (lanes P, dstate N) -> the compiled shape (P, states per lane, channels per
+# lane) the plan must use; together these cover every compiled shape
+LANE_CASES = [(1, 4, (1, 4, 1)), (2, 7, (2, 4, 1)), (4, 13, (4, 4, 1)), (4, 40, (4, 16, 2)),
+              (8, 16, (8, 2, 1)), (8, 25, (8, 4, 1)), (8, 50, (8, 8, 1)), (16, 61, (16, 4, 1))]
+
+
+@pytest.mark.parametrize("lanes,N,shape", LANE_CASES, ids=lambda v: str(v))
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_lane_shapes(lr, lanes, dtype):
-    N = {1: 4, 2: 7, 4: 13}[lanes]
+def test_lane_shapes(lr, lanes, N, shape, dtype):
     w = workloads.WORKLOADS["dim512"].scaled(batch=2, dim=70, L=333, N=N)
     w = workloads.Workload(**{**w.__dict__, "dtype": dtype, "h0_std": 0.3})
+    tag = "P=%d NS=%d CPL=%d " % shape
     _compare(lr, w, workloads.make_inputs(w), TOL[dtype], lanes=lanes)
+    assert tag in lr.last_plan(), lr.last_plan()
     _compare(lr, w, workloads.make_inputs(w), TOL[dtype], lanes=lanes, segments=3)
+    assert tag in lr.last_plan() and "S=3" in lr.last_plan(), lr.last_plan()
 
 
 # --------------------------------------------------------------------------
