@@ -14,6 +14,11 @@ follows:
 * :func:`sscan_fwd` -- the sequential selective scan of the "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战"
   page, section 2.3 (pseudocode) and section 7.1 (PyTorch reference), and of
   the mamba.py listing on the "图解Blelloch并行扫描" page, section 3.2.
+* :func:`sscan_fwd_full` -- the same scan with its options: softplus of
+  delta + bias inside the op (section 7.1 and section 2.2 of that page), the
+  zero-order-hold B-bar of its section 1.2, and an output gate
+  (y + D*u) * silu(z) (the gate activation fused into the scan kernel on the
+  "为什么Mamba的“并行扫描”不是真并行" page, section 2).
 * :func:`pscan_seq` -- h_t = a_t*h_{t-1} + b_t row by row (the ``pscan``
   primitive of that listing; with a = 1 the prefix sum of its section 1.1).
 * :func:`pscan_blelloch` -- the same recurrence by Blelloch up-sweep /
@@ -67,6 +72,10 @@ def _load():
             _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
             _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int]
         lib.oracle_sscan_fwd_mutant.restype = ctypes.c_int
+        lib.oracle_sscan_fwd_full_mutant.argtypes = [
+            _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+            _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_sscan_fwd_full_mutant.restype = ctypes.c_int
         lib.oracle_mutation_count.argtypes = []
         lib.oracle_mutation_count.restype = ctypes.c_int
         lib.oracle_pscan_seq.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64]
@@ -131,6 +140,51 @@ def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, nthreads: int = 1,
         _ptr(y), _ptr(hT), batch, dim, L, N, int(nthreads), int(mutation))
     if rc != 0:
         raise ValueError(f"oracle_sscan_fwd rejected its arguments ({rc})")
+    return y, hT
+
+
+FLAG_SOFTPLUS = 1
+FLAG_ZOH = 2
+
+
+def sscan_fwd_full(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, *,
+                   delta_softplus: bool = False, zoh: bool = False, nthreads: int = 1,
+                   mutation: int = 0):
+    """The scan with its options, in float64 (the C function's header states
+    the definitions and the passages they follow):
+
+    * ``delta_softplus``: delta <- softplus(delta + delta_bias[d]);
+    * ``zoh``: the zero-order-hold B-bar expm1(delta*A)/A * B instead of delta*B;
+    * ``z`` [batch, dim, L]: out = (y + D*u) * silu(z).
+
+    Returns (y, final_state) like :func:`sscan_fwd`.
+    """
+    u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
+    D, h0, z, delta_bias = _f64(D), _f64(h0), _f64(z), _f64(delta_bias)
+    if u.ndim != 3 or delta.shape != u.shape:
+        raise ValueError("u and delta must both be [batch, dim, L]")
+    batch, dim, L = u.shape
+    if A.ndim != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    if B.shape != (batch, N, L) or C.shape != (batch, N, L):
+        raise ValueError("B and C must be [batch, N, L]")
+    if D is not None and D.shape != (dim,):
+        raise ValueError("D must be [dim]")
+    if z is not None and z.shape != u.shape:
+        raise ValueError("z must be [batch, dim, L]")
+    if delta_bias is not None and delta_bias.shape != (dim,):
+        raise ValueError("delta_bias must be [dim]")
+    if h0 is not None and h0.shape != (batch, dim, N):
+        raise ValueError("h0 must be [batch, dim, N]")
+    flags = (FLAG_SOFTPLUS if delta_softplus else 0) | (FLAG_ZOH if zoh else 0)
+    y = np.zeros((batch, dim, L), dtype=np.float64)
+    hT = np.zeros((batch, dim, N), dtype=np.float64)
+    rc = _load().oracle_sscan_fwd_full_mutant(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        _ptr(h0), _ptr(y), _ptr(hT), batch, dim, L, N, flags, int(nthreads), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_sscan_fwd_full rejected its arguments ({rc})")
     return y, hT
 
 

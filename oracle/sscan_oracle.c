@@ -24,6 +24,20 @@
  *    section 1.2); delta is used as given (no softplus inside); y_t uses the
  *    state after the update at t; the D skip multiplies u, not delta*u.
  *
+ *  - oracle_sscan_fwd_full: the same scan with the options the pages attach
+ *    to it, each off by default:
+ *      SOFTPLUS  delta <- softplus(delta + delta_bias[d]) inside the op (the
+ *                F.softplus(delta) of the section 7.1 reference and the
+ *                delta = softplus(Linear(x)) of section 2.2; delta_bias is the
+ *                per-channel bias of that projection, NULL = none);
+ *      ZOH       the zero-order-hold B-bar of section 1.2,
+ *                (delta*A)^-1 (exp(delta*A) - 1) delta*B, which for diagonal A
+ *                is expm1(delta*A[d,n]) / A[d,n] * B (delta*B when A = 0);
+ *      z         an output gate, out = (y + D*u) * silu(z) with
+ *                silu(z) = z / (1 + exp(-z)): the sigmoid gate activation
+ *                fused into the scan kernel on the "为什么Mamba的“并行扫描”
+ *                不是真并行" page, section 2, read as Mamba's SiLU gate.
+ *
  *  - oracle_pscan_seq: the first-order linear recurrence h_t = a_t*h_{t-1}
  *    + b_t, one row at a time (the pscan(deltaA, BX) primitive of the
  *    mamba.py listing, "图解Blelloch并行扫描" section 3.2; with a = 1 it is
@@ -59,8 +73,18 @@ enum {
     MUT_B_NEXT_STEP = 6,     /* read B at t+1 (index slip)                   */
     MUT_C_FROM_B = 7,        /* contract with B instead of C (operand swap)  */
     MUT_D_TIMES_DU = 8,      /* skip term D*delta*u instead of D*u           */
-    MUT_COUNT = 9
+    MUT_BIAS_AFTER_SOFTPLUS = 9, /* softplus(delta) + bias                   */
+    MUT_GATE_SIGMOID = 10,   /* out = y * sigmoid(z) instead of y * silu(z)  */
+    MUT_GATE_BEFORE_D = 11,  /* gate y, then add D*u ungated                 */
+    MUT_ZOH_NO_DIV = 12,     /* ZOH B-bar = expm1(delta*A) * B (1/A dropped) */
+    MUT_ZOH_DELTA_TWICE = 13, /* ZOH B-bar = expm1(delta*A)/A * delta*B      */
+    MUT_COUNT = 14
 };
+
+enum { FLAG_SOFTPLUS = 1, FLAG_ZOH = 2 };
+
+/* log(1 + exp(x)) without overflow */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
 
 typedef struct {
     const double *u, *delta, *A, *B, *C, *D, *h0;
@@ -68,6 +92,8 @@ typedef struct {
     int64_t batch, dim, L, N;
     int64_t first, last; /* channel range [first, last) over batch*dim */
     int mutation;
+    const double *z, *delta_bias; /* [batch, dim, L] and [dim], or NULL */
+    int flags;                     /* FLAG_SOFTPLUS | FLAG_ZOH           */
 } sscan_job;
 
 static void sscan_channels(const sscan_job *j)
@@ -85,8 +111,12 @@ static void sscan_channels(const sscan_job *j)
         double *y = j->out + ch * L;
         for (int64_t n = 0; n < N; ++n)
             h[n] = (j->h0 && j->mutation != MUT_IGNORE_H0) ? j->h0[ch * N + n] : 0.0;
+        const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
         for (int64_t t = 0; t < L; ++t) {
-            const double dt = dl[t];
+            double dt = dl[t];
+            if (j->flags & FLAG_SOFTPLUS)
+                dt = (j->mutation == MUT_BIAS_AFTER_SOFTPLUS) ? softplus(dt) + bias
+                                                              : softplus(dt + bias);
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 hprev[n] = h[n];
@@ -94,7 +124,19 @@ static void sscan_channels(const sscan_job *j)
                 if (j->mutation == MUT_EXP_SIGN) a = exp(-dt * Ad[n]);
                 int64_t tb = t;
                 if (j->mutation == MUT_B_NEXT_STEP && t + 1 < L) tb = t + 1;
-                double bx = dt * Bb[n * L + tb] * u[t];
+                /* B-bar per unit B: delta (Euler) or the zero-order hold */
+                double bbar = dt;
+                if (j->flags & FLAG_ZOH) {
+                    if (Ad[n] == 0.0)
+                        bbar = dt;
+                    else if (j->mutation == MUT_ZOH_NO_DIV)
+                        bbar = expm1(dt * Ad[n]);
+                    else if (j->mutation == MUT_ZOH_DELTA_TWICE)
+                        bbar = expm1(dt * Ad[n]) / Ad[n] * dt;
+                    else
+                        bbar = expm1(dt * Ad[n]) / Ad[n];
+                }
+                double bx = bbar * Bb[n * L + tb] * u[t];
                 if (j->mutation == MUT_NO_DELTA_IN_B) bx = Bb[n * L + tb] * u[t];
                 h[n] = a * h[n] + bx;
             }
@@ -103,11 +145,19 @@ static void sscan_channels(const sscan_job *j)
                 double cv = (j->mutation == MUT_C_FROM_B) ? Bb[n * L + t] : Cb[n * L + t];
                 acc += cv * hv;
             }
-            if (j->D && j->mutation != MUT_DROP_D) {
-                if (j->mutation == MUT_D_TIMES_DU)
-                    acc += j->D[d] * dt * u[t];
+            double skip = 0.0;
+            if (j->D && j->mutation != MUT_DROP_D)
+                skip = (j->mutation == MUT_D_TIMES_DU) ? j->D[d] * dt * u[t] : j->D[d] * u[t];
+            if (j->z) {
+                const double zv = j->z[ch * L + t];
+                const double sig = 1.0 / (1.0 + exp(-zv));
+                const double gate = (j->mutation == MUT_GATE_SIGMOID) ? sig : zv * sig;
+                if (j->mutation == MUT_GATE_BEFORE_D)
+                    acc = acc * gate + skip;
                 else
-                    acc += j->D[d] * u[t];
+                    acc = (acc + skip) * gate;
+            } else {
+                acc += skip;
             }
             y[t] = acc;
         }
@@ -127,18 +177,20 @@ static void *sscan_thread(void *arg)
 /* Layouts (row-major, contiguous): u, delta, out [batch, dim, L]; A [dim, N];
  * B, C [batch, N, L]; D [dim] or NULL; h0, final_state [batch, dim, N] or NULL.
  * nthreads <= 1 runs on the calling thread.  Returns 0, or -1 on bad sizes. */
-int oracle_sscan_fwd_mutant(const double *u, const double *delta, const double *A,
-                            const double *B, const double *C, const double *D,
-                            const double *h0, double *out, double *final_state,
-                            int64_t batch, int64_t dim, int64_t L, int64_t N,
-                            int nthreads, int mutation)
+int oracle_sscan_fwd_full_mutant(const double *u, const double *delta, const double *A,
+                                 const double *B, const double *C, const double *D,
+                                 const double *z, const double *delta_bias,
+                                 const double *h0, double *out, double *final_state,
+                                 int64_t batch, int64_t dim, int64_t L, int64_t N,
+                                 int flags, int nthreads, int mutation)
 {
     if (batch < 0 || dim < 0 || L < 0 || N < 0) return -1;
     if (mutation < 0 || mutation >= MUT_COUNT) return -1;
+    if (flags & ~(FLAG_SOFTPLUS | FLAG_ZOH)) return -1;
     const int64_t nch = batch * dim;
     if (nch == 0) return 0;
     sscan_job base = {u, delta, A, B, C, D, h0, out, final_state,
-                      batch, dim, L, N, 0, nch, mutation};
+                      batch, dim, L, N, 0, nch, mutation, z, delta_bias, flags};
     if (nthreads <= 1 || nch == 1) {
         sscan_channels(&base);
         return 0;
@@ -168,6 +220,16 @@ int oracle_sscan_fwd_mutant(const double *u, const double *delta, const double *
     return 0;
 }
 
+int oracle_sscan_fwd_mutant(const double *u, const double *delta, const double *A,
+                            const double *B, const double *C, const double *D,
+                            const double *h0, double *out, double *final_state,
+                            int64_t batch, int64_t dim, int64_t L, int64_t N,
+                            int nthreads, int mutation)
+{
+    return oracle_sscan_fwd_full_mutant(u, delta, A, B, C, D, NULL, NULL, h0, out, final_state,
+                                        batch, dim, L, N, 0, nthreads, mutation);
+}
+
 int oracle_sscan_fwd(const double *u, const double *delta, const double *A,
                      const double *B, const double *C, const double *D,
                      const double *h0, double *out, double *final_state,
@@ -175,6 +237,20 @@ int oracle_sscan_fwd(const double *u, const double *delta, const double *A,
 {
     return oracle_sscan_fwd_mutant(u, delta, A, B, C, D, h0, out, final_state,
                                    batch, dim, L, N, nthreads, MUT_NONE);
+}
+
+/* The scan with its options: z [batch, dim, L] or NULL (output gate),
+ * delta_bias [dim] or NULL, flags = FLAG_SOFTPLUS (1) | FLAG_ZOH (2). */
+int oracle_sscan_fwd_full(const double *u, const double *delta, const double *A,
+                          const double *B, const double *C, const double *D,
+                          const double *z, const double *delta_bias,
+                          const double *h0, double *out, double *final_state,
+                          int64_t batch, int64_t dim, int64_t L, int64_t N,
+                          int flags, int nthreads)
+{
+    return oracle_sscan_fwd_full_mutant(u, delta, A, B, C, D, z, delta_bias, h0, out,
+                                        final_state, batch, dim, L, N, flags, nthreads,
+                                        MUT_NONE);
 }
 
 int oracle_mutation_count(void) { return MUT_COUNT; }

@@ -324,12 +324,141 @@ def test_oracle_pin(pin):
 
 
 def test_every_planted_mistake_is_caught():
-    n = oracle.mutation_count()
-    assert n >= 9
-    for m in range(1, n):
+    for m in BASE_MUTATIONS:
         f = _oracle_callable(m)
         failed = [p.__name__ for p in PINS if p(f) is not None]
         assert failed, f"planted mistake {m} passed every pin"
+
+
+# ------------------------------------------- pins of the scan's options
+# Each takes full(u, delta, A, B, C, D, z, delta_bias, h0, softplus, zoh)
+# -> (y, hT) and returns None when it holds, else a message.
+
+BASE_MUTATIONS = range(1, 9)     # planted in the plain scan
+OPTION_MUTATIONS = range(9, 14)  # planted in softplus / gate / zero-order hold
+
+
+def pin_softplus_inverse(full):
+    """delta_softplus: softplus(r + bias) = k exactly when r = log(e^k - 1) - bias
+    ("CUDA 内核优化实战" section 7.1 applies softplus inside the op; section 2.2
+    defines delta as softplus of a projection, whose bias is delta_bias)."""
+    u, _, A, B, C, D, h0 = _rand_problem(31)
+    r = _rng(32)
+    k = r.uniform(0.01, 3.0, size=u.shape)
+    bias = r.normal(size=u.shape[1])
+    raw = np.log(np.expm1(k)) - bias[None, :, None]
+    y_ref, h_ref = oracle.sscan_fwd(u, k, A, B, C, D, h0)
+    y, hT = full(u, raw, A, B, C, D, None, bias, h0, True, False)
+    if np.max(np.abs(y - y_ref)) > 1e-12 * (1 + np.max(np.abs(y_ref))):
+        return "softplus(delta + bias) output"
+    if np.max(np.abs(hT - h_ref)) > 1e-12 * (1 + np.max(np.abs(h_ref))):
+        return "softplus(delta + bias) final state"
+    return None
+
+
+def pin_gate_special_values(full):
+    """z-gate out = (y + D u) * z * sigmoid(z) at points where silu has a closed
+    form: silu(0) = 0, silu(40) = 40 to double precision, silu(+-ln 3) =
+    +-ln 3 * (3/4 or 1/4)."""
+    u, delta, A, B, C, D, h0 = _rand_problem(33)
+    y0, h0ref = oracle.sscan_fwd(u, delta, A, B, C, D, h0)
+    pick = _rng(34).integers(0, 5, size=u.shape)
+    ln3 = np.log(3.0)
+    zvals = np.array([0.0, 40.0, ln3, -ln3, 40.0])
+    gate = np.array([0.0, 40.0, 0.75 * ln3, -0.25 * ln3, 40.0])
+    z = zvals[pick]
+    y, hT = full(u, delta, A, B, C, D, z, None, h0, False, False)
+    if np.max(np.abs(y - y0 * gate[pick])) > 1e-12 * (1 + np.max(np.abs(y0 * 40))):
+        return "gated output"
+    if np.max(np.abs(hT - h0ref)) > 0:
+        return "the gate must not touch the state"
+    return None
+
+
+def _zoh_by_ode(u, delta, A, B, C, D, h0, substeps=400):
+    """Integrate dh/dt = A h + B_t u_t over each step's duration delta_t with the
+    input held (RK4, many substeps) -- the zero-order hold by its definition,
+    independent of the closed form."""
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    y = np.zeros((batch, dim, L))
+    hT = np.zeros((batch, dim, N))
+    for b in range(batch):
+        for d in range(dim):
+            h = h0[b, d].copy() if h0 is not None else np.zeros(N)
+            a = A[d]
+            for t in range(L):
+                f = B[b, :, t] * u[b, d, t]
+                dt = delta[b, d, t] / substeps
+                for _ in range(substeps):
+                    k1 = a * h + f
+                    k2 = a * (h + 0.5 * dt * k1) + f
+                    k3 = a * (h + 0.5 * dt * k2) + f
+                    k4 = a * (h + dt * k3) + f
+                    h = h + dt / 6.0 * (k1 + 2 * k2 + 2 * k3 + k4)
+                y[b, d, t] = C[b, :, t] @ h + (D[d] * u[b, d, t] if D is not None else 0.0)
+            hT[b, d] = h
+    return y, hT
+
+
+def pin_zoh_matches_ode(full):
+    """ZOH B-bar ("CUDA 内核优化实战" section 1.2): the discrete step equals the
+    exact solution of the continuous system over a step with the input held."""
+    u, delta, A, B, C, D, h0 = _rand_problem(35, batch=1, dim=2, L=9, N=3)
+    y_ode, h_ode = _zoh_by_ode(u, delta, A, B, C, D, h0)
+    y, hT = full(u, delta, A, B, C, D, None, None, h0, False, True)
+    if np.max(np.abs(y - y_ode)) > 1e-9 * (1 + np.max(np.abs(y_ode))):
+        return "zoh output vs the integrated ODE"
+    if np.max(np.abs(hT - h_ode)) > 1e-9 * (1 + np.max(np.abs(h_ode))):
+        return "zoh final state vs the integrated ODE"
+    return None
+
+
+def pin_zoh_small_A_is_euler(full):
+    """As A -> 0 the ZOH B-bar tends to delta*B (A = 0 exactly: equal)."""
+    u, delta, A, B, C, D, h0 = _rand_problem(36)
+    A0 = np.zeros_like(A)
+    y_e, h_e = oracle.sscan_fwd(u, delta, A0, B, C, D, h0)
+    y_z, h_z = full(u, delta, A0, B, C, D, None, None, h0, False, True)
+    if np.max(np.abs(y_z - y_e)) > 1e-13 * (1 + np.max(np.abs(y_e))):
+        return "zoh with A = 0"
+    y_e, _ = oracle.sscan_fwd(u, delta, A0 - 1e-9, B, C, D, h0)
+    y_z, _ = full(u, delta, A0 - 1e-9, B, C, D, None, None, h0, False, True)
+    if np.max(np.abs(y_z - y_e)) > 1e-7 * (1 + np.max(np.abs(y_e))):
+        return "zoh with A = -1e-9"
+    return None
+
+
+OPTION_PINS = [pin_softplus_inverse, pin_gate_special_values, pin_zoh_matches_ode,
+               pin_zoh_small_A_is_euler]
+
+
+def _full_callable(mutation=0):
+    def f(u, delta, A, B, C, D, z, bias, h0, softplus, zoh):
+        return oracle.sscan_fwd_full(u, delta, A, B, C, D, z, bias, h0, delta_softplus=softplus,
+                                     zoh=zoh, mutation=mutation)
+    return f
+
+
+@pytest.mark.parametrize("pin", OPTION_PINS, ids=lambda p: p.__name__)
+def test_oracle_option_pin(pin):
+    msg = pin(_full_callable())
+    assert msg is None, msg
+
+
+def test_every_planted_option_mistake_is_caught():
+    assert oracle.mutation_count() == OPTION_MUTATIONS[-1] + 1
+    for m in OPTION_MUTATIONS:
+        f = _full_callable(m)
+        failed = [p.__name__ for p in OPTION_PINS if p(f) is not None]
+        assert failed, f"planted option mistake {m} passed every pin"
+
+
+def test_options_off_is_the_plain_scan():
+    u, delta, A, B, C, D, h0 = _rand_problem(37)
+    y0, h0r = oracle.sscan_fwd(u, delta, A, B, C, D, h0)
+    y1, h1 = oracle.sscan_fwd_full(u, delta, A, B, C, D, None, None, h0)
+    assert np.array_equal(y0, y1) and np.array_equal(h0r, h1)
 
 
 def test_threaded_oracle_equals_single_thread():
