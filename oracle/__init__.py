@@ -153,7 +153,8 @@ def sscan_fwd_full(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, 
     """The scan with its options, in float64 (the C function's header states
     the definitions and the passages they follow):
 
-    * ``delta_softplus``: delta <- softplus(delta + delta_bias[d]);
+    * ``delta_bias`` [dim]: delta <- delta + delta_bias[d];
+    * ``delta_softplus``: then delta <- softplus(delta);
     * ``zoh``: the zero-order-hold B-bar expm1(delta*A)/A * B instead of delta*B;
     * ``z`` [batch, dim, L]: out = (y + D*u) * silu(z).
 

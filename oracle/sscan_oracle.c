@@ -26,10 +26,11 @@
  *
  *  - oracle_sscan_fwd_full: the same scan with the options the pages attach
  *    to it, each off by default:
- *      SOFTPLUS  delta <- softplus(delta + delta_bias[d]) inside the op (the
+ *      delta_bias  delta <- delta + delta_bias[d] (the per-channel bias of
+ *                the projection that makes delta, section 2.2; NULL = none);
+ *      SOFTPLUS  then delta <- softplus(delta) inside the op (the
  *                F.softplus(delta) of the section 7.1 reference and the
- *                delta = softplus(Linear(x)) of section 2.2; delta_bias is the
- *                per-channel bias of that projection, NULL = none);
+ *                delta = softplus(Linear(x)) of section 2.2);
  *      ZOH       the zero-order-hold B-bar of section 1.2,
  *                (delta*A)^-1 (exp(delta*A) - 1) delta*B, which for diagonal A
  *                is expm1(delta*A[d,n]) / A[d,n] * B (delta*B when A = 0);
@@ -117,6 +118,8 @@ static void sscan_channels(const sscan_job *j)
             if (j->flags & FLAG_SOFTPLUS)
                 dt = (j->mutation == MUT_BIAS_AFTER_SOFTPLUS) ? softplus(dt) + bias
                                                               : softplus(dt + bias);
+            else
+                dt += bias;
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 hprev[n] = h[n];

@@ -353,6 +353,10 @@ def pin_softplus_inverse(full):
         return "softplus(delta + bias) output"
     if np.max(np.abs(hT - h_ref)) > 1e-12 * (1 + np.max(np.abs(h_ref))):
         return "softplus(delta + bias) final state"
+    # without softplus the bias alone shifts delta
+    y, _ = full(u, k - bias[None, :, None], A, B, C, D, None, bias, h0, False, False)
+    if np.max(np.abs(y - y_ref)) > 1e-12 * (1 + np.max(np.abs(y_ref))):
+        return "delta + bias output"
     return None
 
 
