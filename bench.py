@@ -295,6 +295,35 @@ def bench_workload(w, steps, warmup, dev, stream, flush, e2e=False):
     return res
 
 
+def bench_fused(w, steps, warmup, dev, stream, flush, pk):
+    """The scan with its options on workload ``w``: raw delta with a per-channel
+    bias and softplus inside the op, and the SiLU output gate z.  Algorithmic
+    bytes add z (read, one per (b, d, t)) and the bias (D fp32)."""
+    import torch
+    import linear_recurrence_gb300 as lr
+    x = workloads.make_inputs(w)
+    o = workloads.make_option_inputs(w)
+    g = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    go = {k: v.to(dev) for k, v in o.items()}
+    out = torch.empty_like(g["u"])
+    fs = torch.empty((w.batch, w.dim, w.N), dtype=torch.float32, device=dev)
+
+    def step():
+        lr.sscan_fwd(g["u"], go["delta_raw"], g["A"], g["B"], g["C"], g["D"], g["h0"],
+                     z=go["z"], delta_bias=go["delta_bias"], delta_softplus=True,
+                     out=out, final_state=fs, stream=stream)
+
+    t, launches, _ = time_device(step, steps, warmup, flush, stream)
+    rf = roofline(w, t, pk)
+    es = 4 if w.dtype == "f32" else 2
+    extra_bytes = w.batch * w.dim * w.L * es + w.dim * 4
+    gbs = (algorithmic(w)["bytes"] + extra_bytes) / t / 1e9
+    return {"workload": f"{w.name} + delta_bias + softplus + silu(z) gate", "ms": t * 1e3,
+            "value": w.channels * w.L / t, "unit": UNIT, "hbm_gbs": gbs, "bound": rf["bound"],
+            "frac_of_plain_roofline": rf["frac_of_roofline"], "plan": lr.last_plan(),
+            "launches_per_call": launches / steps}
+
+
 def bench_step(steps, warmup, dev, stream, flush, pk):
     """The single-step decode update on DECODE_WORKLOAD: HBM-bound on the fp32
     state (read + write 8 bytes per (b, d, n))."""
@@ -445,6 +474,8 @@ def main():
                          "hbm_gbs": rfx["hbm_gbs"], "bound": rfx["bound"],
                          "frac": rfx["frac"], "frac_of_roofline": rfx["frac_of_roofline"],
                          "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"]}
+        per["bf16_2k_fused"] = bench_fused(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3,
+                                           dev, stream, flush, pk)
         per["pscan_8k"] = bench_pscan(max(5, args.steps // 2), 3, dev, stream, flush)
         per["decode_step"] = bench_step(max(5, args.steps // 2), 3, dev, stream, flush, pk)
         extra["per_workload"] = per

@@ -102,6 +102,38 @@ int sscan_fwd_ex(const void *u, const void *delta, const float *A, const void *B
 int pscan(const float *a, const float *b, float *h, const float *h0,
           int64_t rows, int64_t len, void *stream);
 
+/* Option bits of sscan_fwd_fused. */
+#define SSCAN_DELTA_SOFTPLUS 1 /* delta <- softplus(delta (+ delta_bias)) inside the op */
+#define SSCAN_ZOH 2            /* zero-order-hold B-bar instead of delta*B               */
+
+/*
+ * sscan_fwd_fused -- sscan_fwd with the options the pages attach to the scan,
+ * each applied inside the same kernels (no extra pass over memory):
+ *
+ *   delta_bias [dim] float32 or NULL: delta <- delta + delta_bias[d];
+ *   SSCAN_DELTA_SOFTPLUS: then delta <- softplus(delta) = log(1 + e^delta)
+ *       (the F.softplus(delta) of the reference in "Mamba 状态空间模型：从理论到
+ *       生产级推理的 CUDA 内核优化实战" section 7.1; delta = softplus(Linear(x))
+ *       of its section 2.2);
+ *   SSCAN_ZOH: B-bar = (delta*A)^-1 (exp(delta*A) - 1) delta*B, i.e. per state
+ *       expm1(delta*A[d,n]) / A[d,n] * B (delta*B where A = 0): the
+ *       zero-order-hold discretisation of that page's section 1.2;
+ *   z [batch, dim, L] in the I/O dtype or NULL: out = (y + D*u) * silu(z),
+ *       silu(z) = z / (1 + e^-z), the output gate (the sigmoid gate activation
+ *       fused into the scan kernel on the "为什么Mamba的“并行扫描”不是真并行"
+ *       page, section 2, taken as Mamba's SiLU gate).
+ *
+ * The final state is that of the scan (the gate does not touch it).  segments
+ * and lanes pin the plan as in sscan_fwd_ex (0 = automatic).  Other arguments,
+ * layouts, ownership and errors are those of sscan_fwd; unknown flag bits are
+ * SSCAN_ERR_INVALID.
+ */
+int sscan_fwd_fused(const void *u, const void *delta, const float *A, const void *B,
+                    const void *C, const float *D, const void *z, const float *delta_bias,
+                    const float *h0, void *out, float *final_state, int64_t batch, int64_t dim,
+                    int64_t seqlen, int64_t dstate, int dtype, int flags, int segments, int lanes,
+                    void *stream);
+
 /*
  * sscan_step -- one autoregressive decode step: advance the cached state of
  * every (batch, channel) by one token and read it out (the recurrent

@@ -26,6 +26,7 @@ from ._build import LIB as LIB_PATH
 
 SSCAN_OK, SSCAN_ERR_INVALID, SSCAN_ERR_CUDA, SSCAN_ERR_TIMEOUT = 0, 1, 2, 3
 SSCAN_F32, SSCAN_BF16 = 0, 1
+SSCAN_DELTA_SOFTPLUS, SSCAN_ZOH = 1, 2
 
 _vp, _fp, _i64, _int = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _lock = threading.Lock()
@@ -37,6 +38,8 @@ SIGNATURES = {
                          _i64, _i64, _i64, _i64, _int, _vp]),
     "sscan_fwd_ex": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
                             _i64, _i64, _i64, _i64, _int, _int, _int, _vp]),
+    "sscan_fwd_fused": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _fp, _vp, _fp,
+                               _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp]),
     "sscan_fwd_noalloc": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
                                  _i64, _i64, _i64, _i64, _int, _int, _vp]),
     "sscan_step": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _int, _vp]),
@@ -124,10 +127,16 @@ def _check(t, name, shape, dtype, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, out=None, final_state=None,
+def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, z=None, delta_bias=None,
+              delta_softplus: bool = False, zoh: bool = False, out=None, final_state=None,
               return_final_state: bool = True, segments: int = 0, lanes: int = 0,
               stream=None):
     """Selective-scan forward on the GPU.  See the module docstring.
+
+    Options (all inside the same kernels): ``delta_bias`` [dim] float32 is
+    added to delta, ``delta_softplus`` then applies softplus to it, ``zoh``
+    uses the zero-order-hold B-bar, and ``z`` [batch, dim, L] (I/O dtype)
+    gates the output: out = (y + D*u) * silu(z).
 
     ``segments`` / ``lanes`` pin the launch plan (0 = automatic); the result is
     the same computation under any plan.  Returns ``(y, final_state)``
@@ -155,6 +164,10 @@ def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, out=None, final_state=None,
         _check(D, "D", (dim,), torch.float32, dev)
     if h0 is not None:
         _check(h0, "h0", (batch, dim, N), torch.float32, dev)
+    if z is not None:
+        _check(z, "z", (batch, dim, L), io, dev)
+    if delta_bias is not None:
+        _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
     if out is None:
         out = torch.empty((batch, dim, L), dtype=io, device=dev)
     else:
@@ -164,9 +177,16 @@ def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, out=None, final_state=None,
     elif final_state is not None:
         _check(final_state, "final_state", (batch, dim, N), torch.float32, dev)
     dtype = SSCAN_F32 if io == torch.float32 else SSCAN_BF16
-    rc = lib().sscan_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                            _ptr(h0), _ptr(out), _ptr(final_state), batch, dim, L, N,
-                            dtype, int(segments), int(lanes), _stream_handle(stream))
+    flags = (SSCAN_DELTA_SOFTPLUS if delta_softplus else 0) | (SSCAN_ZOH if zoh else 0)
+    if z is None and delta_bias is None and flags == 0:
+        rc = lib().sscan_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _ptr(h0), _ptr(out), _ptr(final_state), batch, dim, L, N,
+                                dtype, int(segments), int(lanes), _stream_handle(stream))
+    else:
+        rc = lib().sscan_fwd_fused(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                   _ptr(z), _ptr(delta_bias), _ptr(h0), _ptr(out),
+                                   _ptr(final_state), batch, dim, L, N, dtype, flags,
+                                   int(segments), int(lanes), _stream_handle(stream))
     if rc != SSCAN_OK:
         raise SscanError(rc, "sscan_fwd")
     return out, final_state

@@ -181,10 +181,10 @@ int sscan_get_last_error(void) {
     return status;
 }
 
-int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                 const float* D, const float* h0, void* out, float* final_state, int64_t batch,
-                 int64_t dim, int64_t seqlen, int64_t dstate, int dtype, int segments, int lanes,
-                 void* stream) {
+int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                    const float* D, const void* z, const float* delta_bias, const float* h0, void* out,
+                    float* final_state, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                    int dtype, int flags, int segments, int lanes, void* stream) {
     g_rec.launches = 0;
     snprintf(g_rec.plan, sizeof(g_rec.plan), "rejected");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -193,6 +193,7 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > sscan::kMaxDstate)
         return SSCAN_ERR_INVALID;
     if (segments < 0 || lanes < 0) return SSCAN_ERR_INVALID;
+    if (flags & ~(SSCAN_DELTA_SOFTPLUS | SSCAN_ZOH)) return SSCAN_ERR_INVALID;
     // every element index of every array must fit comfortably in int64 and
     // every grid in a 32-bit grid dimension
     const long long big = (long long)1 << 46;
@@ -222,7 +223,7 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     const int esz = f32 ? 4 : 2;
     const int vece = 16 / esz;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
-                     aligned16(C) && aligned16(out);
+                     aligned16(C) && aligned16(out) && (z == nullptr || aligned16(z));
     sscan::FwdPlan pl;
     const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
     if (prc != SSCAN_OK) return prc;
@@ -235,11 +236,16 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     p.batch = batch; p.dim = dim; p.L = seqlen; p.N = dstate;
     p.Tseg = pl.Tseg; p.S = (int)S; p.tiles_per_batch = (int)pl.tiles_per_batch;
     p.vec = vec ? 1 : 0;
+    p.z = z;
+    p.delta_bias = delta_bias;
+    p.delta_softplus = (flags & SSCAN_DELTA_SOFTPLUS) ? 1 : 0;
+    p.zoh = (flags & SSCAN_ZOH) ? 1 : 0;
 
     snprintf(g_rec.plan, sizeof(g_rec.plan),
-             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s", f32 ? "f32" : "bf16",
-             sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
-             S == 1 ? "single" : "local+correct");
+             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s",
+             f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
+             S == 1 ? "single" : "local+correct", delta_bias ? " bias" : "",
+             p.delta_softplus ? " softplus" : "", p.zoh ? " zoh" : "", z ? " gate" : "");
 
     cudaError_t e;
     if (S == 1) {
@@ -272,6 +278,14 @@ int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B
     if (e != cudaSuccess) return fail_cuda(e);
     if (ef != cudaSuccess) return fail_cuda(ef);
     return SSCAN_OK;
+}
+
+int sscan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const float* h0, void* out, float* final_state, int64_t batch,
+                 int64_t dim, int64_t seqlen, int64_t dstate, int dtype, int segments, int lanes,
+                 void* stream) {
+    return sscan_fwd_fused(u, delta, A, B, C, D, nullptr, nullptr, h0, out, final_state, batch, dim,
+                           seqlen, dstate, dtype, 0, segments, lanes, stream);
 }
 
 int sscan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,

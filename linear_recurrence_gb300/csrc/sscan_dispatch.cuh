@@ -1,7 +1,7 @@
 // Host-side dispatch from a runtime launch plan to the compiled kernel
 // variants, and the launch planner shared by the entry points.  The variants
-// are instantiated in four translation units (two per I/O dtype) so they
-// compile in parallel.
+// are instantiated in twelve translation units so that they compile in
+// parallel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -33,24 +33,48 @@ inline int shape_channels(Shape sh) { return shape_warps(sh) * (32 / sh.P) * sh.
 
 // Per-unit entry points: enqueue one kernel on `stream` (returns the launch
 // error, or cudaErrorInvalidValue for a shape the unit does not hold), and the
-// resident CTAs per SM of a shape (0 if unknown).
-cudaError_t fwd_launch_f32_a(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-cudaError_t fwd_launch_f32_b(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-cudaError_t fwd_launch_bf16_a(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-cudaError_t fwd_launch_bf16_b(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-int fwd_occupancy_f32_a(Shape sh);
-int fwd_occupancy_f32_b(Shape sh);
-int fwd_occupancy_bf16_a(Shape sh);
-int fwd_occupancy_bf16_b(Shape sh);
+// resident CTAs per SM of a shape (0 if unknown).  Units: I/O dtype x shape
+// group (a: P <= 4, b: P >= 8) x variant (e: the plain scan; o: with the
+// delta bias / softplus / gate options; z: options and the zero-order hold).
+#define SSCAN_DECLARE_UNIT(SUFFIX)                                                               \
+    cudaError_t fwd_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t stream); \
+    int fwd_occupancy_##SUFFIX(Shape sh);
+SSCAN_DECLARE_UNIT(f32_a_e)
+SSCAN_DECLARE_UNIT(f32_b_e)
+SSCAN_DECLARE_UNIT(bf16_a_e)
+SSCAN_DECLARE_UNIT(bf16_b_e)
+SSCAN_DECLARE_UNIT(f32_a_o)
+SSCAN_DECLARE_UNIT(f32_b_o)
+SSCAN_DECLARE_UNIT(bf16_a_o)
+SSCAN_DECLARE_UNIT(bf16_b_o)
+SSCAN_DECLARE_UNIT(f32_a_z)
+SSCAN_DECLARE_UNIT(f32_b_z)
+SSCAN_DECLARE_UNIT(bf16_a_z)
+SSCAN_DECLARE_UNIT(bf16_b_z)
+#undef SSCAN_DECLARE_UNIT
 
+// Kernel variant of a launch: 0 plain, 1 options, 2 options + zero-order hold.
+inline int fwd_variant(const FwdParams& p) {
+    if (p.zoh) return 2;
+    return (p.z != nullptr || p.delta_bias != nullptr || p.delta_softplus) ? 1 : 0;
+}
 inline cudaError_t fwd_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream) {
-    if (sh.P <= 4)
-        return f32 ? fwd_launch_f32_a(p, sh, grid, stream) : fwd_launch_bf16_a(p, sh, grid, stream);
-    return f32 ? fwd_launch_f32_b(p, sh, grid, stream) : fwd_launch_bf16_b(p, sh, grid, stream);
+    const bool a = sh.P <= 4;
+    switch (fwd_variant(p)) {
+        case 2:
+            if (f32) return a ? fwd_launch_f32_a_z(p, sh, grid, stream) : fwd_launch_f32_b_z(p, sh, grid, stream);
+            return a ? fwd_launch_bf16_a_z(p, sh, grid, stream) : fwd_launch_bf16_b_z(p, sh, grid, stream);
+        case 1:
+            if (f32) return a ? fwd_launch_f32_a_o(p, sh, grid, stream) : fwd_launch_f32_b_o(p, sh, grid, stream);
+            return a ? fwd_launch_bf16_a_o(p, sh, grid, stream) : fwd_launch_bf16_b_o(p, sh, grid, stream);
+        default:
+            if (f32) return a ? fwd_launch_f32_a_e(p, sh, grid, stream) : fwd_launch_f32_b_e(p, sh, grid, stream);
+            return a ? fwd_launch_bf16_a_e(p, sh, grid, stream) : fwd_launch_bf16_b_e(p, sh, grid, stream);
+    }
 }
 inline int fwd_occupancy(bool f32, Shape sh) {
-    if (sh.P <= 4) return f32 ? fwd_occupancy_f32_a(sh) : fwd_occupancy_bf16_a(sh);
-    return f32 ? fwd_occupancy_f32_b(sh) : fwd_occupancy_bf16_b(sh);
+    if (sh.P <= 4) return f32 ? fwd_occupancy_f32_a_e(sh) : fwd_occupancy_bf16_a_e(sh);
+    return f32 ? fwd_occupancy_f32_b_e(sh) : fwd_occupancy_bf16_b_e(sh);
 }
 
 // A launch plan of the forward pass (defined in sscan_abi.cu).
@@ -69,10 +93,10 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
 
 // Shared implementation, included by the per-unit translation units only.
 #ifdef SSCAN_DISPATCH_IMPL
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 static cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
-    auto kern = sscan_fwd_chunked<T, NS, P, CPL>;
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
+    auto kern = sscan_fwd_chunked<T, NS, P, CPL, OPT>;
     // the state slots of a shape must cover every state: the kernel stages
     // B/C rows n < N into NSP slots
     if (p.N < 1 || p.N > (long long)Cfg::NSP) return cudaErrorInvalidValue;
@@ -91,10 +115,10 @@ static cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t str
     return cudaGetLastError();
 }
 
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 static int occupancy_variant() {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
-    auto kern = sscan_fwd_chunked<T, NS, P, CPL>;
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
+    auto kern = sscan_fwd_chunked<T, NS, P, CPL, OPT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
         cudaSuccess)
         return 0;
@@ -105,13 +129,13 @@ static int occupancy_variant() {
     return n;
 }
 
-// A unit sets `using UnitT = float;` (or bf16) and then expands
-// SSCAN_DEFINE_UNIT(f32_a, SSCAN_SHAPES_A) and so on.
+// A unit sets `using UnitT = float;` (or bf16) and `constexpr int UnitOPT`, then
+// expands SSCAN_DEFINE_UNIT(f32_a_e, SSCAN_SHAPES_A) and so on.
 #define SSCAN_LAUNCH_CASE(P_, NS_, CPL_)                                   \
     if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_)                      \
-        return launch_variant<UnitT, NS_, P_, CPL_>(p, grid, st);
+        return launch_variant<UnitT, NS_, P_, CPL_, UnitOPT>(p, grid, st);
 #define SSCAN_OCC_CASE(P_, NS_, CPL_)                                      \
-    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_variant<UnitT, NS_, P_, CPL_>();
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_variant<UnitT, NS_, P_, CPL_, UnitOPT>();
 #define SSCAN_DEFINE_UNIT(SUFFIX, SHAPES)                                                       \
     cudaError_t fwd_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t st) { \
         SHAPES(SSCAN_LAUNCH_CASE)                                                               \

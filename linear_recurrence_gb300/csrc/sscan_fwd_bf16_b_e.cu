@@ -1,0 +1,11 @@
+// bfloat16-I/O variants of the selective-scan kernel (lanes per channel >= 8), the plain scan.
+#define SSCAN_DISPATCH_IMPL
+#include "sscan_dispatch.cuh"
+
+namespace sscan {
+
+using UnitT = bf16;
+constexpr int UnitOPT = 0;
+SSCAN_DEFINE_UNIT(bf16_b_e, SSCAN_SHAPES_B)
+
+}  // namespace sscan

@@ -1,0 +1,11 @@
+// float32-I/O variants of the selective-scan kernel (lanes per channel <= 4), the plain scan.
+#define SSCAN_DISPATCH_IMPL
+#include "sscan_dispatch.cuh"
+
+namespace sscan {
+
+using UnitT = float;
+constexpr int UnitOPT = 0;
+SSCAN_DEFINE_UNIT(f32_a_e, SSCAN_SHAPES_A)
+
+}  // namespace sscan

@@ -1,0 +1,11 @@
+// float32-I/O variants of the selective-scan kernel (lanes per channel >= 8), with the options and the zero-order-hold B-bar.
+#define SSCAN_DISPATCH_IMPL
+#include "sscan_dispatch.cuh"
+
+namespace sscan {
+
+using UnitT = float;
+constexpr int UnitOPT = 2;
+SSCAN_DEFINE_UNIT(f32_b_z, SSCAN_SHAPES_B)
+
+}  // namespace sscan

@@ -66,7 +66,32 @@ struct FwdParams {
     int mode;
     int seg_count;     // segments covered by this grid: grid = tiles * seg_count
     int vec;           // rows are 16-byte aligned: cp.async staging, vector stores
+    const void* z;            // [batch, dim, L] output gate (out *= silu(z)), or NULL
+    const float* delta_bias;  // [dim] added to delta, or NULL
+    int delta_softplus;       // delta <- softplus(delta (+ bias)) inside the op
+    int zoh;                  // zero-order-hold B-bar (the kernel's ZOH variant)
 };
+
+// delta as the scan uses it: delta + bias, then softplus when asked for
+__device__ __forceinline__ float delta_in(float x, float bias, bool softplus) {
+    x += bias;
+    return softplus ? (x > 20.f ? x : log1pf(expf(x))) : x;
+}
+
+// Zero-order-hold B-bar per unit B, (exp(delta*A) - 1) / A, given the exponent
+// argument y = delta*A*log2(e), a = 2^y and invA = 1/A (0 when A = 0).  Where
+// |delta*A| < 1/16 the difference a - 1 would cancel, so there the series
+// delta*(1 + x/2 + x^2/6 + x^3/24), x = delta*A, is used (truncation below
+// 2e-7 relative); A = 0 gives delta, the Euler value.
+__device__ __forceinline__ float zoh_coef(float dt, float y, float a, float invA) {
+    const float x = y * 0.69314718055994531f;
+    if (fabsf(x) < 0.0625f)
+        return dt * fmaf(x, fmaf(x, fmaf(x, 1.f / 24.f, 1.f / 6.f), 0.5f), 1.f);
+    return (a - 1.f) * invA;
+}
+
+// silu(z) = z * sigmoid(z), the output gate
+__device__ __forceinline__ float silu(float z) { return z / (1.f + ex2(-z * 1.4426950408889634f)); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 #ifndef SSCAN_CHUNK_STEPS
@@ -84,7 +109,7 @@ constexpr int warps_for(int P, int CPL) {
     return (16 * P) / (32 * CPL) < 2 ? 2 : ((16 * P) / (32 * CPL) > 8 ? 8 : (16 * P) / (32 * CPL));
 }
 
-template <typename T, int NS_, int P_, int CPL_>
+template <typename T, int NS_, int P_, int CPL_, int OPT_ = 0>
 struct FwdCfg {
     static constexpr int NS = NS_;
     static constexpr int P = P_;
@@ -101,7 +126,9 @@ struct FwdCfg {
     static constexpr int RROW = TC + VECE;            // raw row (T), padded by 16 bytes
     static constexpr int FROW = TC + 4;               // fp32 row, padded by 16 bytes
     static constexpr int PPR = TC / VECE;             // 16-byte pieces per row
-    static constexpr int ROWS = 2 * DT + 2 * NSP;     // u, delta, B, C
+    static constexpr int OPT = OPT_;                  // 0 plain; 1 options; 2 options + zero-order hold
+    static constexpr int ROWS = (OPT > 0 ? 3 : 2) * DT + 2 * NSP;  // u, delta, B, C (, z)
+    static constexpr int ZROW0 = 2 * DT + 2 * NSP;    // first z row (options only)
     static constexpr int RAW_ELEMS = ROWS * RROW;
     static constexpr int RAW_BYTES = RAW_ELEMS * (int)sizeof(T);
     static constexpr int STAGES = 3;
@@ -160,9 +187,9 @@ __device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, 
 // Shared memory: raw ring [STAGES][ROWS][RROW] (T, cp.async targets), then the
 // fp32 work rows [ROWS][FROW] (bf16 only), then the partial outputs [DT][RS].
 // Rows: u [0, DT), delta [DT, 2DT), B [2DT, 2DT+NSP), C [2DT+NSP, 2DT+2NSP).
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 struct Smem {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     T* raw;
     float* work;
     float* yp;
@@ -180,16 +207,17 @@ struct Smem {
 
 // Vector path: issue this thread's 16-byte cp.async pieces of chunk [t0, t0+TC)
 // into stage st.  Out-of-range pieces are zero-filled (delta = 0 keeps the state).
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long b, long long d0,
                                             long long t0, long long t_end, int tid, bool load_u,
                                             bool load_b, bool load_c) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
     const T* gu = static_cast<const T*>(p.u);
     const T* gd = static_cast<const T*>(p.delta);
     const T* gB = static_cast<const T*>(p.B);
     const T* gC = static_cast<const T*>(p.C);
+    const T* gz = static_cast<const T*>(p.z);
     for (int q = tid; q < DT * PPR; q += Cfg::kThreads) {
         const int r = q / PPR, pc = q % PPR;
         const long long t = t0 + (long long)pc * VE;
@@ -198,6 +226,8 @@ __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long
         const long long off = (b * p.dim + (ok ? dd : 0)) * p.L + (ok ? t : 0);
         if (load_u) cp_async16(st + r * RROW + pc * VE, gu + off, ok ? 16 : 0);
         cp_async16(st + (DT + r) * RROW + pc * VE, gd + off, ok ? 16 : 0);
+        if constexpr (OPT > 0)
+            if (gz != nullptr) cp_async16(st + (Cfg::ZROW0 + r) * RROW + pc * VE, gz + off, ok ? 16 : 0);
     }
     const int N = (int)p.N;
     for (int q = tid; q < N * PPR; q += Cfg::kThreads) {
@@ -211,31 +241,72 @@ __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long
 }
 
 // bf16 vector path: widen a landed stage to the fp32 work rows (after a barrier,
-// since a thread widens pieces other threads copied).
-template <typename T, int NS, int P, int CPL>
-__device__ __forceinline__ void widen_stage(const T* st, float* wk, int nrows_bc, int tid) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
-    constexpr int DT = Cfg::DT, RROW = Cfg::RROW, FROW = Cfg::FROW, TC = Cfg::TC;
-    // rows 0 .. 2DT-1 (u, delta), then B rows 2DT .. 2DT+N-1 and C rows 2DT+NSP ..
-    constexpr int Q4 = TC / 4;  // 4-element groups per row
-    const int nr = 2 * DT + 2 * nrows_bc;
-    for (int q = tid; q < nr * Q4; q += Cfg::kThreads) {
-        int r = q / Q4;
-        const int c = (q % Q4) * 4;
-        if (r >= 2 * DT + nrows_bc) r += Cfg::NSP - nrows_bc;  // C block
-        float v[4];
-        load4_smem(st + r * RROW + c, v);
-        *reinterpret_cast<float4*>(wk + r * FROW + c) = make_float4(v[0], v[1], v[2], v[3]);
+// since a thread widens pieces other threads copied), one 16-byte piece (8
+// values) per item.  Rows: u and delta [0, 2DT), B [2DT, 2DT+N),
+// C [2DT+NSP, 2DT+NSP+N), z [ZROW0, ZROW0+DT) when gated.  delta is
+// transformed (bias, softplus) on the way, except in padding.
+__device__ __forceinline__ void widen8(const bf16* src, float* dst) {
+    const uint4 q = *reinterpret_cast<const uint4*>(src);
+    *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                                                  __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xffff0000u),
+                                                      __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xffff0000u));
+}
+
+template <typename T, int NS, int P, int CPL, int OPT>
+__device__ __forceinline__ void widen_stage(const FwdParams& p, const T* st, float* wk, long long d0,
+                                            long long t0, long long t_end, int tid) {
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
+    constexpr int DT = Cfg::DT, RROW = Cfg::RROW, FROW = Cfg::FROW, TC = Cfg::TC, NSP = Cfg::NSP;
+    constexpr int Q8 = TC / 8;  // 16-byte pieces per row
+    const int N = (int)p.N;
+    // u and delta rows
+    for (int q = tid; q < 2 * DT * Q8; q += Cfg::kThreads) {
+        const int r = q / Q8, c = (q % Q8) * 8;
+        widen8(st + r * RROW + c, wk + r * FROW + c);
+    }
+    // B and C rows of the N states
+    for (int q = tid; q < 2 * N * Q8; q += Cfg::kThreads) {
+        const int k = q / Q8, c = (q % Q8) * 8;
+        const int r = 2 * DT + (k < N ? k : NSP + (k - N));
+        widen8(st + r * RROW + c, wk + r * FROW + c);
+    }
+    if constexpr (OPT > 0) {
+        if (p.z != nullptr)
+            for (int q = tid; q < DT * Q8; q += Cfg::kThreads) {
+                const int r = Cfg::ZROW0 + q / Q8, c = (q % Q8) * 8;
+                widen8(st + r * RROW + c, wk + r * FROW + c);
+            }
+    }
+}
+
+// delta transform (bias, softplus) of a chunk's fp32 delta rows in place (the
+// stage itself for fp32 I/O, the widened rows for bf16);
+// padding (channels beyond dim, steps beyond the segment) stays 0 so that it
+// keeps the state.  Runs after the rows are visible to every thread.
+template <typename T, int NS, int P, int CPL, int OPT>
+__device__ __forceinline__ void transform_delta_rows(const FwdParams& p, float* rows, long long d0,
+                                                     long long t0, long long t_end, int tid) {
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
+    constexpr int DT = Cfg::DT, FROW = Cfg::FROW, TC = Cfg::TC;
+    for (int q = tid; q < DT * TC; q += Cfg::kThreads) {
+        const int r = q / TC, tt = q % TC;
+        const long long dd = d0 + r;
+        if (dd < p.dim && t0 + tt < t_end) {
+            const float bias = p.delta_bias != nullptr ? p.delta_bias[dd] : 0.f;
+            float& v = rows[(DT + r) * FROW + tt];
+            v = delta_in(v, bias, p.delta_softplus != 0);
+        }
     }
 }
 
 // Scalar path (rows not 16-byte aligned): element loads with bounds checks
 // straight into the fp32 rows the lanes read.
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* rows, long long b,
                                                   long long d0, long long t0, long long t_end, int tid,
                                                   bool load_u, bool load_b, bool load_c) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, NSP = Cfg::NSP;
     const T* gu = static_cast<const T*>(p.u);
     const T* gd = static_cast<const T*>(p.delta);
@@ -247,7 +318,16 @@ __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* row
         const bool ok = dd < p.dim && t < t_end;
         const long long off = (b * p.dim + dd) * p.L + t;
         if (load_u) rows[r * FROW + tt] = ok ? to_f32(gu[off]) : 0.f;
-        rows[(DT + r) * FROW + tt] = ok ? to_f32(gd[off]) : 0.f;
+        float dv = 0.f;
+        if (ok) {
+            dv = to_f32(gd[off]);
+            if (OPT > 0 && (p.delta_softplus != 0 || p.delta_bias != nullptr))
+                dv = delta_in(dv, p.delta_bias != nullptr ? p.delta_bias[dd] : 0.f, p.delta_softplus != 0);
+        }
+        rows[(DT + r) * FROW + tt] = dv;
+        if constexpr (OPT > 0)
+            if (p.z != nullptr)
+                rows[(Cfg::ZROW0 + r) * FROW + tt] = ok ? to_f32(static_cast<const T*>(p.z)[off]) : 0.f;
     }
     const int N = (int)p.N;
     for (int q = tid; q < N * TC; q += Cfg::kThreads) {
@@ -270,12 +350,13 @@ __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* row
 // the homogeneous recurrence h = a*h of the carry correction (u and B are not
 // read; D is not added).  Returns the chunk's sum of delta per channel when
 // DSUM.
-template <typename T, int NS, int P, int CPL, bool WRITE_Y, bool SCALAR, bool DSUM, bool NO_B>
+template <typename T, int NS, int P, int CPL, int OPT, bool WRITE_Y, bool SCALAR, bool DSUM, bool NO_B, bool ZOH>
 __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, const int (&rr)[CPL], int g,
                                               const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                              const float (&invA)[CPL][NS], const float (&invAs)[CPL],
                                               float (&h)[CPL][NS], const float (&Dl)[CPL],
                                               float (&csum)[CPL]) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, NSP = Cfg::NSP, RS = Cfg::RS;
     constexpr int QS = NS < 4 ? NS : 4;  // states per quad
     constexpr int NQ = NS / QS;
@@ -294,16 +375,22 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
             if (!NO_B) load4_smem(su + rr[j] * FROW + t4, uu[j]);
             load4_smem(sd + rr[j] * FROW + t4, dd[j]);
         }
-        // terms of a (channel, step) shared by all its states
+        // terms of a (channel, step) shared by all its states.  du is the
+        // input factor of B: delta*u (Euler), u (general zero-order hold, whose
+        // factor is per state) or B-bar/B * u (zero-order hold, shared rate)
         float du[CPL][4], as[CPL][4], y[CPL][4];
 #pragma unroll
         for (int j = 0; j < CPL; ++j)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 if (DSUM) csum[j] += dd[j][s];
-                du[j][s] = NO_B ? 0.f : dd[j][s] * uu[j][s];
+                const float ys = dd[j][s] * As[j];
+                as[j][s] = SCALAR ? ex2(ys) : 0.f;
+                if (NO_B) du[j][s] = 0.f;
+                else if (!ZOH) du[j][s] = dd[j][s] * uu[j][s];
+                else if (SCALAR) du[j][s] = zoh_coef(dd[j][s], ys, as[j][s], invAs[j]) * uu[j][s];
+                else du[j][s] = uu[j][s];
                 y[j][s] = NO_B ? 0.f : Dl[j] * uu[j][s];
-                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
             }
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
@@ -321,9 +408,16 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
 #pragma unroll
                     for (int kk = 0; kk < QS; ++kk) {
                         const int k = q * QS + kk;
-                        const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
-                        if (NO_B) h[j][k] = a * h[j][k];
-                        else h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[kk][s]);
+                        const float yk = dd[j][s] * Al2[j][k];
+                        const float a = SCALAR ? as[j][s] : ex2(yk);
+                        if (NO_B) {
+                            h[j][k] = a * h[j][k];
+                        } else if (ZOH && !SCALAR) {
+                            const float c = zoh_coef(dd[j][s], yk, a, invA[j][k]);
+                            h[j][k] = fmaf(a, h[j][k], (c * du[j][s]) * bb[kk][s]);
+                        } else {
+                            h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[kk][s]);
+                        }
                         if (WRITE_Y) y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
                     }
         }
@@ -338,11 +432,11 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
 
 // Sum the P partials of every output of the chunk and store it (CORR: add it to
 // the output already written).  Item q covers 4 steps of tile row q % DT.
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp, const float* yloc,
-                                            long long b, long long d0, long long t0, long long t_end, int tid,
-                                            bool corr, bool vec) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
+                                            const float* zrows, long long b, long long d0, long long t0,
+                                            long long t_end, int tid, bool corr, bool vec) {
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, RS = Cfg::RS;
     T* go = static_cast<T*>(p.out);
     for (int q = tid; q < DT * (TC / 4); q += Cfg::kThreads) {
@@ -357,6 +451,12 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
             load4_smem(yp + r * RS + gg * FROW + t4, w);
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] += w[e];
+        }
+        if (OPT > 0 && zrows != nullptr) {  // out = (y + D*u) * silu(z); a correction is gated alike
+            float zv[4];
+            load4_smem(zrows + r * FROW + t4, zv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] *= silu(zv[e]);
         }
         if (corr) {  // the local outputs of the chunk, staged in the u rows
             float w[4];
@@ -384,14 +484,14 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
     }
 }
 
-template <typename T, int NS, int P, int CPL>
-__global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chunked(const FwdParams p) {
-    using Cfg = FwdCfg<T, NS, P, CPL>;
+template <typename T, int NS, int P, int CPL, int OPT>
+__global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fwd_chunked(const FwdParams p) {
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, NSP = Cfg::NSP, STAGES = Cfg::STAGES;
     constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    const Smem<T, NS, P, CPL> sm(smem_raw);
+    const Smem<T, NS, P, CPL, OPT> sm(smem_raw);
 
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane % P, gi = lane / P;
@@ -418,6 +518,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chu
     long long ch[CPL];
     bool dval[CPL];
     float Al2[CPL][NS], As[CPL], Dl[CPL], h[CPL][NS];
+    float invA[CPL][NS], invAs[CPL];  // 1/A (0 where A = 0), for the zero-order hold
     bool uniform_rate = true;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
@@ -433,8 +534,10 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chu
             const float a = nv ? p.A[dch * p.N + n] : a_first;
             uniform_rate &= (a == a_first);
             Al2[j][k] = nv ? a * kLog2e : 0.f;
+            invA[j][k] = (nv && a != 0.f) ? 1.f / a : 0.f;
         }
         As[j] = a_first * kLog2e;
+        invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
         Dl[j] = (!corr && g == 0 && p.D != nullptr && dval[j]) ? p.D[dch] : 0.f;
         if (corr) {
             fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
@@ -498,7 +601,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chu
 #pragma unroll
         for (int j = 0; j < STAGES - 1; ++j) {
             if (j < nchunks)
-                issue_chunk<T, NS, P, CPL>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid,
+                issue_chunk<T, NS, P, CPL, OPT>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid,
                                            load_u, load_b, load_c);
             cp_async_commit();
         }
@@ -513,7 +616,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chu
             cp_async_wait<STAGES - 2>();
         } else {
             __syncthreads();  // the previous chunk's readers are done with the rows
-            load_chunk_scalar<T, NS, P, CPL>(q, sm.rows(i), b, d0, t0, t_end, tid, load_u, load_b, load_c);
+            load_chunk_scalar<T, NS, P, CPL, OPT>(q, sm.rows(i), b, d0, t0, t_end, tid, load_u, load_b, load_c);
         }
         if (corr) {
             bool live = false;
@@ -527,28 +630,35 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chu
         }
         if constexpr (!Cfg::kF32) {
             if (vec) {
-                widen_stage<T, NS, P, CPL>(sm.stage(i), sm.work, N, tid);
+                widen_stage<T, NS, P, CPL, OPT>(p, sm.stage(i), sm.work, d0, t0, t_end, tid);
+                __syncthreads();
+            }
+        }
+        // (the scalar loader applies the delta transform as it loads)
+        if constexpr (OPT > 0) {
+            if (vec && (p.delta_softplus != 0 || p.delta_bias != nullptr)) {
+                transform_delta_rows<T, NS, P, CPL, OPT>(p, sm.rows(i), d0, t0, t_end, tid);
                 __syncthreads();
             }
         }
         if (vec) {
             const int nx = i + STAGES - 1;
             if (nx < nchunks)
-                issue_chunk<T, NS, P, CPL>(q, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid,
+                issue_chunk<T, NS, P, CPL, OPT>(q, sm.stage(nx), b, d0, t_begin + (long long)nx * TC, t_end, tid,
                                            load_u, load_b, load_c);
             cp_async_commit();
         }
         float csum[CPL];
         const float* rows = sm.rows(i);
         if (corr) {
-            if (scalar) compute_chunk<T, NS, P, CPL, true, true, false, true>(rows, sm.yp, rr, g, Al2, As, h, Dl, csum);
-            else compute_chunk<T, NS, P, CPL, true, false, false, true>(rows, sm.yp, rr, g, Al2, As, h, Dl, csum);
+            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, false, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
+            else compute_chunk<T, NS, P, CPL, OPT, true, false, false, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
         } else if (dsum_on) {
-            if (scalar) compute_chunk<T, NS, P, CPL, true, true, true, false>(rows, sm.yp, rr, g, Al2, As, h, Dl, csum);
-            else compute_chunk<T, NS, P, CPL, true, false, true, false>(rows, sm.yp, rr, g, Al2, As, h, Dl, csum);
+            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, true, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
+            else compute_chunk<T, NS, P, CPL, OPT, true, false, true, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
         } else {
-            if (scalar) compute_chunk<T, NS, P, CPL, true, true, false, false>(rows, sm.yp, rr, g, Al2, As, h, Dl, csum);
-            else compute_chunk<T, NS, P, CPL, true, false, false, false>(rows, sm.yp, rr, g, Al2, As, h, Dl, csum);
+            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, false, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
+            else compute_chunk<T, NS, P, CPL, OPT, true, false, false, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
         }
         if (dsum_on) {
 #pragma unroll
@@ -560,7 +670,8 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL>::kThreads) sscan_fwd_chu
             }
         }
         __syncthreads();  // every lane's partials of the chunk are in place
-        store_chunk<T, NS, P, CPL>(p, sm.yp, rows, b, d0, t0, t_end, tid, corr, vec);
+        store_chunk<T, NS, P, CPL, OPT>(p, sm.yp, rows, (OPT > 0 && p.z != nullptr) ? rows + Cfg::ZROW0 * Cfg::FROW : nullptr, b,
+                                   d0, t0, t_end, tid, corr, vec);
     }
     cp_async_wait<0>();
     if (corr) return;

@@ -33,7 +33,8 @@ def lr():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for f in ("sscan_fwd", "sscan_fwd_ex", "sscan_step", "pscan", "sscan_status_string",
+    for f in ("sscan_fwd", "sscan_fwd_ex", "sscan_fwd_fused", "sscan_step", "pscan",
+              "sscan_status_string",
               "sscan_get_last_error", "sscan_max_dstate", "sscan_last_launch_count",
               "sscan_last_plan"):
         assert f in names, f
@@ -85,6 +86,11 @@ def test_invalid_calls_return_before_any_cuda_call(lr):
     # sizes whose element count overflows
     assert raw.sscan_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
                          1 << 40, 1 << 40, 1 << 20, 16, 0, None) == lr.SSCAN_ERR_INVALID
+    # unknown option bits, missing pointer with options
+    assert raw.sscan_fwd_fused(fake, fake, fake, fake, fake, None, None, None, None, fake, None,
+                               1, 1, 8, 16, 0, 4, 0, 0, None) == lr.SSCAN_ERR_INVALID
+    assert raw.sscan_fwd_fused(fake, None, fake, fake, fake, None, fake, fake, None, fake, None,
+                               1, 1, 8, 16, 0, 3, 0, 0, None) == lr.SSCAN_ERR_INVALID
     assert raw.sscan_step(fake, fake, fake, fake, fake, None, None, fake, 1, 1, 4, 0, None) == \
         lr.SSCAN_ERR_INVALID
     assert raw.sscan_step(fake, fake, fake, fake, fake, None, fake, fake, 1, 1, 65, 0, None) == \

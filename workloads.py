@@ -120,6 +120,23 @@ def make_inputs(w: Workload, seed: int | None = None):
     }
 
 
+def make_option_inputs(w: Workload):
+    """Inputs of the scan's options for workload ``w`` (a generator of its own,
+    seeded ``w.seed + 100``, so the plain inputs stay as they are): the raw
+    delta before softplus ~ N(delta_mu, delta_sigma) in the I/O dtype (its
+    softplus has the plain recipe's distribution), a per-channel delta bias
+    ~ N(0, 0.1^2) float32, and the gate z ~ N(0, 1) in the I/O dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 100)
+    shp = (w.batch, w.dim, w.L)
+    raw = torch.randn(shp, generator=g, dtype=torch.float32) * w.delta_sigma + w.delta_mu
+    bias = torch.randn((w.dim,), generator=g, dtype=torch.float32) * 0.1
+    z = torch.randn(shp, generator=g, dtype=torch.float32)
+    dt = io_dtype(w.dtype)
+    return {"delta_raw": raw.to(dt).contiguous(), "delta_bias": bias.contiguous(),
+            "z": z.to(dt).contiguous()}
+
+
 @dataclass(frozen=True)
 class PscanWorkload:
     name: str
