@@ -19,6 +19,8 @@ follows:
   zero-order-hold B-bar of its section 1.2, and an output gate
   (y + D*u) * silu(z) (the gate activation fused into the scan kernel on the
   "为什么Mamba的“并行扫描”不是真并行" page, section 2).
+* :func:`sscan_bwd` -- the gradients of :func:`sscan_fwd` by the chain rule in
+  reverse time (the backward pass of "并行扫描与硬件感知优化", section 3.3).
 * :func:`pscan_seq` -- h_t = a_t*h_{t-1} + b_t row by row (the ``pscan``
   primitive of that listing; with a = 1 the prefix sum of its section 1.1).
 * :func:`pscan_blelloch` -- the same recurrence by Blelloch up-sweep /
@@ -76,6 +78,10 @@ def _load():
             _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
             _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_sscan_fwd_full_mutant.restype = ctypes.c_int
+        lib.oracle_sscan_bwd_mutant.argtypes = [_dp] * 16 + [_i64, _i64, _i64, _i64, ctypes.c_int]
+        lib.oracle_sscan_bwd_mutant.restype = ctypes.c_int
+        lib.oracle_bwd_mutation_count.argtypes = []
+        lib.oracle_bwd_mutation_count.restype = ctypes.c_int
         lib.oracle_mutation_count.argtypes = []
         lib.oracle_mutation_count.restype = ctypes.c_int
         lib.oracle_pscan_seq.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64]
@@ -187,6 +193,38 @@ def sscan_fwd_full(u, delta, A, B, C, D=None, z=None, delta_bias=None, h0=None, 
     if rc != 0:
         raise ValueError(f"oracle_sscan_fwd_full rejected its arguments ({rc})")
     return y, hT
+
+
+def bwd_mutation_count() -> int:
+    return int(_load().oracle_bwd_mutation_count())
+
+
+def sscan_bwd(u, delta, A, B, C, D, h0, dy, dhT=None, *, mutation: int = 0):
+    """Gradients of the selective scan in float64 (the chain rule on the forward
+    recurrence in reverse time; the C function's header states the formulas).
+
+    dy [batch, dim, L] is dL/dy, dhT [batch, dim, N] dL/d(final_state) (None =
+    0).  Returns a dict with du, ddelta [batch, dim, L]; dA [dim, N]; dB, dC
+    [batch, N, L]; dD [dim] (None when D is None); dh0 [batch, dim, N].
+    """
+    u, delta, A, B, C, dy = map(_f64, (u, delta, A, B, C, dy))
+    D, h0, dhT = _f64(D), _f64(h0), _f64(dhT)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    if dy.shape != u.shape:
+        raise ValueError("dy must be [batch, dim, L]")
+    if dhT is not None and dhT.shape != (batch, dim, N):
+        raise ValueError("dhT must be [batch, dim, N]")
+    out = {"du": np.zeros((batch, dim, L)), "ddelta": np.zeros((batch, dim, L)),
+           "dA": np.zeros((dim, N)), "dB": np.zeros((batch, N, L)), "dC": np.zeros((batch, N, L)),
+           "dD": None if D is None else np.zeros(dim), "dh0": np.zeros((batch, dim, N))}
+    rc = _load().oracle_sscan_bwd_mutant(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(dy), _ptr(dhT),
+        _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+        _ptr(out["dD"]), _ptr(out["dh0"]), batch, dim, L, N, int(mutation))
+    if rc != 0:
+        raise ValueError("oracle_sscan_bwd rejected its arguments")
+    return out
 
 
 def sscan_fwd_channels(u, delta, A, B, C, D, h0, channels, *, nthreads: int = 1):

@@ -363,3 +363,102 @@ int oracle_pscan_blelloch(const double *a, const double *b, double h0, double *h
     free(eb);
     return 0;
 }
+
+/*
+ * oracle_sscan_bwd: gradients of the selective scan (the backward pass whose
+ * recompute strategy "并行扫描与硬件感知优化 (mhpq.cn/news/1077344)" section
+ * 3.3 describes).  Given the forward of oracle_sscan_fwd and the upstream
+ * gradients dy [batch, dim, L] and dhT [batch, dim, N] (NULL = 0) of the
+ * outputs y and final_state, it returns the gradients of every input, by the
+ * chain rule on the forward recurrence taken in reverse time:
+ *
+ *   g_t[n]   = dL/dh_t[n] = C[b,n,t]*dy_t + a_{t+1}[n]*g_{t+1}[n],
+ *              g_{L-1} = C*dy + dhT                      (a_t = exp(delta_t*A[d,n]))
+ *   ddelta_t = sum_n g_t[n]*(h_{t-1}[n]*a_t[n]*A[d,n] + u_t*B[b,n,t])
+ *   du_t     = sum_n g_t[n]*delta_t*B[b,n,t] + D[d]*dy_t
+ *   dB[b,n,t] += g_t[n]*delta_t*u_t         (summed over d)
+ *   dC[b,n,t] += dy_t*h_t[n]                (summed over d)
+ *   dA[d,n]   += g_t[n]*h_{t-1}[n]*a_t[n]*delta_t   (summed over b, t)
+ *   dD[d]     += dy_t*u_t                   (summed over b, t)
+ *   dh0[n]    = a_0[n]*g_0[n]
+ *
+ * The forward states are kept for every step (plain and slow).  Outputs are
+ * overwritten: du, ddelta [batch, dim, L]; dA [dim, N]; dB, dC [batch, N, L];
+ * dD [dim] and dh0 [batch, dim, N] may be NULL.  Returns 0, or -1 on bad
+ * sizes.  BWD mutations plant deliberate slips for the oracle's own pins.
+ */
+enum {
+    BMUT_NONE = 0,
+    BMUT_NO_CARRY_DECAY = 1, /* g_t = C*dy + g_{t+1} (a_{t+1} dropped)       */
+    BMUT_HT_FOR_HPREV = 2,   /* use h_t instead of h_{t-1} in dL/da_t       */
+    BMUT_DU_NO_D = 3,        /* forget D*dy in du                            */
+    BMUT_DB_NO_U = 4,        /* dB = g*delta (u dropped)                     */
+    BMUT_DH0_NO_DECAY = 5,   /* dh0 = g_0                                    */
+    BMUT_COUNT = 6
+};
+
+int oracle_bwd_mutation_count(void) { return BMUT_COUNT; }
+
+int oracle_sscan_bwd_mutant(const double *u, const double *delta, const double *A,
+                            const double *B, const double *C, const double *D,
+                            const double *h0, const double *dy, const double *dhT,
+                            double *du, double *ddelta, double *dA, double *dB, double *dC,
+                            double *dD, double *dh0, int64_t batch, int64_t dim, int64_t L,
+                            int64_t N, int mutation)
+{
+    if (batch < 0 || dim < 0 || L < 0 || N < 0) return -1;
+    if (mutation < 0 || mutation >= BMUT_COUNT) return -1;
+    memset(dA, 0, sizeof(double) * (size_t)(dim * N));
+    memset(dB, 0, sizeof(double) * (size_t)(batch * N * L));
+    memset(dC, 0, sizeof(double) * (size_t)(batch * N * L));
+    if (dD) memset(dD, 0, sizeof(double) * (size_t)dim);
+    const size_t nh = (size_t)(L + 1) * (size_t)(N > 0 ? N : 1);
+    double *hs = (double *)malloc(nh * sizeof(double)); /* hs[(t+1)*N + n] = h_t, hs[n] = h_{-1} */
+    double *g = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t ch = b * dim + d;
+            const double *uu = u + ch * L, *dl = delta + ch * L, *dyy = dy + ch * L;
+            const double *Ad = A + d * N, *Bb = B + b * N * L, *Cb = C + b * N * L;
+            for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[ch * N + n] : 0.0;
+            for (int64_t t = 0; t < L; ++t)
+                for (int64_t n = 0; n < N; ++n)
+                    hs[(t + 1) * N + n] = exp(dl[t] * Ad[n]) * hs[t * N + n] + dl[t] * Bb[n * L + t] * uu[t];
+            for (int64_t n = 0; n < N; ++n) g[n] = dhT ? dhT[ch * N + n] : 0.0; /* G_{L-1} */
+            for (int64_t t = L - 1; t >= 0; --t) {
+                double sdu = 0.0, sdd = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double a = exp(dl[t] * Ad[n]);
+                    const double gt = Cb[n * L + t] * dyy[t] + g[n];
+                    const double hprev = (mutation == BMUT_HT_FOR_HPREV) ? hs[(t + 1) * N + n] : hs[t * N + n];
+                    sdd += gt * (hprev * a * Ad[n] + uu[t] * Bb[n * L + t]);
+                    sdu += gt * dl[t] * Bb[n * L + t];
+                    dB[b * N * L + n * L + t] += gt * dl[t] * ((mutation == BMUT_DB_NO_U) ? 1.0 : uu[t]);
+                    dC[b * N * L + n * L + t] += dyy[t] * hs[(t + 1) * N + n];
+                    dA[d * N + n] += gt * hprev * a * dl[t];
+                    g[n] = (mutation == BMUT_NO_CARRY_DECAY) ? gt : a * gt; /* G_{t-1} */
+                    if (t == 0 && dh0) dh0[ch * N + n] = (mutation == BMUT_DH0_NO_DECAY) ? gt : a * gt;
+                }
+                if (D && mutation != BMUT_DU_NO_D) sdu += D[d] * dyy[t];
+                du[ch * L + t] = sdu;
+                ddelta[ch * L + t] = sdd;
+                if (dD && D) dD[d] += dyy[t] * uu[t];
+            }
+            if (L == 0 && dh0)
+                for (int64_t n = 0; n < N; ++n) dh0[ch * N + n] = dhT ? dhT[ch * N + n] : 0.0;
+        }
+    }
+    free(hs);
+    free(g);
+    return 0;
+}
+
+int oracle_sscan_bwd(const double *u, const double *delta, const double *A, const double *B,
+                     const double *C, const double *D, const double *h0, const double *dy,
+                     const double *dhT, double *du, double *ddelta, double *dA, double *dB,
+                     double *dC, double *dD, double *dh0, int64_t batch, int64_t dim, int64_t L,
+                     int64_t N)
+{
+    return oracle_sscan_bwd_mutant(u, delta, A, B, C, D, h0, dy, dhT, du, ddelta, dA, dB, dC,
+                                   dD, dh0, batch, dim, L, N, BMUT_NONE);
+}

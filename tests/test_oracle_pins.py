@@ -465,6 +465,78 @@ def test_options_off_is_the_plain_scan():
     assert np.array_equal(y0, y1) and np.array_equal(h0r, h1)
 
 
+# ------------------------------------------------- pins of the gradients
+# The backward oracle is pinned to central finite differences of the forward
+# oracle (itself pinned above) on the loss L = sum dy*y + sum dhT*final_state.
+
+
+def _fd_gradients(u, delta, A, B, C, D, h0, dy, dhT, eps=1e-6):
+    args = {"u": u, "delta": delta, "A": A, "B": B, "C": C, "D": D, "h0": h0}
+
+    def loss(a):
+        y, hT = oracle.sscan_fwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["h0"])
+        return float(np.sum(dy * y) + np.sum(dhT * hT))
+
+    grads = {}
+    for name, x in args.items():
+        gx = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            e = eps * max(1.0, abs(x[idx]))
+            xp = x.copy()
+            xp[idx] += e
+            xm = x.copy()
+            xm[idx] -= e
+            gx[idx] = (loss({**args, name: xp}) - loss({**args, name: xm})) / (2 * e)
+        grads[name] = gx
+    return grads
+
+
+def pin_bwd_finite_differences(bwd):
+    """Every gradient of the scan against central finite differences."""
+    u, delta, A, B, C, D, h0 = _rand_problem(41, batch=2, dim=2, L=6, N=3)
+    r = _rng(42)
+    dy = r.normal(size=u.shape)
+    dhT = r.normal(size=h0.shape)
+    fd = _fd_gradients(u, delta, A, B, C, D, h0, dy, dhT)
+    g = bwd(u, delta, A, B, C, D, h0, dy, dhT)
+    pairs = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "h0": "dh0"}
+    for x, gname in pairs.items():
+        err = np.max(np.abs(g[gname] - fd[x]) / (1 + np.abs(fd[x])))
+        if err > 1e-6:
+            return f"{gname} vs finite differences: {err:.2e}"
+    return None
+
+
+def pin_bwd_no_upstream_is_zero(bwd):
+    """dy = 0 and dhT = 0 give zero gradients everywhere."""
+    u, delta, A, B, C, D, h0 = _rand_problem(43)
+    g = bwd(u, delta, A, B, C, D, h0, np.zeros_like(u), np.zeros_like(h0))
+    if any(np.any(v != 0) for v in g.values() if v is not None):
+        return "nonzero gradient without upstream gradient"
+    return None
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_no_upstream_is_zero]
+
+
+def _bwd_callable(mutation=0):
+    def f(u, delta, A, B, C, D, h0, dy, dhT):
+        return oracle.sscan_bwd(u, delta, A, B, C, D, h0, dy, dhT, mutation=mutation)
+    return f
+
+
+@pytest.mark.parametrize("pin", BWD_PINS, ids=lambda p: p.__name__)
+def test_oracle_bwd_pin(pin):
+    msg = pin(_bwd_callable())
+    assert msg is None, msg
+
+
+def test_every_planted_bwd_mistake_is_caught():
+    for m in range(1, oracle.bwd_mutation_count()):
+        failed = [p.__name__ for p in BWD_PINS if p(_bwd_callable(m)) is not None]
+        assert failed, f"planted backward mistake {m} passed every pin"
+
+
 def test_threaded_oracle_equals_single_thread():
     u, delta, A, B, C, D, h0 = _rand_problem(19, batch=3, dim=5, L=33, N=4)
     y1, h1 = oracle.sscan_fwd(u, delta, A, B, C, D, h0, nthreads=1)
