@@ -324,6 +324,41 @@ def bench_fused(w, steps, warmup, dev, stream, flush, pk):
             "launches_per_call": launches / steps}
 
 
+def bench_bwd(w, steps, warmup, dev, stream, flush, pk, t_fwd):
+    """The backward pass (sscan_bwd) on workload ``w`` with random upstream
+    gradients of y and the final state.  Algorithmic work per element: the
+    recomputed state (1 ex2, 4 FP32) and the reverse sweep (1 ex2, 12 FP32);
+    bytes: read u, delta, dy, B, C, A, D, h0 and the final-state gradient, write
+    du, ddelta (I/O dtype), dB, dC (fp32), dA, dD, dh0."""
+    import torch
+    import linear_recurrence_gb300 as lr
+    x = workloads.make_inputs(w)
+    g = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    gen = torch.Generator().manual_seed(w.seed + 200)
+    dy = torch.randn((w.batch, w.dim, w.L), generator=gen).to(workloads.io_dtype(w.dtype)).to(dev)
+    dhT = torch.randn((w.batch, w.dim, w.N), generator=gen).to(dev)
+
+    def step():
+        lr.sscan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["h0"], dy, dhT, stream=stream)
+
+    t, launches, _ = time_device(step, steps, warmup, flush, stream)
+    es = 4 if w.dtype == "f32" else 2
+    bdl, bnl, dn = w.batch * w.dim * w.L, w.batch * w.N * w.L, w.dim * w.N
+    nbytes = (5 * bdl * es + 2 * bnl * es + 2 * bnl * 4 + 2 * dn * 4 + 2 * w.dim * 4
+              + 2 * w.batch * w.dim * w.N * 4 + (w.batch * w.dim * w.N * 4 if w.h0_std > 0 else 0))
+    elems = bdl * w.N
+    clk = pk["sm_max_mhz"] * 1e6
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_exp = 2 * elems / (MUFU_PER_CLK_SM * SM_COUNT * clk)
+    t_fp32 = 16 * elems / (FP32_PER_CLK_SM * SM_COUNT * clk)
+    t_roof = max(t_hbm, t_exp, t_fp32)
+    return {"workload": f"{w.name} backward (sscan_bwd)", "ms": t * 1e3, "value": bdl / t, "unit": UNIT,
+            "hbm_gbs": nbytes / t / 1e9, "bound": "hbm" if t_hbm >= max(t_exp, t_fp32) else "alu",
+            "frac_of_roofline": t_roof / t, "t_roofline_us": t_roof * 1e6,
+            "bwd_over_fwd": t / t_fwd if t_fwd else None, "plan": lr.last_plan(),
+            "launches_per_call": launches / steps}
+
+
 def bench_step(steps, warmup, dev, stream, flush, pk):
     """The single-step decode update on DECODE_WORKLOAD: HBM-bound on the fp32
     state (read + write 8 bytes per (b, d, n))."""
@@ -474,6 +509,8 @@ def main():
                          "hbm_gbs": rfx["hbm_gbs"], "bound": rfx["bound"],
                          "frac": rfx["frac"], "frac_of_roofline": rfx["frac_of_roofline"],
                          "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"]}
+        per["bf16_2k_bwd"] = bench_bwd(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3, dev,
+                                       stream, flush, pk, per.get("bf16_2k", {}).get("ms", 0) * 1e-3)
         per["bf16_2k_fused"] = bench_fused(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3,
                                            dev, stream, flush, pk)
         per["pscan_8k"] = bench_pscan(max(5, args.steps // 2), 3, dev, stream, flush)

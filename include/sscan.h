@@ -135,6 +135,34 @@ int sscan_fwd_fused(const void *u, const void *delta, const float *A, const void
                     void *stream);
 
 /*
+ * sscan_bwd -- gradients of sscan_fwd (no options), the backward pass with the
+ * chunk-boundary recompute of "并行扫描与硬件感知优化 (mhpq.cn/news/1077344)"
+ * section 3.3: the state at every 16-step boundary is kept in library scratch
+ * (batch*dim*ceil(L/16)*N floats, stream-ordered), and each chunk's states are
+ * recomputed from it during the reverse sweep.  For upstream gradients
+ * dy = dL/dy and dfinal_state = dL/d(final state) (a_t = exp(delta_t*A[d,n])):
+ *
+ *   g_t      = C_t*dy_t + a_{t+1}*g_{t+1},  g_{L-1} = C*dy + dfinal_state
+ *   ddelta_t = sum_n g_t*(h_{t-1}*a_t*A + u_t*B_t)
+ *   du_t     = sum_n g_t*delta_t*B_t + D*dy_t
+ *   dB[b,n,t] = sum_d g_t*delta_t*u_t,  dC[b,n,t] = sum_d dy_t*h_t
+ *   dA[d,n]   = sum_{b,t} g_t*h_{t-1}*a_t*delta_t,  dD[d] = sum_{b,t} dy_t*u_t
+ *   dh0       = a_0*g_0
+ *
+ * Inputs are those of sscan_fwd plus dy [batch, dim, L] (I/O dtype) and
+ * dfinal_state [batch, dim, N] float32 or NULL (zero).  Outputs (device,
+ * caller-owned, overwritten): du, ddelta [batch, dim, L] in the I/O dtype;
+ * dA [dim, N], dB and dC [batch, N, L] float32; dD [dim] float32 (ignored when
+ * D is NULL; may be NULL); dh0 [batch, dim, N] float32 or NULL.  dA, dB, dC and
+ * dD are sums over channels or batches accumulated with float atomics, so
+ * their rounding order is not fixed.  Errors as sscan_fwd.
+ */
+int sscan_bwd(const void *u, const void *delta, const float *A, const void *B, const void *C,
+              const float *D, const float *h0, const void *dy, const float *dfinal_state,
+              void *du, void *ddelta, float *dA, float *dB, float *dC, float *dD, float *dh0,
+              int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void *stream);
+
+/*
  * sscan_step -- one autoregressive decode step: advance the cached state of
  * every (batch, channel) by one token and read it out (the recurrent
  * inference step whose state cache "Mamba 状态空间模型：从理论到生产级推理的

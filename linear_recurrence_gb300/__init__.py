@@ -42,6 +42,8 @@ SIGNATURES = {
                                _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp]),
     "sscan_fwd_noalloc": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp,
                                  _i64, _i64, _i64, _i64, _int, _int, _vp]),
+    "sscan_bwd": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _fp, _vp, _vp, _fp, _fp, _fp, _fp,
+                         _fp, _i64, _i64, _i64, _i64, _int, _vp]),
     "sscan_step": (_int, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _int, _vp]),
     "pscan": (_int, [_fp, _fp, _fp, _fp, _i64, _i64, _vp]),
     "sscan_status_string": (ctypes.c_char_p, [_int]),
@@ -192,6 +194,50 @@ def sscan_fwd(u, delta, A, B, C, D=None, h0=None, *, z=None, delta_bias=None,
     return out, final_state
 
 
+def sscan_bwd(u, delta, A, B, C, D, h0, dy, dfinal_state=None, *, stream=None):
+    """Gradients of :func:`sscan_fwd` (no options) for upstream gradients ``dy``
+    [batch, dim, L] (I/O dtype) and ``dfinal_state`` [batch, dim, N] float32
+    (None = 0).  Returns a dict with du, ddelta (I/O dtype), dA, dB, dC, dD (None
+    when D is None) and dh0 (float32)."""
+    if u.dim() != 3:
+        raise ValueError("u must be [batch, dim, L]")
+    batch, dim, L = u.shape
+    if A.dim() != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("sscan_bwd runs on CUDA tensors only")
+    io = u.dtype
+    if io not in (torch.float32, torch.bfloat16):
+        raise ValueError("u must be float32 or bfloat16")
+    for t, name, shape, dt in ((u, "u", (batch, dim, L), io), (delta, "delta", (batch, dim, L), io),
+                               (A, "A", (dim, N), torch.float32), (B, "B", (batch, N, L), io),
+                               (C, "C", (batch, N, L), io), (dy, "dy", (batch, dim, L), io)):
+        _check(t, name, shape, dt, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (batch, dim, N), torch.float32, dev)
+    if dfinal_state is not None:
+        _check(dfinal_state, "dfinal_state", (batch, dim, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"du": torch.empty((batch, dim, L), dtype=io, device=dev),
+         "ddelta": torch.empty((batch, dim, L), dtype=io, device=dev),
+         "dA": torch.empty((dim, N), **f32), "dB": torch.empty((batch, N, L), **f32),
+         "dC": torch.empty((batch, N, L), **f32),
+         "dD": None if D is None else torch.empty((dim,), **f32),
+         "dh0": torch.empty((batch, dim, N), **f32)}
+    dtype = SSCAN_F32 if io == torch.float32 else SSCAN_BF16
+    rc = lib().sscan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(dy),
+                         _ptr(dfinal_state), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]),
+                         _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dh0"]),
+                         batch, dim, L, N, dtype, _stream_handle(stream))
+    if rc != SSCAN_OK:
+        raise SscanError(rc, "sscan_bwd")
+    return g
+
+
 def sscan_step(u, delta, A, B, C, D=None, *, state, out=None, stream=None):
     """One decode step: advances ``state`` [batch, dim, N] (float32, in place)
     by one token and returns y [batch, dim].  u, delta: [batch, dim]; B, C:
@@ -251,6 +297,6 @@ def pscan(a, b, h0=None, *, out=None, stream=None):
     return out
 
 
-__all__ = ["sscan_fwd", "sscan_step", "pscan", "status_string", "get_last_error", "max_dstate",
+__all__ = ["sscan_fwd", "sscan_bwd", "sscan_step", "pscan", "status_string", "get_last_error", "max_dstate",
            "last_launch_count", "last_plan", "load_library", "SscanError",
            "SIGNATURES", "LIB_PATH"]

@@ -1,0 +1,467 @@
+// Backward pass of the selective scan for sm_103a, with chunk-boundary
+// recompute: only the state at every chunk boundary is kept, and the states
+// inside a chunk are recomputed from it when the reverse sweep reaches the
+// chunk (the recompute strategy of "并行扫描与硬件感知优化
+// (mhpq.cn/news/1077344)" section 3.3).
+//
+// For the loss gradients dy = dL/dy and dhT = dL/d(final state), per batch b,
+// channel d, state n and step t (a_t = exp(delta_t*A[d,n])):
+//   g_t      = C_t*dy_t + a_{t+1}*g_{t+1},  g_{L-1} = C*dy + dhT   (dL/dh_t)
+//   ddelta_t = sum_n g_t*(h_{t-1}*a_t*A + u_t*B_t)
+//   du_t     = sum_n g_t*delta_t*B_t + D*dy_t
+//   dB_t    += g_t*delta_t*u_t,  dC_t += dy_t*h_t        (summed over channels)
+//   dA      += g_t*h_{t-1}*a_t*delta_t,  dD += dy_t*u_t  (summed over batch, time)
+//   dh0      = a_0*g_0
+//
+// One CTA of 4 warps owns DT channels of one batch for the whole sequence.
+// P lanes share a channel, lane g owning states n = k*P + g (NS of them).
+// Phase 1 runs the forward recurrence once and writes the state at every
+// chunk boundary to global scratch.  Phase 2 walks the chunks backwards: it
+// stages u, delta, dy, B and C of the chunk in shared memory (cp.async, two
+// stages, in reverse order), recomputes the chunk's states from its boundary
+// state into lane-private shared memory, then sweeps the chunk in reverse,
+// carrying G = a_{t+1}*g_{t+1} in registers.  Per-step sums over a channel's
+// states (du, ddelta) and over the CTA's channels (dB, dC) go through shared
+// memory partials; dB and dC are accumulated into float32 outputs with
+// atomic adds, dA and dD once per lane at the end.
+#pragma once
+
+#include "device_utils.cuh"
+
+namespace sscan {
+
+struct BwdParams {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;      // [dim] or NULL
+    const float* h0;     // [batch, dim, N] or NULL
+    const void* dy;      // [batch, dim, L]
+    const float* dhT;    // [batch, dim, N] or NULL
+    void* du;            // [batch, dim, L]  I/O dtype
+    void* ddelta;        // [batch, dim, L]  I/O dtype
+    float* dA;           // [dim, N]       accumulated (zeroed by the host)
+    float* dB;           // [batch, N, L]  accumulated (zeroed by the host)
+    float* dC;           // [batch, N, L]  accumulated (zeroed by the host)
+    float* dD;           // [dim] or NULL, accumulated (zeroed by the host)
+    float* dh0;          // [batch, dim, N] or NULL
+    float* ckpt;         // [batch*dim, nchunks, N]: state before each chunk
+    long long batch, dim, L, N;
+    int tiles_per_batch;
+    int vec;             // rows 16-byte aligned: cp.async staging, vector stores
+};
+
+constexpr int kBwdChunk = 16;  // steps per chunk (and checkpoint spacing)
+
+template <typename T, int NS_, int P_>
+struct BwdCfg {
+    static constexpr int NS = NS_;
+    static constexpr int P = P_;
+    static constexpr int kWarps = 4;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int GPW = 32 / P;
+    static constexpr int DT = kWarps * GPW;           // channels per CTA
+    static constexpr int NSP = NS * P;                // state slots per channel
+    static constexpr int TC = kBwdChunk;
+    static constexpr bool kF32 = sizeof(T) == 4;
+    static constexpr int VECE = 16 / (int)sizeof(T);
+    static constexpr int RROW = TC + VECE;            // raw row (T), padded by 16 bytes
+    static constexpr int FROW = TC + 4;               // fp32 row, padded by 16 bytes
+    static constexpr int PPR = TC / VECE;             // 16-byte pieces per row
+    // rows: u [0,DT), delta [DT,2DT), dy [2DT,3DT), B [3DT,3DT+NSP), C [3DT+NSP, 3DT+2NSP)
+    static constexpr int ROWS = 3 * DT + 2 * NSP;
+    static constexpr int RAW_ELEMS = ROWS * RROW;
+    static constexpr int RAW_BYTES = RAW_ELEMS * (int)sizeof(T);
+    static constexpr int STAGES = 2;
+    static constexpr int WORK_FLOATS = kF32 ? 0 : ROWS * FROW;
+    static constexpr int HB_FLOATS = TC * NS * kThreads;   // lane-private recomputed states
+    // per-step partial sums: du, ddelta over the P lanes of a channel
+    // [2][DT][P][FROW] (channel stride RS), dB, dC over the channels
+    // [2][NSP][DT][FROW] (state stride RSB); RS/4 and RSB/4 odd keep the
+    // epilogue's quarter-warp reads in distinct banks
+    static constexpr int RS = ((P * FROW / 4) % 2 == 1) ? P * FROW : P * FROW + 4;
+    static constexpr int RSB = ((DT * FROW / 4) % 2 == 1) ? DT * FROW : DT * FROW + 4;
+    static constexpr int PU_FLOATS = 2 * DT * RS;
+    static constexpr int PB_FLOATS = 2 * NSP * RSB;
+    static constexpr int SMEM_BYTES =
+        STAGES * RAW_BYTES + (WORK_FLOATS + HB_FLOATS + PU_FLOATS + PB_FLOATS) * 4;
+    static_assert(RROW * sizeof(T) % 16 == 0, "smem rows must stay 16-byte aligned");
+    static_assert(!kF32 || RROW == FROW, "fp32 lanes read the raw rows");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// Stage chunk [t0, t0+TC) of one CTA.  Phase 1 needs only u, delta and B.
+template <typename T, int NS, int P>
+__device__ __forceinline__ void bwd_issue(const BwdParams& p, T* st, long long b, long long d0,
+                                          long long t0, int tid, bool full) {
+    using Cfg = BwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
+    const T* gu = static_cast<const T*>(p.u);
+    const T* gd = static_cast<const T*>(p.delta);
+    const T* gy = static_cast<const T*>(p.dy);
+    const T* gB = static_cast<const T*>(p.B);
+    const T* gC = static_cast<const T*>(p.C);
+    for (int q = tid; q < DT * PPR; q += Cfg::kThreads) {
+        const int r = q / PPR, pc = q % PPR;
+        const long long t = t0 + (long long)pc * VE;
+        const long long dd = d0 + r;
+        const bool ok = dd < p.dim && t < p.L;
+        const long long off = (b * p.dim + (ok ? dd : 0)) * p.L + (ok ? t : 0);
+        cp_async16(st + r * RROW + pc * VE, gu + off, ok ? 16 : 0);
+        cp_async16(st + (DT + r) * RROW + pc * VE, gd + off, ok ? 16 : 0);
+        if (full) cp_async16(st + (2 * DT + r) * RROW + pc * VE, gy + off, ok ? 16 : 0);
+    }
+    const int N = (int)p.N;
+    for (int q = tid; q < N * PPR; q += Cfg::kThreads) {
+        const int n = q / PPR, pc = q % PPR;
+        const long long t = t0 + (long long)pc * VE;
+        const bool ok = t < p.L;
+        const long long off = (b * p.N + n) * p.L + (ok ? t : 0);
+        cp_async16(st + (3 * DT + n) * RROW + pc * VE, gB + off, ok ? 16 : 0);
+        if (full) cp_async16(st + (3 * DT + NSP + n) * RROW + pc * VE, gC + off, ok ? 16 : 0);
+    }
+}
+
+// Element loads with bounds checks straight into fp32 rows (unaligned rows).
+template <typename T, int NS, int P>
+__device__ __forceinline__ void bwd_load_scalar(const BwdParams& p, float* rows, long long b, long long d0,
+                                                long long t0, int tid, bool full) {
+    using Cfg = BwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, NSP = Cfg::NSP;
+    const T* gu = static_cast<const T*>(p.u);
+    const T* gd = static_cast<const T*>(p.delta);
+    const T* gy = static_cast<const T*>(p.dy);
+    const T* gB = static_cast<const T*>(p.B);
+    const T* gC = static_cast<const T*>(p.C);
+    for (int q = tid; q < DT * TC; q += Cfg::kThreads) {
+        const int r = q / TC, tt = q % TC;
+        const long long dd = d0 + r, t = t0 + tt;
+        const bool ok = dd < p.dim && t < p.L;
+        const long long off = (b * p.dim + dd) * p.L + t;
+        rows[r * FROW + tt] = ok ? to_f32(gu[off]) : 0.f;
+        rows[(DT + r) * FROW + tt] = ok ? to_f32(gd[off]) : 0.f;
+        if (full) rows[(2 * DT + r) * FROW + tt] = ok ? to_f32(gy[off]) : 0.f;
+    }
+    const int N = (int)p.N;
+    for (int q = tid; q < N * TC; q += Cfg::kThreads) {
+        const int n = q / TC, tt = q % TC;
+        const long long t = t0 + tt;
+        const bool ok = t < p.L;
+        const long long off = (b * p.N + n) * p.L + t;
+        rows[(3 * DT + n) * FROW + tt] = ok ? to_f32(gB[off]) : 0.f;
+        if (full) rows[(3 * DT + NSP + n) * FROW + tt] = ok ? to_f32(gC[off]) : 0.f;
+    }
+}
+
+// bf16: widen a landed stage (all rows but the unused B/C slots >= N)
+template <typename T, int NS, int P>
+__device__ __forceinline__ void bwd_widen(const T* st, float* wk, int N, int tid) {
+    using Cfg = BwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, RROW = Cfg::RROW, FROW = Cfg::FROW, TC = Cfg::TC, NSP = Cfg::NSP;
+    constexpr int Q4 = TC / 4;
+    const int nr = 3 * DT + 2 * N;
+    for (int q = tid; q < nr * Q4; q += Cfg::kThreads) {
+        int r = q / Q4;
+        const int c = (q % Q4) * 4;
+        if (r >= 3 * DT + N) r += NSP - N;
+        float v[4];
+        load4_smem(st + r * RROW + c, v);
+        *reinterpret_cast<float4*>(wk + r * FROW + c) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+template <typename T, int NS, int P>
+__global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(const BwdParams p) {
+    using Cfg = BwdCfg<T, NS, P>;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, NSP = Cfg::NSP, FROW = Cfg::FROW, RROW = Cfg::RROW;
+    constexpr int STAGES = Cfg::STAGES, NT = Cfg::kThreads, RS = Cfg::RS, RSB = Cfg::RSB;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* raw = reinterpret_cast<T*>(smem_raw);
+    float* work = reinterpret_cast<float*>(smem_raw + STAGES * Cfg::RAW_BYTES);
+    float* hb = work + Cfg::WORK_FLOATS;
+    float* pu = hb + Cfg::HB_FLOATS;   // [du|ddelta][DT][RS]
+    float* pb = pu + Cfg::PU_FLOATS;   // [dB|dC][NSP][RSB]
+    auto stage = [&](int i) { return raw + (i % STAGES) * Cfg::RAW_ELEMS; };
+    auto rows_of = [&](int i) -> float* {
+        if constexpr (Cfg::kF32) return reinterpret_cast<float*>(stage(i));
+        else return work;
+    };
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int g = lane % P, gi = lane / P;
+    const int r = w * Cfg::GPW + gi;  // the lane's channel row in the tile
+    const bool vec = p.vec != 0;
+    const long long b = blockIdx.x / p.tiles_per_batch;
+    const long long d0 = (long long)(blockIdx.x % p.tiles_per_batch) * DT;
+    const long long dch = d0 + r;
+    const bool dval = dch < p.dim;
+    const long long ch = b * p.dim + (dval ? dch : 0);
+    const int N = (int)p.N;
+    const int nchunks = (int)((p.L + TC - 1) / TC);
+
+    float A[NS], Al2[NS], h[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        const int n = k * P + g;
+        const bool nv = dval && n < N;
+        A[k] = nv ? p.A[dch * p.N + n] : 0.f;
+        Al2[k] = A[k] * 1.4426950408889634f;
+        h[k] = (nv && p.h0 != nullptr) ? p.h0[ch * p.N + n] : 0.f;
+    }
+    const float Dd = (dval && p.D != nullptr) ? p.D[dch] : 0.f;
+
+    // B/C rows of state slots >= N are never copied: zero them once
+    if (N < NSP) {
+        const int nz = NSP - N;
+        for (int q = tid; q < 2 * nz * TC; q += NT) {
+            const int rz = q / TC, tt = q % TC;
+            const int row = 3 * DT + (rz < nz ? N + rz : NSP + N + (rz - nz));
+            if constexpr (Cfg::kF32) {
+#pragma unroll
+                for (int st = 0; st < STAGES; ++st) stage(st)[row * RROW + tt] = 0.f;
+            } else {
+                work[row * FROW + tt] = 0.f;
+            }
+        }
+    }
+
+    // ---- phase 1: forward sweep, state before every chunk -> ckpt
+    float* ck = p.ckpt + ch * (long long)nchunks * p.N;
+    if (vec) {
+        bwd_issue<T, NS, P>(p, stage(0), b, d0, 0, tid, false);
+        cp_async_commit();
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        if (vec) {
+            if (c + 1 < nchunks) bwd_issue<T, NS, P>(p, stage(c + 1), b, d0, (long long)(c + 1) * TC, tid, false);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            bwd_load_scalar<T, NS, P>(p, rows_of(c), b, d0, (long long)c * TC, tid, false);
+        }
+        __syncthreads();
+        if constexpr (!Cfg::kF32) {
+            if (vec) {
+                bwd_widen<T, NS, P>(stage(c), work, N, tid);
+                __syncthreads();
+            }
+        }
+        if (dval) {
+#pragma unroll
+            for (int k = 0; k < NS; ++k)
+                if (k * P + g < N) ck[(long long)c * p.N + k * P + g] = h[k];
+        }
+        const float* rows = rows_of(c);
+        const float* su = rows + r * FROW;
+        const float* sd = rows + (DT + r) * FROW;
+        const float* sB = rows + (3 * DT + g) * FROW;
+#pragma unroll 2
+        for (int t4 = 0; t4 < TC; t4 += 4) {
+            float uu[4], dd[4];
+            load4_smem(su + t4, uu);
+            load4_smem(sd + t4, dd);
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                float bb[4];
+                load4_smem(sB + k * P * FROW + t4, bb);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) h[k] = fmaf(ex2(dd[s] * Al2[k]), h[k], (dd[s] * uu[s]) * bb[s]);
+            }
+        }
+        __syncthreads();  // the rows of chunk c are free for the next copy
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- phase 2: reverse sweep over the chunks
+    float G[NS], dAacc[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        const int n = k * P + g;
+        G[k] = (dval && n < N && p.dhT != nullptr) ? p.dhT[ch * p.N + n] : 0.f;
+        dAacc[k] = 0.f;
+    }
+    float dDacc = 0.f;
+    if (vec) {
+        bwd_issue<T, NS, P>(p, stage(nchunks - 1), b, d0, (long long)(nchunks - 1) * TC, tid, true);
+        cp_async_commit();
+    }
+    for (int c = nchunks - 1; c >= 0; --c) {
+        const long long t0 = (long long)c * TC;
+        if (vec) {
+            if (c > 0) bwd_issue<T, NS, P>(p, stage(c - 1), b, d0, t0 - TC, tid, true);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            bwd_load_scalar<T, NS, P>(p, rows_of(c), b, d0, t0, tid, true);
+        }
+        __syncthreads();
+        if constexpr (!Cfg::kF32) {
+            if (vec) {
+                bwd_widen<T, NS, P>(stage(c), work, N, tid);
+                __syncthreads();
+            }
+        }
+        const float* rows = rows_of(c);
+        const float* su = rows + r * FROW;
+        const float* sd = rows + (DT + r) * FROW;
+        const float* sy = rows + (2 * DT + r) * FROW;
+        const float* sB = rows + (3 * DT + g) * FROW;
+        const float* sC = rows + (3 * DT + NSP + g) * FROW;
+
+        // recompute the chunk's states from its boundary state (lane-private,
+        // 4 steps of a state per float4: hb[(t4/4 * NS + k) * NT + tid])
+        float hs[NS];
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int n = k * P + g;
+            hs[k] = (dval && n < N) ? ck[(long long)c * p.N + n] : 0.f;
+            h[k] = hs[k];
+        }
+#pragma unroll 2
+        for (int t4 = 0; t4 < TC; t4 += 4) {
+            float uu[4], dd[4];
+            load4_smem(su + t4, uu);
+            load4_smem(sd + t4, dd);
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                float bb[4], hv[4];
+                load4_smem(sB + k * P * FROW + t4, bb);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    h[k] = fmaf(ex2(dd[s] * Al2[k]), h[k], (dd[s] * uu[s]) * bb[s]);
+                    hv[s] = h[k];
+                }
+                *reinterpret_cast<float4*>(hb + ((t4 / 4) * NS + k) * NT * 4 + tid * 4) =
+                    make_float4(hv[0], hv[1], hv[2], hv[3]);
+            }
+        }
+
+        // reverse sweep, 4 steps at a time
+#pragma unroll 1
+        for (int t4 = TC - 4; t4 >= 0; t4 -= 4) {
+            float uu[4], dd[4], dyv[4];
+            load4_smem(su + t4, uu);
+            load4_smem(sd + t4, dd);
+            load4_smem(sy + t4, dyv);
+            float sdu[4] = {0.f, 0.f, 0.f, 0.f}, sdd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                float bb[4], cc[4], hv[4];
+                load4_smem(sB + k * P * FROW + t4, bb);
+                load4_smem(sC + k * P * FROW + t4, cc);
+                load4_smem(hb + ((t4 / 4) * NS + k) * NT * 4 + tid * 4, hv);
+                float hp;  // h at the step before t4
+                if (t4 > 0) hp = hb[(((t4 - 4) / 4) * NS + k) * NT * 4 + tid * 4 + 3];
+                else hp = hs[k];
+                float pbv[4], pcv[4];
+#pragma unroll
+                for (int s = 3; s >= 0; --s) {
+                    const float hprev = s > 0 ? hv[s - 1] : hp;
+                    const float a = ex2(dd[s] * Al2[k]);
+                    const float gt = fmaf(cc[s], dyv[s], G[k]);
+                    const float gha = (gt * hprev) * a;
+                    dAacc[k] = fmaf(gha, dd[s], dAacc[k]);
+                    const float gb = gt * bb[s];
+                    sdd[s] = fmaf(gha, A[k], fmaf(gb, uu[s], sdd[s]));
+                    sdu[s] = fmaf(gb, dd[s], sdu[s]);
+                    pbv[s] = gt * (dd[s] * uu[s]);
+                    pcv[s] = dyv[s] * hv[s];
+                    G[k] = a * gt;
+                }
+                const int n = k * P + g;
+                *reinterpret_cast<float4*>(pb + n * RSB + r * FROW + t4) = make_float4(pbv[0], pbv[1], pbv[2], pbv[3]);
+                *reinterpret_cast<float4*>(pb + NSP * RSB + n * RSB + r * FROW + t4) =
+                    make_float4(pcv[0], pcv[1], pcv[2], pcv[3]);
+            }
+            if (g == 0) {
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    sdu[s] = fmaf(Dd, dyv[s], sdu[s]);
+                    dDacc = fmaf(dyv[s], uu[s], dDacc);
+                }
+            }
+            *reinterpret_cast<float4*>(pu + r * RS + g * FROW + t4) = make_float4(sdu[0], sdu[1], sdu[2], sdu[3]);
+            *reinterpret_cast<float4*>(pu + DT * RS + r * RS + g * FROW + t4) =
+                make_float4(sdd[0], sdd[1], sdd[2], sdd[3]);
+        }
+        __syncthreads();  // every partial of the chunk is in place
+
+        // epilogue: du, ddelta (sum over the P lanes of a channel)
+        T* gdu = static_cast<T*>(p.du);
+        T* gdd = static_cast<T*>(p.ddelta);
+        for (int q = tid; q < 2 * DT * (TC / 4); q += NT) {
+            const int which = q / (DT * (TC / 4));
+            const int qq = q % (DT * (TC / 4));
+            const int rr = qq % DT, t4 = (qq / DT) * 4;
+            const long long dd = d0 + rr, t = t0 + t4;
+            if (dd >= p.dim || t >= p.L) continue;
+            const float* src = pu + which * DT * RS + rr * RS;
+            float v[4];
+            load4_smem(src + t4, v);
+#pragma unroll
+            for (int gg = 1; gg < P; ++gg) {
+                float x[4];
+                load4_smem(src + gg * FROW + t4, x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] += x[e];
+            }
+            T* o = (which ? gdd : gdu) + (b * p.dim + dd) * p.L + t;
+            if (vec) {
+                if constexpr (Cfg::kF32) {
+                    *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+                    const unsigned lo = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[0])) |
+                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[1])) << 16);
+                    const unsigned hi = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[2])) |
+                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[3])) << 16);
+                    *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (t + e < p.L) o[e] = from_f32<T>(v[e]);
+            }
+        }
+        // epilogue: dB, dC (sum over the CTA's channels, then one atomic add)
+        for (int q = tid; q < 2 * N * (TC / 4); q += NT) {
+            const int which = q / (N * (TC / 4));
+            const int qq = q % (N * (TC / 4));
+            const int n = qq % N, t4 = (qq / N) * 4;
+            const long long t = t0 + t4;
+            if (t >= p.L) continue;
+            const float* src = pb + which * NSP * RSB + n * RSB;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int rr = 0; rr < DT; ++rr) {
+                if (d0 + rr >= p.dim) break;
+                float x[4];
+                load4_smem(src + rr * FROW + t4, x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] += x[e];
+            }
+            float* o = (which ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (t + e < p.L) atomicAdd(o + e, v[e]);
+        }
+        // the next chunk's copy, partials and recompute start after this barrier
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    if (dval) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int n = k * P + g;
+            if (n < N) {
+                atomicAdd(p.dA + dch * p.N + n, dAacc[k]);
+                if (p.dh0 != nullptr) p.dh0[ch * p.N + n] = G[k];
+            }
+        }
+        if (g == 0 && p.dD != nullptr) atomicAdd(p.dD + dch, dDacc);
+    }
+}
+
+}  // namespace sscan

@@ -33,7 +33,7 @@ def lr():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for f in ("sscan_fwd", "sscan_fwd_ex", "sscan_fwd_fused", "sscan_step", "pscan",
+    for f in ("sscan_fwd", "sscan_fwd_ex", "sscan_fwd_fused", "sscan_bwd", "sscan_step", "pscan",
               "sscan_status_string",
               "sscan_get_last_error", "sscan_max_dstate", "sscan_last_launch_count",
               "sscan_last_plan"):
@@ -100,6 +100,12 @@ def test_invalid_calls_return_before_any_cuda_call(lr):
     assert lr.last_plan() == "empty"
     assert raw.sscan_step(fake, fake, fake, fake, fake, None, fake, fake, 1, 1, 0, 0, None) == \
         lr.SSCAN_ERR_INVALID
+    assert raw.sscan_bwd(fake, fake, fake, fake, fake, None, None, fake, None, fake, fake, fake, fake,
+                         fake, None, None, 1, 1, 8, 65, 0, None) == lr.SSCAN_ERR_INVALID
+    assert raw.sscan_bwd(fake, fake, fake, fake, fake, None, None, fake, None, fake, fake, None, fake,
+                         fake, None, None, 1, 1, 8, 16, 0, None) == lr.SSCAN_ERR_INVALID
+    assert raw.sscan_bwd(fake, fake, fake, fake, fake, None, None, fake, None, fake, fake, fake, fake,
+                         fake, None, None, 0, 4, 8, 16, 1, None) == lr.SSCAN_OK
     assert raw.pscan(None, fake, fake, None, 1, 1, None) == lr.SSCAN_ERR_INVALID
     assert raw.pscan(fake, fake, fake, None, -1, 1, None) == lr.SSCAN_ERR_INVALID
     assert lr.last_launch_count() == 0
