@@ -110,8 +110,14 @@ def roofline(w, t_s, pk):
 
 
 def kernel_source_hash():
+    """Hash of the sources of the forward scan (kernel, dispatch, planner): the
+    recorded ncu traffic is valid only for the sources it was taken on."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(_ROOT, "linear_recurrence_gb300", "csrc", "*"))):
+    csrc = os.path.join(_ROOT, "linear_recurrence_gb300", "csrc")
+    files = [os.path.join(csrc, n) for n in ("device_utils.cuh", "sscan_fwd_kernel.cuh",
+                                             "sscan_dispatch.cuh", "sscan_abi.cu")]
+    files += glob.glob(os.path.join(csrc, "sscan_fwd_*_*.cu"))
+    for p in sorted(files):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

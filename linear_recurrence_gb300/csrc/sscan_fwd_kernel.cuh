@@ -72,10 +72,23 @@ struct FwdParams {
     int zoh;                  // zero-order-hold B-bar (the kernel's ZOH variant)
 };
 
+// softplus(x) = log(1 + e^x) from the MUFU exponent and logarithm: with
+// e = e^x, log1p(e) is taken from its Maclaurin series e - e^2/2 + e^3/3 where
+// e < 1/64 (truncation below 2^-26 relative), else as ln2 * log2(1 + e), whose
+// absolute error (2^-22) is then below 1e-5 of the result; x > 20 gives x.
+__device__ __forceinline__ float softplus_f(float x) {
+    if (x > 20.f) return x;
+    const float e = ex2(x * 1.4426950408889634f);
+    if (e < 0.015625f) return e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
+    float l;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + e));
+    return l * 0.69314718055994531f;
+}
+
 // delta as the scan uses it: delta + bias, then softplus when asked for
 __device__ __forceinline__ float delta_in(float x, float bias, bool softplus) {
     x += bias;
-    return softplus ? (x > 20.f ? x : log1pf(expf(x))) : x;
+    return softplus ? softplus_f(x) : x;
 }
 
 // Zero-order-hold B-bar per unit B, (exp(delta*A) - 1) / A, given the exponent
@@ -91,7 +104,7 @@ __device__ __forceinline__ float zoh_coef(float dt, float y, float a, float invA
 }
 
 // silu(z) = z * sigmoid(z), the output gate
-__device__ __forceinline__ float silu(float z) { return z / (1.f + ex2(-z * 1.4426950408889634f)); }
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + ex2(-z * 1.4426950408889634f)); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 #ifndef SSCAN_CHUNK_STEPS
@@ -243,8 +256,7 @@ __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long
 // bf16 vector path: widen a landed stage to the fp32 work rows (after a barrier,
 // since a thread widens pieces other threads copied), one 16-byte piece (8
 // values) per item.  Rows: u and delta [0, 2DT), B [2DT, 2DT+N),
-// C [2DT+NSP, 2DT+NSP+N), z [ZROW0, ZROW0+DT) when gated.  delta is
-// transformed (bias, softplus) on the way, except in padding.
+// C [2DT+NSP, 2DT+NSP+N), z [ZROW0, ZROW0+DT) when gated.
 __device__ __forceinline__ void widen8(const bf16* src, float* dst) {
     const uint4 q = *reinterpret_cast<const uint4*>(src);
     *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
@@ -260,10 +272,22 @@ __device__ __forceinline__ void widen_stage(const FwdParams& p, const T* st, flo
     constexpr int DT = Cfg::DT, RROW = Cfg::RROW, FROW = Cfg::FROW, TC = Cfg::TC, NSP = Cfg::NSP;
     constexpr int Q8 = TC / 8;  // 16-byte pieces per row
     const int N = (int)p.N;
-    // u and delta rows
+    // u and delta rows; with the options, delta is transformed (bias,
+    // softplus) on the way, except in padding
+    const bool xform = OPT > 0 && (p.delta_softplus != 0 || p.delta_bias != nullptr);
     for (int q = tid; q < 2 * DT * Q8; q += Cfg::kThreads) {
         const int r = q / Q8, c = (q % Q8) * 8;
         widen8(st + r * RROW + c, wk + r * FROW + c);
+        if (xform && r >= DT) {
+            const long long dd = d0 + (r - DT);
+            if (dd < p.dim) {
+                const float bias = p.delta_bias != nullptr ? p.delta_bias[dd] : 0.f;
+                float* v = wk + r * FROW + c;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (t0 + c + e < t_end) v[e] = delta_in(v[e], bias, p.delta_softplus != 0);
+            }
+        }
     }
     // B and C rows of the N states
     for (int q = tid; q < 2 * N * Q8; q += Cfg::kThreads) {
@@ -280,8 +304,8 @@ __device__ __forceinline__ void widen_stage(const FwdParams& p, const T* st, flo
     }
 }
 
-// delta transform (bias, softplus) of a chunk's fp32 delta rows in place (the
-// stage itself for fp32 I/O, the widened rows for bf16);
+// delta transform (bias, softplus) of a chunk's delta rows in place in an fp32
+// stage (bf16 stages are transformed as they are widened);
 // padding (channels beyond dim, steps beyond the segment) stays 0 so that it
 // keeps the state.  Runs after the rows are visible to every thread.
 template <typename T, int NS, int P, int CPL, int OPT>
@@ -634,8 +658,8 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
                 __syncthreads();
             }
         }
-        // (the scalar loader applies the delta transform as it loads)
-        if constexpr (OPT > 0) {
+        // (the scalar loader and the bf16 widening apply the delta transform)
+        if constexpr (OPT > 0 && Cfg::kF32) {
             if (vec && (p.delta_softplus != 0 || p.delta_bias != nullptr)) {
                 transform_delta_rows<T, NS, P, CPL, OPT>(p, sm.rows(i), d0, t0, t_end, tid);
                 __syncthreads();
