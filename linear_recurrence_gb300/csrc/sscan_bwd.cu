@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <algorithm>
+
 #include "../../include/sscan.h"
 #include "sscan_bwd_kernel.cuh"
 
@@ -112,9 +114,27 @@ extern "C" int sscan_bwd(const void* u, const void* delta, const float* A, const
     const int vece = dtype == SSCAN_F32 ? 4 : 8;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
                      aligned16(C) && aligned16(dy) && aligned16(du) && aligned16(ddelta);
-    const long long nchunks = (seqlen + sscan::kBwdChunk - 1) / sscan::kBwdChunk;
+    const long long TC = sscan::kBwdChunk;
+    const long long nchunks = (seqlen + TC - 1) / TC;
+    // time split: about 12 warps per SM (4 per CTA), segments of 8 chunks or more
+    long long S = 1;
+    {
+        int dev = 0, nsm = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && nsm > 0) {
+            const long long target = 3LL * nsm;  // CTAs
+            if (grid < target) S = (target + grid - 1) / grid;
+            S = std::min(S, std::max(1LL, nchunks / 8));
+        }
+    }
+    const long long Tseg = ((nchunks + S - 1) / S) * TC;
+    S = (seqlen + Tseg - 1) / Tseg;
+    if (grid * S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    const size_t nckpt = (size_t)(batch * dim) * (size_t)nchunks * (size_t)dstate;
+    const size_t nseg = (size_t)(batch * dim) * (size_t)S;
+    const size_t scratch_floats = nckpt + (S > 1 ? nseg * (2 * (size_t)dstate + 1) : 0);
     void* scratch = nullptr;
-    e = cudaMallocAsync(&scratch, (size_t)(batch * dim) * (size_t)nchunks * (size_t)dstate * sizeof(float), st);
+    e = cudaMallocAsync(&scratch, scratch_floats * sizeof(float), st);
     if (e != cudaSuccess) {
         sscan::record_error(e);
         return SSCAN_ERR_CUDA;
@@ -124,14 +144,28 @@ extern "C" int sscan_bwd(const void* u, const void* delta, const float* A, const
     p.dy = dy; p.dhT = dfinal_state;
     p.du = du; p.ddelta = ddelta; p.dA = dA; p.dB = dB; p.dC = dC; p.dD = D ? dD : nullptr; p.dh0 = dh0;
     p.ckpt = static_cast<float*>(scratch);
+    p.seg_h = p.ckpt + nckpt;
+    p.seg_g = p.seg_h + nseg * (size_t)dstate;
+    p.seg_dsum = p.seg_g + nseg * (size_t)dstate;
     p.batch = batch; p.dim = dim; p.L = seqlen; p.N = dstate;
+    p.Tseg = Tseg; p.S = (int)S;
     p.tiles_per_batch = (int)tiles_per_batch;
     p.vec = vec ? 1 : 0;
-    char plan[128];
-    snprintf(plan, sizeof(plan), "bwd %s P=%d NS=%d vec=%d tiles=%lld chunks=%lld",
-             dtype == SSCAN_F32 ? "f32" : "bf16", s.P, s.NS, (int)vec, grid, nchunks);
-    sscan::record_call(1, st, plan);
-    e = dtype == SSCAN_F32 ? launch_dtype<float>(p, s, grid, st) : launch_dtype<sscan::bf16>(p, s, grid, st);
+    char plan[160];
+    snprintf(plan, sizeof(plan), "bwd %s P=%d NS=%d vec=%d tiles=%lld chunks=%lld S=%lld Tseg=%lld",
+             dtype == SSCAN_F32 ? "f32" : "bf16", s.P, s.NS, (int)vec, grid, nchunks, S, Tseg);
+    sscan::record_call(S > 1 ? 2 : 1, st, plan);
+    e = cudaSuccess;
+    if (S > 1) {  // per-segment aggregates first
+        p.mode = 1;
+        e = dtype == SSCAN_F32 ? launch_dtype<float>(p, s, grid * S, st)
+                               : launch_dtype<sscan::bf16>(p, s, grid * S, st);
+    }
+    if (e == cudaSuccess) {
+        p.mode = 0;
+        e = dtype == SSCAN_F32 ? launch_dtype<float>(p, s, grid * S, st)
+                               : launch_dtype<sscan::bf16>(p, s, grid * S, st);
+    }
     const cudaError_t ef = cudaFreeAsync(scratch, st);
     if (e == cudaSuccess) e = ef;
     if (e != cudaSuccess) {

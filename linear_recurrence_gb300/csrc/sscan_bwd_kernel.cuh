@@ -24,6 +24,16 @@
 // states (du, ddelta) and over the CTA's channels (dB, dC) go through shared
 // memory partials; dB and dC are accumulated into float32 outputs with
 // atomic adds, dA and dD once per lane at the end.
+//
+// Few channels and long sequences are split into S time segments, each its
+// own CTA.  A first launch (mode 1) computes per segment the forward
+// aggregate (its end state from a zero start, and sum(delta), whose decay is
+// 2^(A log2e sum(delta))) and the reverse one (dL/dh at its start from a zero
+// gradient at its end).  The gradient launch (mode 0) then folds the forward
+// aggregates of the earlier segments into its entry state and the reverse
+// aggregates of the later segments (with dL/d(final state)) into its exit
+// gradient, both in order under (a1,b1) o (a2,b2) = (a2 a1, a2 b1 + b2), and
+// runs the exact backward of its segment.
 #pragma once
 
 #include "device_utils.cuh"
@@ -48,7 +58,13 @@ struct BwdParams {
     float* dD;           // [dim] or NULL, accumulated (zeroed by the host)
     float* dh0;          // [batch, dim, N] or NULL
     float* ckpt;         // [batch*dim, nchunks, N]: state before each chunk
+    float* seg_h;        // [batch*dim, S, N] local end state of each segment (time split)
+    float* seg_g;        // [batch*dim, S, N] local dL/dh entering each segment from its end
+    float* seg_dsum;     // [batch*dim, S]    sum of delta over each segment
     long long batch, dim, L, N;
+    long long Tseg;      // steps per segment (multiple of the chunk)
+    int S;               // time segments
+    int mode;            // 0: gradients of a segment; 1: its aggregates (time split)
     int tiles_per_batch;
     int vec;             // rows 16-byte aligned: cp.async staging, vector stores
 };
@@ -193,13 +209,19 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
     const int g = lane % P, gi = lane / P;
     const int r = w * Cfg::GPW + gi;  // the lane's channel row in the tile
     const bool vec = p.vec != 0;
-    const long long b = blockIdx.x / p.tiles_per_batch;
-    const long long d0 = (long long)(blockIdx.x % p.tiles_per_batch) * DT;
+    const int seg = blockIdx.x % p.S;
+    const int tile = blockIdx.x / p.S;
+    const long long b = tile / p.tiles_per_batch;
+    const long long d0 = (long long)(tile % p.tiles_per_batch) * DT;
     const long long dch = d0 + r;
     const bool dval = dch < p.dim;
     const long long ch = b * p.dim + (dval ? dch : 0);
     const int N = (int)p.N;
     const int nchunks = (int)((p.L + TC - 1) / TC);
+    const int cps = (int)(p.Tseg / TC);  // chunks per segment
+    const int c_begin = seg * cps;
+    const int c_end = min(nchunks, c_begin + cps);
+    const bool agg = p.mode == 1;
 
     float A[NS], Al2[NS], h[NS];
 #pragma unroll
@@ -208,9 +230,34 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
         const bool nv = dval && n < N;
         A[k] = nv ? p.A[dch * p.N + n] : 0.f;
         Al2[k] = A[k] * 1.4426950408889634f;
-        h[k] = (nv && p.h0 != nullptr) ? p.h0[ch * p.N + n] : 0.f;
+        h[k] = (nv && seg == 0 && p.h0 != nullptr) ? p.h0[ch * p.N + n] : 0.f;
     }
     const float Dd = (dval && p.D != nullptr) ? p.D[dch] : 0.f;
+    // entry state of a later segment of the gradient launch: the fold of the
+    // forward aggregates of segments 0 .. seg-1 (four segments' loads at a time)
+    if (!agg && seg > 0 && dval) {
+        const float* sh = p.seg_h + ch * p.S * p.N;
+        const float* sd = p.seg_dsum + ch * p.S;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) h[k] = (k * P + g < N) ? sh[k * P + g] : 0.f;
+        for (int sp = 1; sp < seg; sp += 4) {
+            float dv[4], hv[4][NS];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool on = sp + q < seg;
+                dv[q] = on ? sd[sp + q] : 0.f;
+#pragma unroll
+                for (int k = 0; k < NS; ++k)
+                    hv[q][k] = (on && k * P + g < N) ? sh[(long long)(sp + q) * p.N + k * P + g] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (sp + q < seg) {
+#pragma unroll
+                    for (int k = 0; k < NS; ++k) h[k] = fmaf(ex2(Al2[k] * dv[q]), h[k], hv[q][k]);
+                }
+        }
+    }
 
     // B/C rows of state slots >= N are never copied: zero them once
     if (N < NSP) {
@@ -227,15 +274,17 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
         }
     }
 
-    // ---- phase 1: forward sweep, state before every chunk -> ckpt
+    // ---- phase 1: forward sweep over the segment, state before every chunk ->
+    // ckpt (the aggregate launch keeps only the end state and sum(delta))
     float* ck = p.ckpt + ch * (long long)nchunks * p.N;
+    float dsum = 0.f, dcomp = 0.f;  // Kahan sum of delta (aggregate launch)
     if (vec) {
-        bwd_issue<T, NS, P>(p, stage(0), b, d0, 0, tid, false);
+        if (c_begin < c_end) bwd_issue<T, NS, P>(p, stage(c_begin), b, d0, (long long)c_begin * TC, tid, false);
         cp_async_commit();
     }
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
         if (vec) {
-            if (c + 1 < nchunks) bwd_issue<T, NS, P>(p, stage(c + 1), b, d0, (long long)(c + 1) * TC, tid, false);
+            if (c + 1 < c_end) bwd_issue<T, NS, P>(p, stage(c + 1), b, d0, (long long)(c + 1) * TC, tid, false);
             cp_async_commit();
             cp_async_wait<1>();
         } else {
@@ -248,7 +297,7 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
                 __syncthreads();
             }
         }
-        if (dval) {
+        if (dval && !agg) {
 #pragma unroll
             for (int k = 0; k < NS; ++k)
                 if (k * P + g < N) ck[(long long)c * p.N + k * P + g] = h[k];
@@ -257,11 +306,13 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
         const float* su = rows + r * FROW;
         const float* sd = rows + (DT + r) * FROW;
         const float* sB = rows + (3 * DT + g) * FROW;
+        float csum = 0.f;
 #pragma unroll 2
         for (int t4 = 0; t4 < TC; t4 += 4) {
             float uu[4], dd[4];
             load4_smem(su + t4, uu);
             load4_smem(sd + t4, dd);
+            csum += (dd[0] + dd[1]) + (dd[2] + dd[3]);
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
                 float bb[4];
@@ -270,28 +321,61 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
                 for (int s = 0; s < 4; ++s) h[k] = fmaf(ex2(dd[s] * Al2[k]), h[k], (dd[s] * uu[s]) * bb[s]);
             }
         }
+        const float yk = csum - dcomp;
+        const float tk = dsum + yk;
+        dcomp = (tk - dsum) - yk;
+        dsum = tk;
         __syncthreads();  // the rows of chunk c are free for the next copy
     }
     cp_async_wait<0>();
     __syncthreads();
+    if (agg && dval) {
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+            if (k * P + g < N) p.seg_h[(ch * p.S + seg) * p.N + k * P + g] = h[k];
+        if (g == 0) p.seg_dsum[ch * p.S + seg] = dsum;
+    }
 
-    // ---- phase 2: reverse sweep over the chunks
+    // ---- phase 2: reverse sweep over the segment's chunks.  The exit gradient
+    // G is dL/d(final state) for the last segment, else the reverse fold of
+    // the later segments' aggregates; the aggregate launch starts from zero.
     float G[NS], dAacc[NS];
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
         const int n = k * P + g;
-        G[k] = (dval && n < N && p.dhT != nullptr) ? p.dhT[ch * p.N + n] : 0.f;
+        G[k] = (!agg && dval && n < N && p.dhT != nullptr) ? p.dhT[ch * p.N + n] : 0.f;
         dAacc[k] = 0.f;
+    }
+    if (!agg && seg < p.S - 1 && dval) {
+        const float* sg = p.seg_g + ch * p.S * p.N;
+        const float* sd = p.seg_dsum + ch * p.S;
+        for (int sp = p.S - 1; sp > seg; sp -= 4) {
+            float dv[4], gv[4][NS];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool on = sp - q > seg;
+                dv[q] = on ? sd[sp - q] : 0.f;
+#pragma unroll
+                for (int k = 0; k < NS; ++k)
+                    gv[q][k] = (on && k * P + g < N) ? sg[(long long)(sp - q) * p.N + k * P + g] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (sp - q > seg) {
+#pragma unroll
+                    for (int k = 0; k < NS; ++k) G[k] = fmaf(ex2(Al2[k] * dv[q]), G[k], gv[q][k]);
+                }
+        }
     }
     float dDacc = 0.f;
     if (vec) {
-        bwd_issue<T, NS, P>(p, stage(nchunks - 1), b, d0, (long long)(nchunks - 1) * TC, tid, true);
+        if (c_begin < c_end) bwd_issue<T, NS, P>(p, stage(c_end - 1), b, d0, (long long)(c_end - 1) * TC, tid, true);
         cp_async_commit();
     }
-    for (int c = nchunks - 1; c >= 0; --c) {
+    for (int c = c_end - 1; c >= c_begin; --c) {
         const long long t0 = (long long)c * TC;
         if (vec) {
-            if (c > 0) bwd_issue<T, NS, P>(p, stage(c - 1), b, d0, t0 - TC, tid, true);
+            if (c > c_begin) bwd_issue<T, NS, P>(p, stage(c - 1), b, d0, t0 - TC, tid, true);
             cp_async_commit();
             cp_async_wait<1>();
         } else {
@@ -310,6 +394,24 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
         const float* sy = rows + (2 * DT + r) * FROW;
         const float* sB = rows + (3 * DT + g) * FROW;
         const float* sC = rows + (3 * DT + NSP + g) * FROW;
+
+        if (agg) {  // the reverse aggregate: dL/dh carried back from a zero gradient
+#pragma unroll 1
+            for (int t4 = TC - 4; t4 >= 0; t4 -= 4) {
+                float dd[4], dyv[4];
+                load4_smem(sd + t4, dd);
+                load4_smem(sy + t4, dyv);
+#pragma unroll
+                for (int k = 0; k < NS; ++k) {
+                    float cc[4];
+                    load4_smem(sC + k * P * FROW + t4, cc);
+#pragma unroll
+                    for (int s = 3; s >= 0; --s) G[k] = ex2(dd[s] * Al2[k]) * fmaf(cc[s], dyv[s], G[k]);
+                }
+            }
+            __syncthreads();  // the rows of chunk c are free for the next copy
+            continue;
+        }
 
         // recompute the chunk's states from its boundary state (lane-private,
         // 4 steps of a state per float4: hb[(t4/4 * NS + k) * NT + tid])
@@ -426,12 +528,12 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
             }
         }
         // epilogue: dB, dC (sum over the CTA's channels, then one atomic add)
-        for (int q = tid; q < 2 * N * (TC / 4); q += NT) {
-            const int which = q / (N * (TC / 4));
-            const int qq = q % (N * (TC / 4));
-            const int n = qq % N, t4 = (qq / N) * 4;
+        for (int q = tid; q < 2 * NSP * (TC / 4); q += NT) {
+            const int which = q / (NSP * (TC / 4));
+            const int qq = q % (NSP * (TC / 4));
+            const int n = qq % NSP, t4 = (qq / NSP) * 4;
             const long long t = t0 + t4;
-            if (t >= p.L) continue;
+            if (n >= N || t >= p.L) continue;
             const float* src = pb + which * NSP * RSB + n * RSB;
             float v[4] = {0.f, 0.f, 0.f, 0.f};
             for (int rr = 0; rr < DT; ++rr) {
@@ -451,13 +553,21 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
     }
     cp_async_wait<0>();
 
+    if (agg) {
+        if (dval) {
+#pragma unroll
+            for (int k = 0; k < NS; ++k)
+                if (k * P + g < N) p.seg_g[(ch * p.S + seg) * p.N + k * P + g] = G[k];
+        }
+        return;
+    }
     if (dval) {
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
             const int n = k * P + g;
             if (n < N) {
                 atomicAdd(p.dA + dch * p.N + n, dAacc[k]);
-                if (p.dh0 != nullptr) p.dh0[ch * p.N + n] = G[k];
+                if (p.dh0 != nullptr && seg == 0) p.dh0[ch * p.N + n] = G[k];
             }
         }
         if (g == 0 && p.dD != nullptr) atomicAdd(p.dD + dch, dDacc);

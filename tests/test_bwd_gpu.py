@@ -74,6 +74,15 @@ def test_bwd_lengths_and_unaligned_rows(lr, L, dtype):
     _check(lr, dtype, x, dy, dhT)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dim,L,N", [(20, 1024, 16), (37, 2000, 13), (8, 4096, 64)])
+def test_bwd_time_split(lr, dtype, dim, L, N):
+    # few channels and a long sequence: the plan splits time into segments
+    _, x, dy, dhT = _inputs(dtype, 1, dim, L, N, seed=80 + N)
+    _check(lr, dtype, x, dy, dhT)
+    assert " S=1 " not in lr.last_plan() + " ", lr.last_plan()
+
+
 def test_bwd_without_skip_h0_and_final_gradient(lr):
     _, x, dy, _ = _inputs("f32", 2, 18, 64, 16, seed=70, h0=False, D=False)
     _check(lr, "f32", x, dy, None)
