@@ -152,6 +152,8 @@ struct FwdCfg {
     // rows a quarter-warp reads in the epilogue fall in distinct banks
     static constexpr int RS = ((P * FROW / 4) % 2 == 1) ? P * FROW : P * FROW + 4;
     static constexpr int YP_FLOATS = DT * RS;
+    // epilogue items (4 steps of one channel) per thread
+    static constexpr int IPT = (DT * (TC / 4) + kThreads - 1) / kThreads;
     static constexpr int SMEM_BYTES = STAGES * RAW_BYTES + (WORK_FLOATS + YP_FLOATS) * 4;
     static_assert(32 % P == 0, "lanes per channel must divide the warp");
     static_assert(TC % 4 == 0 && TC % VECE == 0, "chunk must hold whole vectors");
@@ -369,17 +371,15 @@ __device__ __forceinline__ void load_chunk_scalar(const FwdParams& p, float* row
 // channels' u/delta as 16-byte vectors, then walks its states in quads: the
 // B/C rows of 4 states (4 steps each) are read as 16-byte vectors and the quad
 // is advanced 4 steps for all CPL channels.  The 4 partial outputs of each
-// channel are stored at the end of the block.  SCALAR: every state of a
-// channel shares one decay rate (one exponent per channel and step).  NO_B:
-// the homogeneous recurrence h = a*h of the carry correction (u and B are not
-// read; D is not added).  Returns the chunk's sum of delta per channel when
-// DSUM.
-template <typename T, int NS, int P, int CPL, int OPT, bool WRITE_Y, bool SCALAR, bool DSUM, bool NO_B, bool ZOH>
+// channel are stored at the end of the block (the skip term D*u is added by
+// the epilogue).  SCALAR: every state of a channel shares one decay rate (one
+// exponent per channel and step).  NO_B: the homogeneous recurrence h = a*h of
+// the carry correction (u and B are not read).
+template <typename T, int NS, int P, int CPL, int OPT, bool WRITE_Y, bool SCALAR, bool NO_B, bool ZOH>
 __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, const int (&rr)[CPL], int g,
                                               const float (&Al2)[CPL][NS], const float (&As)[CPL],
                                               const float (&invA)[CPL][NS], const float (&invAs)[CPL],
-                                              float (&h)[CPL][NS], const float (&Dl)[CPL],
-                                              float (&csum)[CPL]) {
+                                              float (&h)[CPL][NS]) {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, NSP = Cfg::NSP, RS = Cfg::RS;
     constexpr int QS = NS < 4 ? NS : 4;  // states per quad
@@ -389,8 +389,6 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
     const float* sd = rows + DT * FROW;
     const float* sB = rows + (2 * DT + g) * FROW;
     const float* sC = rows + (2 * DT + NSP + g) * FROW;
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) csum[j] = 0.f;
 #pragma unroll kBlockUnroll
     for (int t4 = 0; t4 < TC; t4 += 4) {
         float uu[CPL][4], dd[CPL][4];
@@ -407,14 +405,13 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
         for (int j = 0; j < CPL; ++j)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                if (DSUM) csum[j] += dd[j][s];
                 const float ys = dd[j][s] * As[j];
                 as[j][s] = SCALAR ? ex2(ys) : 0.f;
                 if (NO_B) du[j][s] = 0.f;
                 else if (!ZOH) du[j][s] = dd[j][s] * uu[j][s];
                 else if (SCALAR) du[j][s] = zoh_coef(dd[j][s], ys, as[j][s], invAs[j]) * uu[j][s];
                 else du[j][s] = uu[j][s];
-                y[j][s] = NO_B ? 0.f : Dl[j] * uu[j][s];
+                y[j][s] = 0.f;
             }
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
@@ -454,19 +451,35 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
     }
 }
 
-// Sum the P partials of every output of the chunk and store it (CORR: add it to
-// the output already written).  Item q covers 4 steps of tile row q % DT.
+// Sum the P partials of every output of the chunk, add the skip term D*u and
+// store it (CORR: add it to the output already written, no skip term).  Item
+// q covers 4 steps of tile row q % DT; a thread's items keep their (row,
+// steps) slot from chunk to chunk, so with DSUM each thread also keeps a
+// running (Kahan) sum of delta per item slot, for the segment aggregate.
 template <typename T, int NS, int P, int CPL, int OPT>
-__device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp, const float* yloc,
+__device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp, const float* rows,
                                             const float* zrows, long long b, long long d0, long long t0,
-                                            long long t_end, int tid, bool corr, bool vec) {
+                                            long long t_end, int tid, bool corr, bool vec, bool dsum_on,
+                                            float (&ds)[FwdCfg<T, NS, P, CPL, OPT>::IPT],
+                                            float (&dc)[FwdCfg<T, NS, P, CPL, OPT>::IPT]) {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, RS = Cfg::RS;
     T* go = static_cast<T*>(p.out);
-    for (int q = tid; q < DT * (TC / 4); q += Cfg::kThreads) {
+#pragma unroll
+    for (int k = 0; k < Cfg::IPT; ++k) {
+        const int q = tid + k * Cfg::kThreads;
+        if (q >= DT * (TC / 4)) break;
         const int r = q % DT, t4 = (q / DT) * 4;
         const long long dd = d0 + r, t = t0 + t4;
         if (dd >= p.dim || t >= t_end) continue;
+        if (dsum_on) {  // padding steps hold delta = 0
+            float dv[4];
+            load4_smem(rows + (DT + r) * FROW + t4, dv);
+            const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dc[k];
+            const float tk = ds[k] + yk;
+            dc[k] = (tk - ds[k]) - yk;
+            ds[k] = tk;
+        }
         float v[4];
         load4_smem(yp + r * RS + t4, v);
 #pragma unroll
@@ -476,6 +489,13 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] += w[e];
         }
+        if (!corr && p.D != nullptr) {  // the skip term, u from the chunk's rows
+            const float Dd = __ldg(p.D + dd);
+            float uv[4];
+            load4_smem(rows + r * FROW + t4, uv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = fmaf(Dd, uv[e], v[e]);
+        }
         if (OPT > 0 && zrows != nullptr) {  // out = (y + D*u) * silu(z); a correction is gated alike
             float zv[4];
             load4_smem(zrows + r * FROW + t4, zv);
@@ -484,7 +504,7 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
         }
         if (corr) {  // the local outputs of the chunk, staged in the u rows
             float w[4];
-            load4_smem(yloc + r * FROW + t4, w);
+            load4_smem(rows + r * FROW + t4, w);
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] += w[e];
         }
@@ -541,7 +561,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
     int rr[CPL];
     long long ch[CPL];
     bool dval[CPL];
-    float Al2[CPL][NS], As[CPL], Dl[CPL], h[CPL][NS];
+    float Al2[CPL][NS], As[CPL], h[CPL][NS];
     float invA[CPL][NS], invAs[CPL];  // 1/A (0 where A = 0), for the zero-order hold
     bool uniform_rate = true;
 #pragma unroll
@@ -562,7 +582,6 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
         As[j] = a_first * kLog2e;
         invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
-        Dl[j] = (!corr && g == 0 && p.D != nullptr && dval[j]) ? p.D[dch] : 0.f;
         if (corr) {
             fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
             if (!dval[j]) {
@@ -631,9 +650,9 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
     }
 
-    float dsum[CPL], dcomp[CPL];  // Kahan sums of delta over the segment
+    float ds[Cfg::IPT], dc[Cfg::IPT];  // Kahan sums of delta per epilogue item slot
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) dsum[j] = dcomp[j] = 0.f;
+    for (int k = 0; k < Cfg::IPT; ++k) ds[k] = dc[k] = 0.f;
     for (int i = 0; i < nchunks; ++i) {
         const long long t0 = t_begin + (long long)i * TC;
         if (vec) {
@@ -672,34 +691,38 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
                                            load_u, load_b, load_c);
             cp_async_commit();
         }
-        float csum[CPL];
         const float* rows = sm.rows(i);
         if (corr) {
-            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, false, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
-            else compute_chunk<T, NS, P, CPL, OPT, true, false, false, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
-        } else if (dsum_on) {
-            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, true, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
-            else compute_chunk<T, NS, P, CPL, OPT, true, false, true, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
+            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
+            else compute_chunk<T, NS, P, CPL, OPT, true, false, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
         } else {
-            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, false, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
-            else compute_chunk<T, NS, P, CPL, OPT, true, false, false, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h, Dl, csum);
-        }
-        if (dsum_on) {
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const float yk = csum[j] - dcomp[j];
-                const float tk = dsum[j] + yk;
-                dcomp[j] = (tk - dsum[j]) - yk;
-                dsum[j] = tk;
-            }
+            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
+            else compute_chunk<T, NS, P, CPL, OPT, true, false, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
         }
         __syncthreads();  // every lane's partials of the chunk are in place
         store_chunk<T, NS, P, CPL, OPT>(p, sm.yp, rows, (OPT > 0 && p.z != nullptr) ? rows + Cfg::ZROW0 * Cfg::FROW : nullptr, b,
-                                   d0, t0, t_end, tid, corr, vec);
+                                   d0, t0, t_end, tid, corr, vec, dsum_on, ds, dc);
     }
     cp_async_wait<0>();
     if (corr) return;
 
+    if (dsum_on) {  // the segment's sum of delta per channel: add up the item slots
+        __syncthreads();  // the last epilogue is done with the partial buffer
+        constexpr int SL = TC / 4;
+#pragma unroll
+        for (int k = 0; k < Cfg::IPT; ++k) {
+            const int q = tid + k * Cfg::kThreads;
+            if (q < DT * SL) sm.yp[q] = ds[k];
+        }
+        __syncthreads();
+        for (int r = tid; r < DT; r += Cfg::kThreads) {
+            if (d0 + r >= p.dim) continue;
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < SL; ++j) sum += sm.yp[j * DT + r];
+            p.seg_dsum[(b * p.dim + d0 + r) * p.S + s] = sum;
+        }
+    }
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         if (!dval[j]) continue;
@@ -710,7 +733,6 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
                 const int n = k * P + g;
                 if (n < N) sst[n] = h[j][k];
             }
-            if (g == 0) p.seg_dsum[ch[j] * p.S + s] = dsum[j];
         } else if (p.final_state != nullptr) {
 #pragma unroll
             for (int k = 0; k < NS; ++k) {

@@ -48,14 +48,16 @@ __global__ void __launch_bounds__(256) sscan_step_kernel(const T* __restrict__ u
                                                          const float* __restrict__ A,
                                                          const T* __restrict__ Bm, const T* __restrict__ Cm,
                                                          const float* __restrict__ D, float* __restrict__ state,
-                                                         T* __restrict__ out, long long batch, long long dim,
+                                                         T* __restrict__ out, long long b0, int dim,
                                                          int N) {
-    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long ch = tid / Q;                 // flat (b, d)
-    const int q = (int)(tid % Q);
-    const bool valid = ch < batch * dim;
-    const long long chc = valid ? ch : 0;
-    const long long b = chc / dim, d = chc % dim;
+    // grid: x over (channel, q) of one batch row, y over batch rows from b0
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    const int dd = tid / Q;  // channel
+    const int q = tid % Q;
+    const bool valid = dd < dim;
+    const long long b = b0 + blockIdx.y;
+    const long long d = valid ? dd : 0;
+    const long long chc = b * dim + d;  // flat (b, d)
     const float dt = valid ? sscan::to_f32(delta[chc]) : 0.f;
     const float uu = valid ? sscan::to_f32(u[chc]) : 0.f;
     const float du = dt * uu;
@@ -121,21 +123,26 @@ cudaError_t launch_step(const void* u, const void* delta, const float* A, const 
     const int G = N > 4 ? 2 : 1;
     int Q = 1;
     while (Q * 4 * G < N) Q *= 2;
-    const long long threads = batch * dim * Q;
-    const long long grid = (threads + 255) / 256;
-    if (grid > (1LL << 31) - 1) return cudaErrorInvalidValue;
+    if (dim * Q > (1LL << 30)) return cudaErrorInvalidValue;
+    const unsigned gx = (unsigned)((dim * Q + 255) / 256);
     const T* tu = static_cast<const T*>(u);
     const T* td = static_cast<const T*>(delta);
     const T* tB = static_cast<const T*>(B);
     const T* tC = static_cast<const T*>(C);
     T* to = static_cast<T*>(out);
+    // batch rows go to grid.y, at most 65535 per launch
 #define SSCAN_STEP_CASE(QQ, GG)                                                                     \
     if (Q == QQ && G == GG) {                                                                       \
-        if (vec)                                                                                    \
-            sscan_step_kernel<T, QQ, GG, true><<<(unsigned)grid, 256, 0, st>>>(tu, td, A, tB, tC, D, state, to, batch, dim, N); \
-        else                                                                                        \
-            sscan_step_kernel<T, QQ, GG, false><<<(unsigned)grid, 256, 0, st>>>(tu, td, A, tB, tC, D, state, to, batch, dim, N); \
-        return cudaGetLastError();                                                                  \
+        for (long long b0 = 0; b0 < batch; b0 += 65535) {                                           \
+            const dim3 grid(gx, (unsigned)(batch - b0 < 65535 ? batch - b0 : 65535));              \
+            if (vec)                                                                                \
+                sscan_step_kernel<T, QQ, GG, true><<<grid, 256, 0, st>>>(tu, td, A, tB, tC, D, state, to, b0, (int)dim, N); \
+            else                                                                                    \
+                sscan_step_kernel<T, QQ, GG, false><<<grid, 256, 0, st>>>(tu, td, A, tB, tC, D, state, to, b0, (int)dim, N); \
+            const cudaError_t e = cudaGetLastError();                                               \
+            if (e != cudaSuccess) return e;                                                         \
+        }                                                                                           \
+        return cudaSuccess;                                                                         \
     }
     SSCAN_STEP_CASE(1, 1) SSCAN_STEP_CASE(1, 2) SSCAN_STEP_CASE(2, 2) SSCAN_STEP_CASE(4, 2)
     SSCAN_STEP_CASE(8, 2)
@@ -164,7 +171,7 @@ extern "C" int sscan_step(const void* u, const void* delta, const float* A, cons
                      (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(B) & rows_align) == 0 &&
                      (reinterpret_cast<uintptr_t>(C) & rows_align) == 0;
-    sscan::record_call(1, st, vec ? "step vec=1" : "step vec=0");
+    sscan::record_call((int)((batch + 65534) / 65535), st, vec ? "step vec=1" : "step vec=0");
     const cudaError_t e =
         dtype == SSCAN_F32
             ? launch_step<float>(u, delta, A, B, C, D, state, out, batch, dim, (int)dstate, vec, st)
