@@ -7,6 +7,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/sscan.h"
 #include "pscan_kernel.cuh"
@@ -26,16 +27,16 @@ struct CallRecord {
 thread_local CallRecord g_rec;
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64] = {};  // per device ordinal; host threads may race
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    int& c = cached[dev & 63];
-    if (c == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        c = n;
+    std::atomic<int>& c = cached[dev & 63];
+    int v = c.load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        c.store(v, std::memory_order_relaxed);
     }
-    return c;
+    return v;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -92,7 +93,7 @@ constexpr ShapePref kPrefs[] = {
 // Resident CTAs per SM of a shape, queried once per device.
 int cached_occupancy(bool f32, Shape sh) {
     constexpr int kNumShapes = (int)(sizeof(kShapes) / sizeof(kShapes[0]));
-    static int cache[64][2][kNumShapes] = {};
+    static std::atomic<int> cache[64][2][kNumShapes] = {};  // host threads may race
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     int idx = 0;
@@ -100,9 +101,13 @@ int cached_occupancy(bool f32, Shape sh) {
            !(kShapes[idx].P == sh.P && kShapes[idx].NS == sh.NS && kShapes[idx].CPL == sh.CPL))
         ++idx;
     if (idx == kNumShapes) return 0;
-    int& c = cache[dev & 63][f32 ? 0 : 1][idx];
-    if (c == 0) c = fwd_occupancy(f32, sh);
-    return c;
+    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1][idx];
+    int v = c.load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = fwd_occupancy(f32, sh);
+        c.store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,

@@ -441,22 +441,27 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
             }
         }
 
-        // reverse sweep, 4 steps at a time
+        // reverse sweep, 4 steps at a time.  Per step the sums over the lane's
+        // states: sdd = sum g*h_prev*a*A, sgb = sum g*B (ddelta adds u*sgb,
+        // du = delta*sgb + D*dy)
 #pragma unroll 1
         for (int t4 = TC - 4; t4 >= 0; t4 -= 4) {
-            float uu[4], dd[4], dyv[4];
+            float uu[4], dd[4], dyv[4], du4[4];
             load4_smem(su + t4, uu);
             load4_smem(sd + t4, dd);
             load4_smem(sy + t4, dyv);
-            float sdu[4] = {0.f, 0.f, 0.f, 0.f}, sdd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) du4[s] = dd[s] * uu[s];
+            float sgb[4] = {0.f, 0.f, 0.f, 0.f}, sdd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
                 float bb[4], cc[4], hv[4];
+                const int o = ((t4 / 4) * NS + k) * NT * 4 + tid * 4;
                 load4_smem(sB + k * P * FROW + t4, bb);
                 load4_smem(sC + k * P * FROW + t4, cc);
-                load4_smem(hb + ((t4 / 4) * NS + k) * NT * 4 + tid * 4, hv);
+                load4_smem(hb + o, hv);
                 float hp;  // h at the step before t4
-                if (t4 > 0) hp = hb[(((t4 - 4) / 4) * NS + k) * NT * 4 + tid * 4 + 3];
+                if (t4 > 0) hp = hb[o - NS * NT * 4 + 3];
                 else hp = hs[k];
                 float pbv[4], pcv[4];
 #pragma unroll
@@ -466,10 +471,9 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
                     const float gt = fmaf(cc[s], dyv[s], G[k]);
                     const float gha = (gt * hprev) * a;
                     dAacc[k] = fmaf(gha, dd[s], dAacc[k]);
-                    const float gb = gt * bb[s];
-                    sdd[s] = fmaf(gha, A[k], fmaf(gb, uu[s], sdd[s]));
-                    sdu[s] = fmaf(gb, dd[s], sdu[s]);
-                    pbv[s] = gt * (dd[s] * uu[s]);
+                    sdd[s] = fmaf(gha, A[k], sdd[s]);
+                    sgb[s] = fmaf(gt, bb[s], sgb[s]);
+                    pbv[s] = gt * du4[s];
                     pcv[s] = dyv[s] * hv[s];
                     G[k] = a * gt;
                 }
@@ -477,6 +481,12 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
                 *reinterpret_cast<float4*>(pb + n * RSB + r * FROW + t4) = make_float4(pbv[0], pbv[1], pbv[2], pbv[3]);
                 *reinterpret_cast<float4*>(pb + NSP * RSB + n * RSB + r * FROW + t4) =
                     make_float4(pcv[0], pcv[1], pcv[2], pcv[3]);
+            }
+            float sdu[4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                sdd[s] = fmaf(uu[s], sgb[s], sdd[s]);
+                sdu[s] = dd[s] * sgb[s];
             }
             if (g == 0) {
 #pragma unroll
