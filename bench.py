@@ -523,7 +523,9 @@ def main():
         per["decode_step"] = bench_step(max(5, args.steps // 2), 3, dev, stream, flush, pk)
         extra["per_workload"] = per
         rate, cores, sample, _ = oracle_rate(w, budget_s=10.0)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        rate1, _, sample1, _ = oracle_rate(w, budget_s=3.0, nthreads=1)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "one_core": {"value": rate1, "sample": sample1}}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
