@@ -130,12 +130,27 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
                 (chosen.P == 0 || c.NS * c.P < chosen.NS * chosen.P))
                 chosen = c;
     }
-    const long long chosen_warps =
-        chosen.P == 0 ? 0 : batch * ceil_div(dim, shape_channels(chosen)) * shape_warps(chosen);
-    const long long target =
-        chosen.P == 0 ? 0
-                      : std::min((long long)nsm * std::max(cached_occupancy(f32, chosen), 1) * shape_warps(chosen),
-                                 (long long)nsm * kTargetWarpsPerSm);
+    auto warps_of = [&](Shape c) { return batch * ceil_div(dim, shape_channels(c)) * shape_warps(c); };
+    auto target_of = [&](Shape c) {
+        return std::min((long long)nsm * std::max(cached_occupancy(f32, c), 1) * shape_warps(c),
+                        (long long)nsm * kTargetWarpsPerSm);
+    };
+    // When so few channels that the sequence must be cut into many segments
+    // (12 or more), two channels per lane halve the shared-memory traffic per
+    // element for B and C; the extra segments they need cost less (measured on
+    // 512 channels x 8192 steps).
+    if (lanes == 0 && chosen.P != 0 && chosen.CPL == 1 && segments == 0) {
+        const long long w1 = warps_of(chosen), t1 = target_of(chosen);
+        if (w1 < t1 && ceil_div(t1, std::max(w1, 1LL)) >= 12) {
+            for (const Shape& c : kShapes)
+                if (c.P == chosen.P && c.NS == chosen.NS && c.CPL == 2) {
+                    chosen = c;
+                    break;
+                }
+        }
+    }
+    const long long chosen_warps = chosen.P == 0 ? 0 : warps_of(chosen);
+    const long long target = chosen.P == 0 ? 0 : target_of(chosen);
     if (chosen.P == 0) return SSCAN_ERR_INVALID;
     const long long DT = shape_channels(chosen);
     const long long TC = kChunkSteps;

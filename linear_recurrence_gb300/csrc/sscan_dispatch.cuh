@@ -22,7 +22,7 @@ struct Shape {
 #define SSCAN_SHAPES_A(X) X(1, 4, 1) X(2, 4, 1) X(4, 4, 1) X(4, 16, 2)
 #endif
 #ifndef SSCAN_SHAPES_B
-#define SSCAN_SHAPES_B(X) X(8, 2, 1) X(8, 4, 1) X(8, 8, 1) X(16, 4, 1)
+#define SSCAN_SHAPES_B(X) X(8, 2, 1) X(8, 2, 2) X(8, 4, 1) X(8, 8, 1) X(16, 4, 1)
 #endif
 #define SSCAN_SHAPE_INIT(P_, NS_, CPL_) {P_, NS_, CPL_},
 constexpr Shape kShapes[] = {SSCAN_SHAPES_A(SSCAN_SHAPE_INIT) SSCAN_SHAPES_B(SSCAN_SHAPE_INIT)};

@@ -101,6 +101,17 @@ LANE_CASES = [(1, 4, (1, 4, 1)), (2, 7, (2, 4, 1)), (4, 13, (4, 4, 1)), (4, 40, 
               (8, 16, (8, 2, 1)), (8, 25, (8, 4, 1)), (8, 50, (8, 8, 1)), (16, 61, (16, 4, 1))]
 
 
+def test_two_channel_shape_for_few_channels(lr):
+    # few channels and a long sequence: the plan takes two channels per lane
+    w = workloads.WORKLOADS["dim512"].scaled(batch=1, dim=48, L=4096, N=16)
+    x = workloads.make_inputs(w)
+    _compare(lr, w, x, TOL["f32"])
+    assert "P=8 NS=2 CPL=2 " in lr.last_plan(), lr.last_plan()
+    wb = workloads.Workload(**{**w.__dict__, "dtype": "bf16", "h0_std": 0.2})
+    _compare(lr, wb, workloads.make_inputs(wb), TOL["bf16"])
+    assert "P=8 NS=2 CPL=2 " in lr.last_plan(), lr.last_plan()
+
+
 @pytest.mark.parametrize("lanes,N,shape", LANE_CASES, ids=lambda v: str(v))
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_lane_shapes(lr, lanes, N, shape, dtype):
