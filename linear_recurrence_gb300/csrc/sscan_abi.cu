@@ -53,6 +53,31 @@ cudaError_t launch_fwd(bool f32, const FwdParams& p, Shape sh, long long grid, c
     ++g_rec.launches;
     return sscan::fwd_launch(f32, p, sh, (int)grid, st);
 }
+cudaError_t launch_fwd_tma(bool f32, const FwdParams& p, Shape sh, long long grid, cudaStream_t st) {
+    if (grid <= 0) return cudaSuccess;
+    ++g_rec.launches;
+    return sscan::fwd_tma_launch(f32, p, sh, (int)grid, st);
+}
+
+// Device status word of the kernels' bounded waits (SSCAN_OK or
+// SSCAN_ERR_TIMEOUT), one per device; read and cleared by sscan_get_last_error.
+__device__ int g_device_status = 0;
+
+// Its device address on the current device (looked up once per device; the
+// lookup may load the module, so a first call should precede stream capture).
+int* device_status_ptr() {
+    static std::atomic<int*> cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    int* v = cached[dev].load(std::memory_order_acquire);
+    if (v == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+        v = static_cast<int*>(ptr);
+        cached[dev].store(v, std::memory_order_release);
+    }
+    return v;
+}
 
 }  // namespace
 
@@ -169,7 +194,77 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
     pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
     pl.S = ceil_div(seqlen, pl.Tseg);
     if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    pl.tma = false;
+    pl.corr_sh = pl.sh;
+    pl.corr_tiles_per_batch = pl.tiles_per_batch;
+    pl.corr_tiles = pl.tiles;
     *out = pl;
+    return SSCAN_OK;
+}
+
+// Resident CTAs per SM of a TMA-kernel shape, queried once per device.
+int cached_tma_occupancy(Shape sh) {
+    static std::atomic<int> cache[64][2] = {};  // (8,2,2), (4,4,2)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::atomic<int>& c = cache[dev & 63][sh.P == 4 ? 1 : 0];
+    int v = c.load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = fwd_tma_occupancy(true, sh);
+        c.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Plan of the fp32 TMA-fed kernel for 8 < N <= 16 (its shapes hold 16 state
+// slots), or SSCAN_ERR_INVALID when it does not apply.  A time split is sized
+// so that the local pass fills the GPU's resident CTA slots in one wave (the
+// pass time is then proportional to the segment length, so the most segments
+// that fit one wave are best); the automatic shape is the one with the most
+// channels per lane whose segments stay long enough (measured on GB300:
+// (4,4,2) from 16 chunks per segment, else (8,2,2); 512 channels x 8192 steps
+// then take (8,2,2) in 19 segments of 14 chunks).  The carry correction runs
+// on the cp.async kernel with one channel per lane.
+int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, int segments, int lanes,
+                 FwdPlan* out) {
+    if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
+    const int nsm = std::max(sm_count(), 1);
+    const long long TC = kChunkSteps;
+    const Shape cands[] = {{4, 4, 2}, {8, 2, 2}};
+    const long long min_chunks[] = {16, 0};
+    FwdPlan best{};
+    bool found = false;
+    for (int i = 0; i < 2 && !found; ++i) {
+        const Shape sh = cands[i];
+        if (!tma_has_shape(sh) || (lanes != 0 && lanes != sh.P)) continue;
+        FwdPlan pl{};
+        pl.sh = sh;
+        pl.tma = true;
+        pl.tiles_per_batch = ceil_div(dim, tma_channels(sh));
+        pl.tiles = batch * pl.tiles_per_batch;
+        if (pl.tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
+        const long long slots = (long long)nsm * std::max(cached_tma_occupancy(sh), 1);
+        long long S = segments;
+        if (S == 0) {
+            S = pl.tiles >= slots ? 1 : slots / pl.tiles;
+            S = std::min(S, std::max(1LL, seqlen / (kMinSegmentChunks * TC)));
+        }
+        S = std::max(1LL, std::min(S, ceil_div(seqlen, TC)));
+        pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
+        pl.S = ceil_div(seqlen, pl.Tseg);
+        if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
+        const bool last = i == 1 || lanes != 0 || segments != 0;
+        if (pl.S == 1 || pl.Tseg >= min_chunks[i] * TC || last) {
+            best = pl;
+            found = true;
+        }
+    }
+    if (!found) return SSCAN_ERR_INVALID;
+    best.corr_sh = Shape{8, 2, 1};
+    best.corr_tiles_per_batch = ceil_div(dim, shape_channels(best.corr_sh));
+    best.corr_tiles = batch * best.corr_tiles_per_batch;
+    if (best.corr_tiles * best.S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    *out = best;
     return SSCAN_OK;
 }
 }  // namespace sscan
@@ -196,6 +291,15 @@ int sscan_get_last_error(void) {
     int status = g_rec.pending_error;
     cudaError_t e = cudaStreamSynchronize(g_rec.stream);
     if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) {  // a bounded wait that gave up on this device
+        int dev_status = SSCAN_OK;
+        e = cudaMemcpyFromSymbol(&dev_status, g_device_status, sizeof(int));
+        if (e == cudaSuccess && dev_status != SSCAN_OK) {
+            const int zero = SSCAN_OK;
+            e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+            if (status == SSCAN_OK) status = dev_status;
+        }
+    }
     if (e != cudaSuccess && status == SSCAN_OK) status = SSCAN_ERR_CUDA;
     g_rec.pending_error = SSCAN_OK;
     return status;
@@ -244,11 +348,23 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     const int vece = 16 / esz;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
                      aligned16(C) && aligned16(out) && (z == nullptr || aligned16(z));
+    // the TMA-fed kernel takes the plain fp32 scan's single or local pass when
+    // the tensor-map rules hold (16-byte aligned rows, coordinates below 2^31);
+    // bf16 stays with the cp.async kernel, whose CTA widens B/C once for all
+    // its warps (the TMA kernel's per-warp widening measured slower)
+    const bool plain = z == nullptr && delta_bias == nullptr && flags == 0;
+    const long long lim = (1LL << 31) - 256;
     sscan::FwdPlan pl;
-    const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
-    if (prc != SSCAN_OK) return prc;
+    bool use_tma = f32 && vec && plain && seqlen < lim && dim < lim && batch < lim &&
+                   sscan::plan_fwd_tma(batch, dim, seqlen, dstate, segments, lanes, &pl) == SSCAN_OK;
+    if (!use_tma) {
+        const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
+        if (prc != SSCAN_OK) return prc;
+    }
     const Shape sh = pl.sh;
     const long long S = pl.S, tiles = pl.tiles;
+    int* status = device_status_ptr();
+    if (status == nullptr) return fail_cuda(cudaErrorInvalidDevicePointer);
 
     FwdParams p{};
     p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.h0 = h0;
@@ -260,18 +376,19 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     p.delta_bias = delta_bias;
     p.delta_softplus = (flags & SSCAN_DELTA_SOFTPLUS) ? 1 : 0;
     p.zoh = (flags & SSCAN_ZOH) ? 1 : 0;
+    p.status = status;
 
     snprintf(g_rec.plan, sizeof(g_rec.plan),
-             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s",
+             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s%s",
              f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
-             S == 1 ? "single" : "local+correct", delta_bias ? " bias" : "",
+             use_tma ? "tma " : "", S == 1 ? "single" : "local+correct", delta_bias ? " bias" : "",
              p.delta_softplus ? " softplus" : "", p.zoh ? " zoh" : "", z ? " gate" : "");
 
     cudaError_t e;
     if (S == 1) {
         p.mode = sscan::MODE_SINGLE;
         p.seg_count = 1;
-        e = launch_fwd(f32, p, sh, tiles, st);
+        e = use_tma ? launch_fwd_tma(f32, p, sh, tiles, st) : launch_fwd(f32, p, sh, tiles, st);
         if (e != cudaSuccess) return fail_cuda(e);
         return SSCAN_OK;
     }
@@ -288,11 +405,12 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     // rounded twice, the second time with the carry added)
     p.mode = sscan::MODE_LOCAL;
     p.seg_count = (int)S;
-    e = launch_fwd(f32, p, sh, tiles * S, st);
+    e = use_tma ? launch_fwd_tma(f32, p, sh, tiles * S, st) : launch_fwd(f32, p, sh, tiles * S, st);
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
-        e = launch_fwd(f32, p, sh, tiles * (S - 1), st);
+        p.tiles_per_batch = (int)pl.corr_tiles_per_batch;
+        e = launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
     }
     cudaError_t ef = cudaFreeAsync(scratch, st);
     if (e != cudaSuccess) return fail_cuda(e);

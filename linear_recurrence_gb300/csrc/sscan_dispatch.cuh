@@ -4,6 +4,7 @@
 // parallel.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "sscan_fwd_kernel.cuh"
@@ -77,6 +78,27 @@ inline int fwd_occupancy(bool f32, Shape sh) {
     return f32 ? fwd_occupancy_f32_b_e(sh) : fwd_occupancy_bf16_b_e(sh);
 }
 
+// Shapes of the TMA-fed kernel (sscan_fwd_tma.cuh): four warps per CTA, so
+// DT = 4 * (32 / P) * CPL channels per CTA.  It serves the plain fp32 scan
+// with 16-byte aligned rows in the single-segment and local-segment modes, for
+// 8 < N <= 16 (measured on GB300: as fast or faster than the cp.async kernel
+// there; slower for wide states, whose B/C ring costs occupancy).
+#ifndef SSCAN_TMA_SHAPES
+#define SSCAN_TMA_SHAPES(X) X(8, 2, 2) X(4, 4, 2)
+#endif
+inline int tma_channels(Shape sh) { return 4 * (32 / sh.P) * sh.CPL; }
+bool tma_has_shape(Shape sh);
+cudaError_t fwd_tma_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+int fwd_tma_occupancy(bool f32, Shape sh);
+cudaError_t fwd_tma_launch_f32(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+cudaError_t fwd_tma_launch_bf16(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+int fwd_tma_occupancy_f32(Shape sh);
+int fwd_tma_occupancy_bf16(Shape sh);
+// Encode a 3-D tensor map {L, rows, batch} of a contiguous [batch, rows, L]
+// fp32 or bf16 array with box {box_l, box_rows, 1} (false on failure).
+bool tma_encode_3d(CUtensorMap* map, const void* base, bool f32, long long L, long long rows, long long batch,
+                   int box_l, int box_rows);
+
 // A launch plan of the forward pass (defined in sscan_abi.cu).
 struct FwdPlan {
     Shape sh;
@@ -84,12 +106,20 @@ struct FwdPlan {
     long long tiles;  // channel tiles (CTAs per segment)
     long long S;      // time segments
     long long Tseg;   // steps per segment
+    bool tma;         // the single/local pass runs on the TMA-fed kernel
+    Shape corr_sh;    // cp.async-kernel shape of the carry correction
+    long long corr_tiles_per_batch;
+    long long corr_tiles;
 };
 // Choose the shape and time split.  lanes: 0 = automatic, else P; segments:
 // 0 = automatic, else S; max_segments (>= 1) caps an automatic split.
 // Returns SSCAN_OK, SSCAN_ERR_INVALID or SSCAN_ERR_CUDA.
 int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
              int lanes, long long max_segments, FwdPlan* out);
+// The plan of the fp32 TMA-fed kernel (plain scan, aligned rows, 8 < N <= 16;
+// lanes 0, 4 or 8), or SSCAN_ERR_INVALID when it does not apply.
+int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, int segments, int lanes,
+                 FwdPlan* out);
 
 // Shared implementation, included by the per-unit translation units only.
 #ifdef SSCAN_DISPATCH_IMPL

@@ -70,6 +70,8 @@ struct FwdParams {
     const float* delta_bias;  // [dim] added to delta, or NULL
     int delta_softplus;       // delta <- softplus(delta (+ bias)) inside the op
     int zoh;                  // zero-order-hold B-bar (the kernel's ZOH variant)
+    int* status;              // device status word: a bounded wait that gives up
+                              // stores SSCAN_ERR_TIMEOUT there
 };
 
 // softplus(x) = log(1 + e^x) from the MUFU exponent and logarithm: with

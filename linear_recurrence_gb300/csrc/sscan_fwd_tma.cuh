@@ -1,0 +1,468 @@
+// Selective-scan forward kernel fed by the Tensor Memory Accelerator, for
+// rows that satisfy the tensor-map rules (16-byte aligned rows, sizes below
+// 2^31).  It computes exactly what sscan_fwd_chunked computes (the recurrence
+// of "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战" section 2.3
+// with the initial/final state of its section 7.1), for the plain scan in the
+// single-segment and local-segment modes; the carry correction of a time
+// split and the fused options stay with sscan_fwd_chunked.
+//
+// What changes against the cp.async kernel is who waits for whom:
+//   * every warp owns its channels end to end.  Its u/delta rows arrive by
+//     one TMA box per row set and chunk, issued by its lane 0 into a
+//     three-stage ring that only this warp reads, completing on the warp's own
+//     mbarrier; the warp sums the P partial outputs of its channels itself
+//     (the lanes of a channel sit in one warp), so the chunk epilogue needs
+//     __syncwarp only;
+//   * the B/C rows of the chunk are shared by the CTA's four warps: one box
+//     each, completing on a CTA-wide mbarrier per stage.  A warp done with a
+//     stage (its lanes have consumed every value they read, then __syncwarp)
+//     counts itself out on a shared-memory counter, and the last of the four
+//     refills the stage, so no warp waits for another except for data that
+//     has not landed.  A refill only overwrites values already read, so the
+//     count needs no fence; the data itself is published by the mbarrier's
+//     transaction count and acquired by its wait;
+//   * bf16 rows are widened by each warp into its own fp32 rows (its u/delta
+//     and a private copy of B/C), which frees the raw stage at once.
+// Boxes are TC + 16 bytes wide: the extra columns (the next chunk's first
+// steps, or zeros past the end) pad every shared-memory row exactly as the
+// cp.async ring does, so the reads of different rows at one step fall in
+// different banks.  Every mbarrier wait is bounded (about a second); a wait
+// that gives up records SSCAN_ERR_TIMEOUT in the status word, waits (again
+// bounded) for the copies still in flight, and ends the warp's work.
+#pragma once
+
+#include <cuda.h>
+
+#include "../../include/sscan.h"
+#include "sscan_dispatch.cuh"
+#include "sscan_fwd_kernel.cuh"
+
+namespace sscan {
+
+// Tensor maps of one launch, 3-D with the innermost dimension first:
+// u and delta {L, dim, batch} with box {RROW, CPW, 1}; B and C {L, N, batch}
+// with box {RROW, NSP, 1}.  The box height past dim (or N) reads zeros.
+struct TmaMaps {
+    CUtensorMap u;
+    CUtensorMap delta;
+    CUtensorMap B;
+    CUtensorMap C;
+};
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+#ifndef SSCAN_TMA_STAGES
+#define SSCAN_TMA_STAGES 3
+#endif
+constexpr int kTmaStages = SSCAN_TMA_STAGES;  // depth of the u/delta and B/C rings
+
+template <typename T, int NS, int P, int CPL>
+struct TmaCfg {
+    using Base = FwdCfg<T, NS, P, CPL, 0>;
+    static constexpr int kWarps = 4;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int GPW = Base::GPW, CPW = Base::CPW, NSP = Base::NSP, TC = Base::TC;
+    static constexpr int DT = kWarps * CPW;  // channels per CTA
+    static constexpr int RROW = Base::RROW;  // raw row: TC + 16 bytes of elements
+    static constexpr int FROW = Base::FROW;  // fp32 row: TC + 4
+    static constexpr bool kF32 = Base::kF32;
+    static constexpr int STAGES = kTmaStages;
+    static constexpr int ESZ = (int)sizeof(T);
+    static constexpr int U_BOX = CPW * RROW * ESZ;   // bytes of one u (or delta) box
+    static constexpr int BC_BOX = NSP * RROW * ESZ;  // bytes of one B (or C) box
+    static constexpr int U_SLOT = align_up(U_BOX, 128);
+    static constexpr int BC_SLOT = align_up(BC_BOX, 128);
+    // partial outputs of a warp: [CPW][RS] with RS = P*FROW (+4 so that RS/4 is odd)
+    static constexpr int RS = ((P * FROW / 4) % 2 == 1) ? P * FROW : P * FROW + 4;
+    // bf16: a warp's fp32 rows [u CPW][delta CPW][B NSP][C NSP]
+    static constexpr int WORK_ROWS = 2 * CPW + 2 * NSP;
+    // items of the warp epilogue: (channel row, 4 steps); per lane
+    static constexpr int IPW = CPW * (TC / 4) / 32;
+    // shared-memory map (bytes from a 128-byte aligned base)
+    static constexpr int OFF_BAR = 0;  // mbarriers [kWarps + 1][STAGES], counters [STAGES]
+    static constexpr int OFF_U = 1024;  // [STAGES][kWarps][u, delta] slots
+    static constexpr int OFF_BC = OFF_U + STAGES * kWarps * 2 * U_SLOT;  // [STAGES][B, C] slots
+    static constexpr int OFF_WORK = OFF_BC + STAGES * 2 * BC_SLOT;
+    static constexpr int WORK_BYTES = kF32 ? 0 : WORK_ROWS * FROW * 4;  // per warp
+    static constexpr int OFF_YP = OFF_WORK + kWarps * WORK_BYTES;
+    static constexpr int YP_BYTES = CPW * RS * 4;  // per warp
+    static constexpr int SMEM_BYTES = OFF_YP + kWarps * YP_BYTES + 128;  // + base alignment
+    static_assert(TC == 32, "epilogue items assume 8 four-step blocks per chunk");
+    static_assert(CPW % 4 == 0, "a warp's epilogue items must fill its lanes");
+    static_assert((kWarps + 1) * STAGES * 8 + STAGES * 4 <= 1024, "barrier area");
+    static_assert(RROW * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
+    static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256, "tensor-map box limits");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// One chunk of the recurrence for the calling lane, from fp32 rows in shared
+// memory with row stride FROW: u rows su[r], delta rows sd[r] of the warp's
+// channel rows r = rl[j]; B/C rows of state slot n at sB[n], sC[n].  Per
+// 4-step block: the lane's u/delta vectors, then its states in quads (B/C of
+// 4 states x 4 steps), each element doing x = delta*A', a = 2^x,
+// h = a*h + (delta*u)*B, y += C*h; the 4 partial outputs of each channel go
+// to yp[rl[j]][g] as one vector.  SCALAR: one decay rate per channel.
+template <int NS, int P, int CPL, int FROW, int RS, bool SCALAR>
+__device__ __forceinline__ void compute_chunk_tma(const float* su, const float* sd, const float* sB,
+                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
+                                                  const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                                  float (&h)[CPL][NS]) {
+    constexpr int TC = kChunkSteps;
+    constexpr int QS = NS < 4 ? NS : 4;
+    constexpr int NQ = NS / QS;
+    static_assert(NS % QS == 0, "states come in whole quads");
+    const float* bB = sB + g * FROW;
+    const float* bC = sC + g * FROW;
+#pragma unroll kBlockUnroll
+    for (int t4 = 0; t4 < TC; t4 += 4) {
+        float dd[CPL][4], du[CPL][4], as[CPL][4], y[CPL][4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            float uu[4];
+            load4_smem(su + rl[j] * FROW + t4, uu);
+            load4_smem(sd + rl[j] * FROW + t4, dd[j]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                du[j][s] = dd[j][s] * uu[s];
+                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                y[j][s] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float bb[QS][4], cc[QS][4];
+#pragma unroll
+            for (int kk = 0; kk < QS; ++kk) {
+                const int k = q * QS + kk;
+                load4_smem(bB + k * P * FROW + t4, bb[kk]);
+                load4_smem(bC + k * P * FROW + t4, cc[kk]);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int kk = 0; kk < QS; ++kk) {
+                        const int k = q * QS + kk;
+                        const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
+                        h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[kk][s]);
+                        y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
+                    }
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            *reinterpret_cast<float4*>(yp + rl[j] * RS + g * FROW + t4) = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+    }
+}
+
+// bf16: widen rows [0, nrows) of TC (+ padding) elements, stride RROW, into
+// fp32 rows of stride FROW; one 16-byte piece (8 values) per item.
+template <int RROW, int FROW, int TC>
+__device__ __forceinline__ void widen_rows_warp(const bf16* src, float* dst, int nrows, int lane) {
+    constexpr int Q8 = TC / 8;
+    for (int q = lane; q < nrows * Q8; q += 32) {
+        const int r = q / Q8, c = (q % Q8) * 8;
+        widen8(src + r * RROW + c, dst + r * FROW + c);
+    }
+}
+
+template <typename T, int NS, int P, int CPL>
+__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
+    sscan_fwd_tma(const FwdParams p, const __grid_constant__ TmaMaps tm) {
+    using Cfg = TmaCfg<T, NS, P, CPL>;
+    constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
+    constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW, RS = Cfg::RS, STAGES = Cfg::STAGES;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ unsigned char smem_dyn[];
+    unsigned char* sbase = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~static_cast<uintptr_t>(127));
+    uint64_t* barU = reinterpret_cast<uint64_t*>(sbase + Cfg::OFF_BAR);  // [kWarps][STAGES]
+    uint64_t* barBC = barU + kWarps * STAGES;                              // [STAGES]
+    unsigned* bc_count = reinterpret_cast<unsigned*>(barBC + STAGES);      // [STAGES]
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int g = lane % P, gi = lane / P;
+    const int tile = blockIdx.x / p.seg_count;
+    const int s = blockIdx.x % p.seg_count;  // single or local mode: segment index
+    const long long b = tile / p.tiles_per_batch;
+    const long long d0 = (long long)(tile % p.tiles_per_batch) * Cfg::DT;
+    const long long dw = d0 + (long long)w * CPW;  // the warp's first channel
+    const long long t_begin = (long long)s * p.Tseg;
+    const long long t_end = min(p.L, t_begin + p.Tseg);
+    const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + TC - 1) / TC) : 0;
+    const int N = (int)p.N;
+
+    unsigned char* u_ring = sbase + Cfg::OFF_U;
+    unsigned char* bc_ring = sbase + Cfg::OFF_BC;
+    float* yp = reinterpret_cast<float*>(sbase + Cfg::OFF_YP + w * Cfg::YP_BYTES);
+    auto u_slot = [&](int st) -> T* {
+        return reinterpret_cast<T*>(u_ring + (st * kWarps + w) * 2 * Cfg::U_SLOT);
+    };
+    auto bc_slot = [&](int st) -> T* { return reinterpret_cast<T*>(bc_ring + st * 2 * Cfg::BC_SLOT); };
+
+    if (tid == 0) {
+        for (int i = 0; i < (kWarps + 1) * STAGES; ++i) mbar_init(barU + i, 1);
+        for (int i = 0; i < STAGES; ++i) bc_count[i] = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // the warp's u/delta boxes of chunk c into stage st (lane 0 only)
+    auto issue_u = [&](int c, int st) {
+        T* dst = u_slot(st);
+        uint64_t* bar = barU + w * STAGES + st;
+        mbar_arrive_expect_tx(bar, 2 * Cfg::U_BOX);
+        const int t0 = (int)(t_begin + (long long)c * TC);
+        tma_load_3d(dst, &tm.u, t0, (int)dw, (int)b, bar);
+        tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::U_SLOT, &tm.delta, t0, (int)dw, (int)b, bar);
+    };
+    // the B/C boxes of chunk c into stage st (one thread)
+    auto issue_bc = [&](int c, int st) {
+        T* dst = bc_slot(st);
+        uint64_t* bar = barBC + st;
+        mbar_arrive_expect_tx(bar, 2 * Cfg::BC_BOX);
+        const int t0 = (int)(t_begin + (long long)c * TC);
+        tma_load_3d(dst, &tm.B, t0, 0, (int)b, bar);
+        tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::BC_SLOT, &tm.C, t0, 0, (int)b, bar);
+    };
+    if (lane == 0) {
+        for (int c = 0; c < STAGES && c < nchunks; ++c) {
+            issue_u(c, c);
+            if (w == 0) issue_bc(c, c);
+        }
+    }
+
+    // the lane's channels (rows rl[j] of the warp) and their decay rates
+    int rl[CPL];
+    long long ch[CPL];
+    bool dval[CPL];
+    float Al2[CPL][NS], As[CPL], h[CPL][NS];
+    bool uniform_rate = true;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        rl[j] = j * GPW + gi;
+        const long long dch = dw + rl[j];
+        dval[j] = dch < p.dim;
+        ch[j] = b * p.dim + (dval[j] ? dch : 0);
+        const float a_first = dval[j] ? p.A[dch * p.N] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int n = k * P + g;
+            const bool nv = dval[j] && n < N;
+            const float a = nv ? p.A[dch * p.N + n] : a_first;
+            uniform_rate &= (a == a_first);
+            Al2[j][k] = nv ? a * kLog2e : 0.f;
+            h[j][k] = (s == 0 && p.h0 != nullptr && nv) ? p.h0[ch[j] * p.N + n] : 0.f;
+        }
+        As[j] = a_first * kLog2e;
+    }
+    const bool scalar = __all_sync(FULL, uniform_rate);
+
+    // epilogue slots: item q = lane + 32k covers channel row q/8, steps 4(q%8)..+3
+    const bool dsum_on = p.mode == MODE_LOCAL;
+    float dsum[Cfg::IPW], dcomp[Cfg::IPW];  // Kahan sums of delta per slot
+#pragma unroll
+    for (int k = 0; k < Cfg::IPW; ++k) dsum[k] = dcomp[k] = 0.f;
+    float Dr[Cfg::IPW];
+#pragma unroll
+    for (int k = 0; k < Cfg::IPW; ++k) {
+        const long long dd = dw + (lane + 32 * k) / 8;
+        Dr[k] = (p.D != nullptr && dd < p.dim) ? __ldg(p.D + dd) : 0.f;
+    }
+    T* gout = static_cast<T*>(p.out);
+    float* work = reinterpret_cast<float*>(sbase + Cfg::OFF_WORK + w * Cfg::WORK_BYTES);
+
+    int i = 0;
+    bool ok = true;
+    for (; i < nchunks; ++i) {
+        const int st = i % STAGES;
+        const unsigned par = (unsigned)(i / STAGES) & 1u;
+        ok = mbar_wait_bounded(barU + w * STAGES + st, par);
+        ok = mbar_wait_bounded(barBC + st, par) && ok;
+        ok = __all_sync(FULL, ok);
+        if (!ok) break;
+        const int nx = i + STAGES;  // the chunk that refills this stage
+        const float *su, *sd, *sB, *sC;
+        if constexpr (Cfg::kF32) {
+            su = reinterpret_cast<const float*>(u_slot(st));
+            sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
+            sB = reinterpret_cast<const float*>(bc_slot(st));
+            sC = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(sB) + Cfg::BC_SLOT);
+        } else {
+            // widen the warp's u/delta rows and the chunk's B/C rows into its
+            // own fp32 rows, then hand both raw stages back
+            const bf16* ru = reinterpret_cast<const bf16*>(u_slot(st));
+            widen_rows_warp<RROW, FROW, TC>(ru, work, CPW, lane);
+            widen_rows_warp<RROW, FROW, TC>(
+                reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(ru) + Cfg::U_SLOT),
+                work + CPW * FROW, CPW, lane);
+            const bf16* rb = reinterpret_cast<const bf16*>(bc_slot(st));
+            widen_rows_warp<RROW, FROW, TC>(rb, work + 2 * CPW * FROW, NSP, lane);
+            widen_rows_warp<RROW, FROW, TC>(
+                reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(rb) + Cfg::BC_SLOT),
+                work + (2 * CPW + NSP) * FROW, NSP, lane);
+            su = work;
+            sd = work + CPW * FROW;
+            sB = work + 2 * CPW * FROW;
+            sC = work + (2 * CPW + NSP) * FROW;
+        }
+        if constexpr (!Cfg::kF32) {
+            __syncwarp();
+            if (lane == 0) {
+                if (nx < nchunks) issue_u(nx, st);
+                const unsigned old = atomicAdd(bc_count + st, 1u);
+                if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+            }
+        }
+        if (scalar)
+            compute_chunk_tma<NS, P, CPL, FROW, RS, true>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
+        else
+            compute_chunk_tma<NS, P, CPL, FROW, RS, false>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
+        __syncwarp();
+        if constexpr (Cfg::kF32) {
+            // B/C of this stage are no longer read by this warp
+            if (lane == 0) {
+                const unsigned old = atomicAdd(bc_count + st, 1u);
+                if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+            }
+        }
+        // warp epilogue: sum the P partials, add D*u, store 4 steps per item
+        const long long t0 = t_begin + (long long)i * TC;
+#pragma unroll
+        for (int k = 0; k < Cfg::IPW; ++k) {
+            const int q = lane + 32 * k;
+            const int r = q / 8, t4 = (q % 8) * 4;
+            const long long dd = dw + r, t = t0 + t4;
+            float v[4];
+            load4_smem(yp + r * RS + t4, v);
+#pragma unroll
+            for (int gg = 1; gg < P; ++gg) {
+                float x[4];
+                load4_smem(yp + r * RS + gg * FROW + t4, x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] += x[e];
+            }
+            float uv[4];
+            load4_smem(su + r * FROW + t4, uv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
+            if (dsum_on) {  // steps past the segment hold delta = 0
+                float dv[4];
+                load4_smem(sd + r * FROW + t4, dv);
+                const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dcomp[k];
+                const float tk = dsum[k] + yk;
+                dcomp[k] = (tk - dsum[k]) - yk;
+                dsum[k] = tk;
+            }
+            if (dd < p.dim && t < t_end) {  // t_end is a multiple of 4 on this path
+                T* o = gout + (b * p.dim + dd) * p.L + t;
+                if constexpr (Cfg::kF32) {
+                    *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+                    const unsigned lo = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[0])) |
+                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[1])) << 16);
+                    const unsigned hi = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[2])) |
+                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[3])) << 16);
+                    *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+                }
+            }
+        }
+        __syncwarp();
+        if constexpr (Cfg::kF32) {
+            // u/delta of this stage are no longer read by this warp
+            if (lane == 0 && nx < nchunks) issue_u(nx, st);
+        }
+    }
+    if (!ok) {
+        // a wait gave up: record it, then wait (bounded) for the copies this
+        // warp may still have in flight before leaving
+        if (lane == 0) {
+            atomicExch(p.status, (int)SSCAN_ERR_TIMEOUT);
+            for (int c = i; c < nchunks && c < i + STAGES; ++c) {
+                mbar_wait_bounded(barU + w * STAGES + c % STAGES, (unsigned)(c / STAGES) & 1u);
+                mbar_wait_bounded(barBC + c % STAGES, (unsigned)(c / STAGES) & 1u);
+            }
+        }
+        return;
+    }
+
+    if (dsum_on) {  // the segment's sum of delta per channel: 8 slots in 8 lanes
+#pragma unroll
+        for (int k = 0; k < Cfg::IPW; ++k) {
+            float v = dsum[k];
+            v += __shfl_xor_sync(FULL, v, 1);
+            v += __shfl_xor_sync(FULL, v, 2);
+            v += __shfl_xor_sync(FULL, v, 4);
+            const long long dd = dw + (lane + 32 * k) / 8;
+            if ((lane & 7) == 0 && dd < p.dim) p.seg_dsum[(b * p.dim + dd) * p.S + s] = v;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        if (!dval[j]) continue;
+        float* dst = p.mode == MODE_LOCAL ? p.seg_state + (ch[j] * p.S + s) * p.N : p.final_state == nullptr ? nullptr : p.final_state + ch[j] * p.N;
+        if (dst == nullptr) continue;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int n = k * P + g;
+            if (n < N) dst[n] = h[j][k];
+        }
+    }
+}
+
+// Shared implementation of the per-dtype launch units (sscan_fwd_tma_*.cu).
+#ifdef SSCAN_TMA_IMPL
+template <typename T, int NS, int P, int CPL>
+cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream) {
+    using Cfg = TmaCfg<T, NS, P, CPL>;
+    if (p.N < 1 || p.N > (long long)Cfg::NSP) return cudaErrorInvalidValue;
+    TmaMaps tm;
+    const bool f32 = Cfg::kF32;
+    if (!tma_encode_3d(&tm.u, p.u, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
+        !tma_encode_3d(&tm.delta, p.delta, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
+        !tma_encode_3d(&tm.B, p.B, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP) ||
+        !tma_encode_3d(&tm.C, p.C, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP))
+        return cudaErrorInvalidValue;
+    auto kern = sscan_fwd_tma<T, NS, P, CPL>;
+    static unsigned long long configured = 0;  // bit per device ordinal (< 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+    }
+    kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p, tm);
+    return cudaGetLastError();
+}
+
+template <typename T, int NS, int P, int CPL>
+int occupancy_tma_variant() {
+    using Cfg = TmaCfg<T, NS, P, CPL>;
+    auto kern = sscan_fwd_tma<T, NS, P, CPL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Cfg::kThreads, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+#define SSCAN_TMA_LAUNCH_CASE(P_, NS_, CPL_) \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return launch_tma_variant<UnitT, NS_, P_, CPL_>(p, grid, st);
+#define SSCAN_TMA_OCC_CASE(P_, NS_, CPL_) \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_tma_variant<UnitT, NS_, P_, CPL_>();
+#define SSCAN_DEFINE_TMA_UNIT(SUFFIX)                                                               \
+    cudaError_t fwd_tma_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t st) { \
+        SSCAN_TMA_SHAPES(SSCAN_TMA_LAUNCH_CASE)                                                     \
+        return cudaErrorInvalidValue;                                                               \
+    }                                                                                               \
+    int fwd_tma_occupancy_##SUFFIX(Shape sh) {                                                      \
+        SSCAN_TMA_SHAPES(SSCAN_TMA_OCC_CASE)                                                        \
+        return 0;                                                                                   \
+    }
+#endif  // SSCAN_TMA_IMPL
+
+}  // namespace sscan

@@ -124,6 +124,29 @@ def test_lane_shapes(lr, lanes, N, shape, dtype):
     assert tag in lr.last_plan() and "S=3" in lr.last_plan(), lr.last_plan()
 
 
+# the TMA-fed kernel (fp32, plain scan, 16-byte aligned rows, 8 < N <= 16):
+# (batch, dim, L, N, lanes, segments, use_D, use_h0)
+TMA_CASES = [
+    (3, 70, 1004, 16, 8, 0, True, True),    # ragged channel tile, 12-step tail chunk
+    (2, 130, 2048, 12, 4, 0, True, True),   # N < 16: box rows past N read zeros
+    (1, 33, 4096, 16, 4, 5, False, True),   # time split, no skip term
+    (2, 64, 996, 9, 8, 3, True, False),     # no h0, short last segment
+    (1, 300, 64, 16, 0, 0, True, True),     # two chunks, warps wholly past dim
+    (4, 17, 8, 16, 8, 0, True, True),       # a partial first chunk only
+]
+
+
+@pytest.mark.parametrize("case", TMA_CASES, ids=lambda c: "x".join(map(str, c[:4])))
+def test_tma_path(lr, case):
+    batch, dim, L, N, lanes, segments, use_D, use_h0 = case
+    w = workloads.WORKLOADS["long64k"].scaled(batch=batch, dim=dim, L=L, N=N)
+    plan = _compare(lr, w, workloads.make_inputs(w), TOL["f32"], lanes=lanes, segments=segments,
+                    use_D=use_D, use_h0=use_h0)
+    assert " tma " in plan, plan
+    if segments:
+        assert f"S={segments} " in plan, plan
+
+
 # --------------------------------------------------------------------------
 # odd shapes and degenerate cases
 
