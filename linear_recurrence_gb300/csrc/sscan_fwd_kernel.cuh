@@ -120,6 +120,11 @@ constexpr int kChunkSteps = SSCAN_CHUNK_STEPS;  // steps per chunk (TC); segment
 // the loop body small enough for the instruction cache at every shape
 constexpr int kBlockUnroll = SSCAN_BLOCK_UNROLL;
 
+#ifndef SSCAN_CP_STAGES
+#define SSCAN_CP_STAGES 3
+#endif
+constexpr int kCpStages = SSCAN_CP_STAGES;  // depth of the cp.async ring
+
 constexpr int warps_for(int P, int CPL) {
     return (16 * P) / (32 * CPL) < 2 ? 2 : ((16 * P) / (32 * CPL) > 8 ? 8 : (16 * P) / (32 * CPL));
 }
@@ -146,7 +151,7 @@ struct FwdCfg {
     static constexpr int ZROW0 = 2 * DT + 2 * NSP;    // first z row (options only)
     static constexpr int RAW_ELEMS = ROWS * RROW;
     static constexpr int RAW_BYTES = RAW_ELEMS * (int)sizeof(T);
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = kCpStages;
     // fp32 rows the lanes read: the raw stage itself for fp32 I/O (RROW == FROW),
     // a widened copy for bf16
     static constexpr int WORK_FLOATS = kF32 ? 0 : ROWS * FROW;
@@ -167,11 +172,12 @@ struct FwdCfg {
 
 // State entering segment s (s >= 1) for the lane's states n = k*P + g of one
 // channel: the fold of the aggregates of segments 0 .. s-1 (segment 0's entry
-// holds its true end state because it started from h0).  Four segments' loads
-// are issued before their folds so the chain waits on memory once per four.
+// holds its true end state because it started from h0).  FB segments' loads
+// are issued before their folds so the chain waits on memory once per FB.
 template <int NS, int P>
 __device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, int s, int g,
                                               const float (&Al2)[NS], float (&h)[NS]) {
+    constexpr int FB = NS <= 2 ? 16 : NS <= 4 ? 8 : 4;
     const float* st = p.seg_state + ch * p.S * p.N;
     const float* ds = p.seg_dsum + ch * p.S;
 #pragma unroll
@@ -179,10 +185,10 @@ __device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, 
         const long long n = (long long)k * P + g;
         h[k] = n < p.N ? st[n] : 0.f;
     }
-    for (int sp = 1; sp < s; sp += 4) {
-        float dv[4], bv[4][NS];
+    for (int sp = 1; sp < s; sp += FB) {
+        float dv[FB], bv[FB][NS];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < FB; ++q) {
             const bool on = sp + q < s;
             dv[q] = on ? ds[sp + q] : 0.f;
 #pragma unroll
@@ -192,7 +198,7 @@ __device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, 
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < FB; ++q) {
             if (sp + q < s) {
 #pragma unroll
                 for (int k = 0; k < NS; ++k) h[k] = fmaf(ex2(Al2[k] * dv[q]), h[k], bv[q][k]);
@@ -453,6 +459,67 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
     }
 }
 
+// One chunk of the carry correction for the calling lane: the homogeneous
+// recurrence h = exp(delta*A) * h from the carried state, with its
+// C-contraction stored as partial outputs exactly as compute_chunk stores
+// them.  A state slot k whose carry has fallen below the lane's threshold in
+// every lane of the warp is frozen: its term is below 2^-24 of the largest
+// carry component and only keeps decaying, so it is skipped (a warp-uniform
+// branch, checked once per 4-step block).  SCALAR: one decay rate per channel
+// (the states decay together; no per-slot check).
+template <typename T, int NS, int P, int CPL, int OPT, bool SCALAR>
+__device__ __forceinline__ void decay_chunk(const float* rows, float* yp, const int (&rr)[CPL], int g,
+                                            const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                            const float (&thr)[CPL], float (&h)[CPL][NS]) {
+    using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
+    constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, NSP = Cfg::NSP, RS = Cfg::RS;
+    constexpr unsigned FULL = 0xffffffffu;
+    const float* sd = rows + DT * FROW;
+    const float* sC = rows + (2 * DT + NSP + g) * FROW;
+#pragma unroll kBlockUnroll
+    for (int t4 = 0; t4 < TC; t4 += 4) {
+        bool live[NS];
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            if (SCALAR) {  // one rate: the states decay together
+                live[k] = true;
+                continue;
+            }
+            bool l = false;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) l |= fabsf(h[j][k]) > thr[j];
+            live[k] = __any_sync(FULL, l);
+        }
+        float dd[CPL][4], as[CPL][4], y[CPL][4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            load4_smem(sd + rr[j] * FROW + t4, dd[j]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                y[j][s] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            if (!live[k]) continue;
+            float cc[4];
+            load4_smem(sC + k * P * FROW + t4, cc);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
+                    h[j][k] *= a;
+                    y[j][s] = fmaf(cc[s], h[j][k], y[j][s]);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            *reinterpret_cast<float4*>(yp + rr[j] * RS + g * FROW + t4) = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+    }
+}
+
 // Sum the P partials of every output of the chunk, add the skip term D*u and
 // store it (CORR: add it to the output already written, no skip term).  Item
 // q covers 4 steps of tile row q % DT; a thread's items keep their (row,
@@ -695,8 +762,8 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
         const float* rows = sm.rows(i);
         if (corr) {
-            if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
-            else compute_chunk<T, NS, P, CPL, OPT, true, false, true, false>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
+            if (scalar) decay_chunk<T, NS, P, CPL, OPT, true>(rows, sm.yp, rr, g, Al2, As, thr, h);
+            else decay_chunk<T, NS, P, CPL, OPT, false>(rows, sm.yp, rr, g, Al2, As, thr, h);
         } else {
             if (scalar) compute_chunk<T, NS, P, CPL, OPT, true, true, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);
             else compute_chunk<T, NS, P, CPL, OPT, true, false, false, OPT == 2>(rows, sm.yp, rr, g, Al2, As, invA, invAs, h);

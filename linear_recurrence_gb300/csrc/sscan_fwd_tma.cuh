@@ -173,9 +173,10 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
     constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW, RS = Cfg::RS, STAGES = Cfg::STAGES;
     constexpr unsigned FULL = 0xffffffffu;
-    extern __shared__ unsigned char smem_dyn[];
-    unsigned char* sbase = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~static_cast<uintptr_t>(127));
+    extern __shared__ __align__(16) unsigned char smem_dyn[];
+    // 128-byte aligned base, offset from the shared array itself so that the
+    // compiler keeps every derived pointer in the shared address space
+    unsigned char* sbase = smem_dyn + ((128u - (smem_addr(smem_dyn) & 127u)) & 127u);
     uint64_t* barU = reinterpret_cast<uint64_t*>(sbase + Cfg::OFF_BAR);  // [kWarps][STAGES]
     uint64_t* barBC = barU + kWarps * STAGES;                              // [STAGES]
     unsigned* bc_count = reinterpret_cast<unsigned*>(barBC + STAGES);      // [STAGES]
