@@ -97,8 +97,9 @@ void record_error(cudaError_t e) { fail_cuda(e); }
 #define SSCAN_TARGET_WARPS 12
 #endif
 constexpr long long kTargetWarpsPerSm = SSCAN_TARGET_WARPS;
-// Shortest automatic segment, in chunks.
+// Shortest automatic segment, in chunks (cp.async kernel, TMA kernel).
 constexpr long long kMinSegmentChunks = 8;
+constexpr long long kMinTmaSegmentChunks = 13;
 
 // Automatic shape per state count, measured on GB300: two or four states per
 // lane and one channel per lane keep the most warps in flight, which the
@@ -217,14 +218,16 @@ int cached_tma_occupancy(Shape sh) {
 }
 
 // Plan of the fp32 TMA-fed kernel for 8 < N <= 16 (its shapes hold 16 state
-// slots), or SSCAN_ERR_INVALID when it does not apply.  A time split is sized
-// so that the local pass fills the GPU's resident CTA slots in one wave (the
-// pass time is then proportional to the segment length, so the most segments
-// that fit one wave are best); the automatic shape is the one with the most
-// channels per lane whose segments stay long enough (measured on GB300:
-// (4,4,2) from 16 chunks per segment, else (8,2,2); 512 channels x 8192 steps
-// then take (8,2,2) in 19 segments of 14 chunks).  The carry correction runs
-// on the cp.async kernel with one channel per lane.
+// slots), or SSCAN_ERR_INVALID when it does not apply.  A time split fills at
+// most one wave of the GPU's resident CTA slots and keeps segments of about
+// 14 chunks or more: every segment beyond the first adds a carry correction over the
+// decay horizon of its entry state (a few chunks for typical step sizes), so
+// shorter segments cost more in corrections than they gain in local-pass
+// parallelism (measured on GB300 with 512 channels x 8192 steps: 16, 18, 19
+// and 26 segments 55, 53, 51 and 58 us; 1536 x 65536: 12 segments 603 us,
+// 19 segments 575 us).  The automatic shape is the one with the most channels per lane
+// whose segments stay at least 16 chunks long ((4,4,2)), else (8,2,2).  The
+// carry correction runs on the cp.async kernel with one channel per lane.
 int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, int segments, int lanes,
                  FwdPlan* out) {
     if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
@@ -247,7 +250,7 @@ int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, 
         long long S = segments;
         if (S == 0) {
             S = pl.tiles >= slots ? 1 : slots / pl.tiles;
-            S = std::min(S, std::max(1LL, seqlen / (kMinSegmentChunks * TC)));
+            S = std::min(S, std::max(1LL, seqlen / (kMinTmaSegmentChunks * TC)));
         }
         S = std::max(1LL, std::min(S, ceil_div(seqlen, TC)));
         pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;

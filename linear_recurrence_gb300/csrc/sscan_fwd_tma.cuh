@@ -9,7 +9,7 @@
 // What changes against the cp.async kernel is who waits for whom:
 //   * every warp owns its channels end to end.  Its u/delta rows arrive by
 //     one TMA box per row set and chunk, issued by its lane 0 into a
-//     three-stage ring that only this warp reads, completing on the warp's own
+//     two-stage ring that only this warp reads, completing on the warp's own
 //     mbarrier; the warp sums the P partial outputs of its channels itself
 //     (the lanes of a channel sit in one warp), so the chunk epilogue needs
 //     __syncwarp only;
@@ -51,10 +51,13 @@ struct TmaMaps {
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// Depth of the u/delta and B/C rings.  Two stages measured faster than three
+// on GB300: the smaller footprint fits one more CTA per SM, and a chunk of
+// compute (over a microsecond per warp) covers the TMA latency.
 #ifndef SSCAN_TMA_STAGES
-#define SSCAN_TMA_STAGES 3
+#define SSCAN_TMA_STAGES 2
 #endif
-constexpr int kTmaStages = SSCAN_TMA_STAGES;  // depth of the u/delta and B/C rings
+constexpr int kTmaStages = SSCAN_TMA_STAGES;
 
 template <typename T, int NS, int P, int CPL>
 struct TmaCfg {
@@ -72,12 +75,18 @@ struct TmaCfg {
     static constexpr int BC_BOX = NSP * RROW * ESZ;  // bytes of one B (or C) box
     static constexpr int U_SLOT = align_up(U_BOX, 128);
     static constexpr int BC_SLOT = align_up(BC_BOX, 128);
-    // partial outputs of a warp: [CPW][RS] with RS = P*FROW (+4 so that RS/4 is odd)
-    static constexpr int RS = ((P * FROW / 4) % 2 == 1) ? P * FROW : P * FROW + 4;
+    // the epilogue runs per half chunk: partial outputs of a warp [CPW][RS]
+    // over TS steps, row (channel) stride RS = P*HROW rounded up so that
+    // RS/4 = 4 (mod 8): the partial vectors a quarter-warp stores (P lanes of
+    // a channel, 8/P channels) and the ones it reads back (two channel rows)
+    // fall in distinct bank groups
+    static constexpr int TS = TC / 2;
+    static constexpr int HROW = TS + 4;
+    static constexpr int RS = align_up(P * HROW - 16, 32) + 16;
     // bf16: a warp's fp32 rows [u CPW][delta CPW][B NSP][C NSP]
     static constexpr int WORK_ROWS = 2 * CPW + 2 * NSP;
-    // items of the warp epilogue: (channel row, 4 steps); per lane
-    static constexpr int IPW = CPW * (TC / 4) / 32;
+    // items of the warp epilogue per half chunk: (channel row, 4 steps); per lane
+    static constexpr int IPH = CPW * (TS / 4) / 32;
     // shared-memory map (bytes from a 128-byte aligned base)
     static constexpr int OFF_BAR = 0;  // mbarriers [kWarps + 1][STAGES], counters [STAGES]
     static constexpr int OFF_U = 1024;  // [STAGES][kWarps][u, delta] slots
@@ -88,33 +97,34 @@ struct TmaCfg {
     static constexpr int YP_BYTES = CPW * RS * 4;  // per warp
     static constexpr int SMEM_BYTES = OFF_YP + kWarps * YP_BYTES + 128;  // + base alignment
     static_assert(TC == 32, "epilogue items assume 8 four-step blocks per chunk");
-    static_assert(CPW % 4 == 0, "a warp's epilogue items must fill its lanes");
+    static_assert(CPW % 8 == 0, "a warp's epilogue items must fill its lanes");
+    static_assert(RS >= P * HROW && (RS / 4) % 8 == 4, "partial row stride");
     static_assert((kWarps + 1) * STAGES * 8 + STAGES * 4 <= 1024, "barrier area");
     static_assert(RROW * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
     static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256, "tensor-map box limits");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// One chunk of the recurrence for the calling lane, from fp32 rows in shared
-// memory with row stride FROW: u rows su[r], delta rows sd[r] of the warp's
-// channel rows r = rl[j]; B/C rows of state slot n at sB[n], sC[n].  Per
-// 4-step block: the lane's u/delta vectors, then its states in quads (B/C of
-// 4 states x 4 steps), each element doing x = delta*A', a = 2^x,
-// h = a*h + (delta*u)*B, y += C*h; the 4 partial outputs of each channel go
-// to yp[rl[j]][g] as one vector.  SCALAR: one decay rate per channel.
-template <int NS, int P, int CPL, int FROW, int RS, bool SCALAR>
+// Steps [T0, T0 + TS) of a chunk of the recurrence for the calling lane, from
+// fp32 rows in shared memory with row stride FROW: u rows su[r], delta rows
+// sd[r] of the warp's channel rows r = rl[j]; B/C rows of state slot n at
+// sB[n], sC[n].  Per 4-step block: the lane's u/delta vectors, then its
+// states in quads (B/C of 4 states x 4 steps), each element doing
+// x = delta*A', a = 2^x, h = a*h + (delta*u)*B, y += C*h; the 4 partial
+// outputs of each channel go to yp[rl[j]][g] (row stride RS, lane stride
+// HROW) as one vector.  SCALAR: one decay rate per channel.
+template <int NS, int P, int CPL, int FROW, int RS, int HROW, int T0, int TS, bool SCALAR>
 __device__ __forceinline__ void compute_chunk_tma(const float* su, const float* sd, const float* sB,
                                                   const float* sC, float* yp, const int (&rl)[CPL], int g,
                                                   const float (&Al2)[CPL][NS], const float (&As)[CPL],
                                                   float (&h)[CPL][NS]) {
-    constexpr int TC = kChunkSteps;
     constexpr int QS = NS < 4 ? NS : 4;
     constexpr int NQ = NS / QS;
     static_assert(NS % QS == 0, "states come in whole quads");
     const float* bB = sB + g * FROW;
     const float* bC = sC + g * FROW;
 #pragma unroll kBlockUnroll
-    for (int t4 = 0; t4 < TC; t4 += 4) {
+    for (int t4 = T0; t4 < T0 + TS; t4 += 4) {
         float dd[CPL][4], du[CPL][4], as[CPL][4], y[CPL][4];
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
@@ -151,7 +161,8 @@ __device__ __forceinline__ void compute_chunk_tma(const float* su, const float* 
         }
 #pragma unroll
         for (int j = 0; j < CPL; ++j)
-            *reinterpret_cast<float4*>(yp + rl[j] * RS + g * FROW + t4) = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+            *reinterpret_cast<float4*>(yp + rl[j] * RS + g * HROW + (t4 - T0)) =
+                make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
     }
 }
 
@@ -259,19 +270,64 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     }
     const bool scalar = __all_sync(FULL, uniform_rate);
 
-    // epilogue slots: item q = lane + 32k covers channel row q/8, steps 4(q%8)..+3
+    // epilogue slots per half chunk: item q = lane + 32k covers channel row
+    // q/4, steps 4(q%4)..+3 of the half
     const bool dsum_on = p.mode == MODE_LOCAL;
-    float dsum[Cfg::IPW], dcomp[Cfg::IPW];  // Kahan sums of delta per slot
+    float dsum[2][Cfg::IPH], dcomp[2][Cfg::IPH];  // Kahan sums of delta per slot
 #pragma unroll
-    for (int k = 0; k < Cfg::IPW; ++k) dsum[k] = dcomp[k] = 0.f;
-    float Dr[Cfg::IPW];
+    for (int k = 0; k < Cfg::IPH; ++k) dsum[0][k] = dcomp[0][k] = dsum[1][k] = dcomp[1][k] = 0.f;
+    float Dr[Cfg::IPH];
 #pragma unroll
-    for (int k = 0; k < Cfg::IPW; ++k) {
-        const long long dd = dw + (lane + 32 * k) / 8;
+    for (int k = 0; k < Cfg::IPH; ++k) {
+        const long long dd = dw + (lane + 32 * k) / 4;
         Dr[k] = (p.D != nullptr && dd < p.dim) ? __ldg(p.D + dd) : 0.f;
     }
     T* gout = static_cast<T*>(p.out);
     float* work = reinterpret_cast<float*>(sbase + Cfg::OFF_WORK + w * Cfg::WORK_BYTES);
+
+    // warp epilogue of one half chunk: sum the P partials, add D*u, store 4
+    // steps per item (and the Kahan sums of delta of a local pass)
+    auto epilogue = [&](int half, long long t0, const float* su, const float* sd) {
+#pragma unroll
+        for (int k = 0; k < Cfg::IPH; ++k) {
+            const int q = lane + 32 * k;
+            const int r = q / 4, t4l = (q % 4) * 4, t4 = half * Cfg::TS + t4l;
+            const long long dd = dw + r, t = t0 + t4;
+            float v[4];
+            load4_smem(yp + r * RS + t4l, v);
+#pragma unroll
+            for (int gg = 1; gg < P; ++gg) {
+                float x[4];
+                load4_smem(yp + r * RS + gg * Cfg::HROW + t4l, x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] += x[e];
+            }
+            float uv[4];
+            load4_smem(su + r * FROW + t4, uv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
+            if (dsum_on) {  // steps past the segment hold delta = 0
+                float dv[4];
+                load4_smem(sd + r * FROW + t4, dv);
+                const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dcomp[half][k];
+                const float tk = dsum[half][k] + yk;
+                dcomp[half][k] = (tk - dsum[half][k]) - yk;
+                dsum[half][k] = tk;
+            }
+            if (dd < p.dim && t < t_end) {  // t_end is a multiple of 4 on this path
+                T* o = gout + (b * p.dim + dd) * p.L + t;
+                if constexpr (Cfg::kF32) {
+                    *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+                    const unsigned lo = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[0])) |
+                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[1])) << 16);
+                    const unsigned hi = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[2])) |
+                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[3])) << 16);
+                    *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+                }
+            }
+        }
+    };
 
     int i = 0;
     bool ok = true;
@@ -315,10 +371,19 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
                 if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
             }
         }
+        constexpr int TS = Cfg::TS, HROW = Cfg::HROW;
+        const long long t0 = t_begin + (long long)i * TC;
         if (scalar)
-            compute_chunk_tma<NS, P, CPL, FROW, RS, true>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
+            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, 0, TS, true>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
         else
-            compute_chunk_tma<NS, P, CPL, FROW, RS, false>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
+            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, 0, TS, false>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
+        __syncwarp();
+        epilogue(0, t0, su, sd);
+        __syncwarp();
+        if (scalar)
+            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, TS, TS, true>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
+        else
+            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, TS, TS, false>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
         __syncwarp();
         if constexpr (Cfg::kF32) {
             // B/C of this stage are no longer read by this warp
@@ -327,47 +392,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
                 if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
             }
         }
-        // warp epilogue: sum the P partials, add D*u, store 4 steps per item
-        const long long t0 = t_begin + (long long)i * TC;
-#pragma unroll
-        for (int k = 0; k < Cfg::IPW; ++k) {
-            const int q = lane + 32 * k;
-            const int r = q / 8, t4 = (q % 8) * 4;
-            const long long dd = dw + r, t = t0 + t4;
-            float v[4];
-            load4_smem(yp + r * RS + t4, v);
-#pragma unroll
-            for (int gg = 1; gg < P; ++gg) {
-                float x[4];
-                load4_smem(yp + r * RS + gg * FROW + t4, x);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] += x[e];
-            }
-            float uv[4];
-            load4_smem(su + r * FROW + t4, uv);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
-            if (dsum_on) {  // steps past the segment hold delta = 0
-                float dv[4];
-                load4_smem(sd + r * FROW + t4, dv);
-                const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dcomp[k];
-                const float tk = dsum[k] + yk;
-                dcomp[k] = (tk - dsum[k]) - yk;
-                dsum[k] = tk;
-            }
-            if (dd < p.dim && t < t_end) {  // t_end is a multiple of 4 on this path
-                T* o = gout + (b * p.dim + dd) * p.L + t;
-                if constexpr (Cfg::kF32) {
-                    *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
-                } else {
-                    const unsigned lo = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[0])) |
-                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[1])) << 16);
-                    const unsigned hi = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[2])) |
-                                        ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[3])) << 16);
-                    *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
-                }
-            }
-        }
+        epilogue(1, t0, su, sd);
         __syncwarp();
         if constexpr (Cfg::kF32) {
             // u/delta of this stage are no longer read by this warp
@@ -387,15 +412,14 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
         return;
     }
 
-    if (dsum_on) {  // the segment's sum of delta per channel: 8 slots in 8 lanes
+    if (dsum_on) {  // the segment's sum of delta per channel: 2 x 4 slots in 4 lanes
 #pragma unroll
-        for (int k = 0; k < Cfg::IPW; ++k) {
-            float v = dsum[k];
+        for (int k = 0; k < Cfg::IPH; ++k) {
+            float v = dsum[0][k] + dsum[1][k];
             v += __shfl_xor_sync(FULL, v, 1);
             v += __shfl_xor_sync(FULL, v, 2);
-            v += __shfl_xor_sync(FULL, v, 4);
-            const long long dd = dw + (lane + 32 * k) / 8;
-            if ((lane & 7) == 0 && dd < p.dim) p.seg_dsum[(b * p.dim + dd) * p.S + s] = v;
+            const long long dd = dw + (lane + 32 * k) / 4;
+            if ((lane & 3) == 0 && dd < p.dim) p.seg_dsum[(b * p.dim + dd) * p.S + s] = v;
         }
     }
 #pragma unroll
