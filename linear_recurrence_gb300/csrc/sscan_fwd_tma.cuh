@@ -108,57 +108,70 @@ struct TmaCfg {
 // Steps [T0, T0 + TS) of a chunk of the recurrence for the calling lane, from
 // fp32 rows in shared memory with row stride FROW: u rows su[r], delta rows
 // sd[r] of the warp's channel rows r = rl[j]; B/C rows of state slot n at
-// sB[n], sC[n].  Per 4-step block: the lane's u/delta vectors, then its
-// states in quads (B/C of 4 states x 4 steps), each element doing
+// sB[n], sC[n].  Per 4-step block: the lane's u/delta vectors and the B/C
+// vectors of its NS states (read one block ahead, so that the shared-memory
+// latency overlaps the previous block's arithmetic), then per element
 // x = delta*A', a = 2^x, h = a*h + (delta*u)*B, y += C*h; the 4 partial
 // outputs of each channel go to yp[rl[j]][g] (row stride RS, lane stride
 // HROW) as one vector.  SCALAR: one decay rate per channel.
-template <int NS, int P, int CPL, int FROW, int RS, int HROW, int T0, int TS, bool SCALAR>
-__device__ __forceinline__ void compute_chunk_tma(const float* su, const float* sd, const float* sB,
-                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
-                                                  const float (&Al2)[CPL][NS], const float (&As)[CPL],
-                                                  float (&h)[CPL][NS]) {
-    constexpr int QS = NS < 4 ? NS : 4;
-    constexpr int NQ = NS / QS;
-    static_assert(NS % QS == 0, "states come in whole quads");
+template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR>
+__device__ __forceinline__ void compute_half_tma(const float* su, const float* sd, const float* sB,
+                                                 const float* sC, float* yp, const int (&rl)[CPL], int g,
+                                                 int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                                 float (&h)[CPL][NS]) {
+    constexpr int NB = TS / 4;
     const float* bB = sB + g * FROW;
     const float* bC = sC + g * FROW;
-#pragma unroll kBlockUnroll
-    for (int t4 = T0; t4 < T0 + TS; t4 += 4) {
-        float dd[CPL][4], du[CPL][4], as[CPL][4], y[CPL][4];
+    float nu[CPL][4], nd[CPL][4], nb[NS][4], nc[NS][4];
+    auto load_block = [&](int t4) {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            float uu[4];
-            load4_smem(su + rl[j] * FROW + t4, uu);
-            load4_smem(sd + rl[j] * FROW + t4, dd[j]);
+            load4_smem(su + rl[j] * FROW + t4, nu[j]);
+            load4_smem(sd + rl[j] * FROW + t4, nd[j]);
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            load4_smem(bB + k * P * FROW + t4, nb[k]);
+            load4_smem(bC + k * P * FROW + t4, nc[k]);
+        }
+    };
+    load_block(T0);
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+        const int t4 = T0 + 4 * blk;
+        float dd[CPL][4], du[CPL][4], as[CPL][4], y[CPL][4], bb[NS][4], cc[NS][4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                du[j][s] = dd[j][s] * uu[s];
+                dd[j][s] = nd[j][s];
+                du[j][s] = nd[j][s] * nu[j][s];
+            }
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                bb[k][s] = nb[k][s];
+                cc[k][s] = nc[k][s];
+            }
+        if (blk + 1 < NB) load_block(t4 + 4);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
                 as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
                 y[j][s] = 0.f;
             }
-        }
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            float bb[QS][4], cc[QS][4];
+        for (int s = 0; s < 4; ++s)
 #pragma unroll
-            for (int kk = 0; kk < QS; ++kk) {
-                const int k = q * QS + kk;
-                load4_smem(bB + k * P * FROW + t4, bb[kk]);
-                load4_smem(bC + k * P * FROW + t4, cc[kk]);
-            }
+            for (int j = 0; j < CPL; ++j)
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-#pragma unroll
-                for (int j = 0; j < CPL; ++j)
-#pragma unroll
-                    for (int kk = 0; kk < QS; ++kk) {
-                        const int k = q * QS + kk;
-                        const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
-                        h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[kk][s]);
-                        y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
-                    }
-        }
+                for (int k = 0; k < NS; ++k) {
+                    const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
+                    h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[k][s]);
+                    y[j][s] = fmaf(cc[k][s], h[j][k], y[j][s]);
+                }
 #pragma unroll
         for (int j = 0; j < CPL; ++j)
             *reinterpret_cast<float4*>(yp + rl[j] * RS + g * HROW + (t4 - T0)) =
@@ -273,9 +286,11 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     // epilogue slots per half chunk: item q = lane + 32k covers channel row
     // q/4, steps 4(q%4)..+3 of the half
     const bool dsum_on = p.mode == MODE_LOCAL;
-    float dsum[2][Cfg::IPH], dcomp[2][Cfg::IPH];  // Kahan sums of delta per slot
+    // Kahan sums of delta per slot (a slot is the same channel row and 4-step
+    // offset in both halves)
+    float dsum[Cfg::IPH], dcomp[Cfg::IPH];
 #pragma unroll
-    for (int k = 0; k < Cfg::IPH; ++k) dsum[0][k] = dcomp[0][k] = dsum[1][k] = dcomp[1][k] = 0.f;
+    for (int k = 0; k < Cfg::IPH; ++k) dsum[k] = dcomp[k] = 0.f;
     float Dr[Cfg::IPH];
 #pragma unroll
     for (int k = 0; k < Cfg::IPH; ++k) {
@@ -309,10 +324,10 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
             if (dsum_on) {  // steps past the segment hold delta = 0
                 float dv[4];
                 load4_smem(sd + r * FROW + t4, dv);
-                const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dcomp[half][k];
-                const float tk = dsum[half][k] + yk;
-                dcomp[half][k] = (tk - dsum[half][k]) - yk;
-                dsum[half][k] = tk;
+                const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dcomp[k];
+                const float tk = dsum[k] + yk;
+                dcomp[k] = (tk - dsum[k]) - yk;
+                dsum[k] = tk;
             }
             if (dd < p.dim && t < t_end) {  // t_end is a multiple of 4 on this path
                 T* o = gout + (b * p.dim + dd) * p.L + t;
@@ -373,27 +388,25 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
         }
         constexpr int TS = Cfg::TS, HROW = Cfg::HROW;
         const long long t0 = t_begin + (long long)i * TC;
-        if (scalar)
-            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, 0, TS, true>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
-        else
-            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, 0, TS, false>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
-        __syncwarp();
-        epilogue(0, t0, su, sd);
-        __syncwarp();
-        if (scalar)
-            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, TS, TS, true>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
-        else
-            compute_chunk_tma<NS, P, CPL, FROW, RS, HROW, TS, TS, false>(su, sd, sB, sC, yp, rl, g, Al2, As, h);
-        __syncwarp();
-        if constexpr (Cfg::kF32) {
-            // B/C of this stage are no longer read by this warp
-            if (lane == 0) {
-                const unsigned old = atomicAdd(bc_count + st, 1u);
-                if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            if (scalar)
+                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true>(su, sd, sB, sC, yp, rl, g, half * TS, Al2,
+                                                                       As, h);
+            else
+                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false>(su, sd, sB, sC, yp, rl, g, half * TS,
+                                                                        Al2, As, h);
+            __syncwarp();
+            if constexpr (Cfg::kF32) {
+                // after the second half, B/C of this stage are no longer read by this warp
+                if (half == 1 && lane == 0) {
+                    const unsigned old = atomicAdd(bc_count + st, 1u);
+                    if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+                }
             }
+            epilogue(half, t0, su, sd);
+            __syncwarp();
         }
-        epilogue(1, t0, su, sd);
-        __syncwarp();
         if constexpr (Cfg::kF32) {
             // u/delta of this stage are no longer read by this warp
             if (lane == 0 && nx < nchunks) issue_u(nx, st);
@@ -412,10 +425,10 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
         return;
     }
 
-    if (dsum_on) {  // the segment's sum of delta per channel: 2 x 4 slots in 4 lanes
+    if (dsum_on) {  // the segment's sum of delta per channel: 4 slots in 4 lanes
 #pragma unroll
         for (int k = 0; k < Cfg::IPH; ++k) {
-            float v = dsum[0][k] + dsum[1][k];
+            float v = dsum[k];
             v += __shfl_xor_sync(FULL, v, 1);
             v += __shfl_xor_sync(FULL, v, 2);
             const long long dd = dw + (lane + 32 * k) / 4;
