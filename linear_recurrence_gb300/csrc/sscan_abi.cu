@@ -227,7 +227,9 @@ int cached_tma_occupancy(Shape sh) {
 // and 26 segments 55, 53, 51 and 58 us; 1536 x 65536: 12 segments 603 us,
 // 19 segments 575 us).  The automatic shape is the one with the most channels per lane
 // whose segments stay at least 16 chunks long ((4,4,2)), else (8,2,2).  The
-// carry correction runs on the cp.async kernel with one channel per lane.
+// carry correction runs on the cp.async kernel, shape (4,4,1) (measured on
+// GB300: dim512 50.3 / 51.2 / 55.3 us with (4,4,1) / (8,2,1) / (2,8,1);
+// long64k 535 / 559 / 568 us).
 int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, int segments, int lanes,
                  FwdPlan* out) {
     if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
@@ -263,7 +265,7 @@ int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, 
         }
     }
     if (!found) return SSCAN_ERR_INVALID;
-    best.corr_sh = Shape{8, 2, 1};
+    best.corr_sh = Shape{4, 4, 1};
     best.corr_tiles_per_batch = ceil_div(dim, shape_channels(best.corr_sh));
     best.corr_tiles = batch * best.corr_tiles_per_batch;
     if (best.corr_tiles * best.S > (1LL << 30)) return SSCAN_ERR_INVALID;

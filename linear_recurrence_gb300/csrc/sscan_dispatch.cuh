@@ -20,7 +20,7 @@ struct Shape {
 // Every compiled shape.  The first group (P <= 4) lives in the *_a units, the
 // second (P >= 8) in the *_b units.
 #ifndef SSCAN_SHAPES_A
-#define SSCAN_SHAPES_A(X) X(1, 4, 1) X(2, 4, 1) X(4, 4, 1) X(4, 16, 2)
+#define SSCAN_SHAPES_A(X) X(1, 4, 1) X(2, 4, 1) X(4, 4, 1) X(4, 16, 2) X(2, 8, 1)
 #endif
 #ifndef SSCAN_SHAPES_B
 #define SSCAN_SHAPES_B(X) X(8, 2, 1) X(8, 2, 2) X(8, 4, 1) X(8, 8, 1) X(16, 4, 1)

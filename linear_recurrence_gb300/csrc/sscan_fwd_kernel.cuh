@@ -463,10 +463,10 @@ __device__ __forceinline__ void compute_chunk(const float* rows, float* yp, cons
 // recurrence h = exp(delta*A) * h from the carried state, with its
 // C-contraction stored as partial outputs exactly as compute_chunk stores
 // them.  A state slot k whose carry has fallen below the lane's threshold in
-// every lane of the warp is frozen: its term is below 2^-24 of the largest
-// carry component and only keeps decaying, so it is skipped (a warp-uniform
-// branch, checked once per 4-step block).  SCALAR: one decay rate per channel
-// (the states decay together; no per-slot check).
+// every lane of the warp at the start of the chunk is frozen for the chunk:
+// its term is below 2^-24 of the largest carry component and only keeps
+// decaying, so it is skipped (a warp-uniform branch).  SCALAR: one decay rate
+// per channel (the states decay together; no per-slot check).
 template <typename T, int NS, int P, int CPL, int OPT, bool SCALAR>
 __device__ __forceinline__ void decay_chunk(const float* rows, float* yp, const int (&rr)[CPL], int g,
                                             const float (&Al2)[CPL][NS], const float (&As)[CPL],
@@ -476,20 +476,20 @@ __device__ __forceinline__ void decay_chunk(const float* rows, float* yp, const 
     constexpr unsigned FULL = 0xffffffffu;
     const float* sd = rows + DT * FROW;
     const float* sC = rows + (2 * DT + NSP + g) * FROW;
+    bool live[NS];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        if (SCALAR) {  // one rate: the states decay together
+            live[k] = true;
+            continue;
+        }
+        bool l = false;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) l |= fabsf(h[j][k]) > thr[j];
+        live[k] = __any_sync(FULL, l);
+    }
 #pragma unroll kBlockUnroll
     for (int t4 = 0; t4 < TC; t4 += 4) {
-        bool live[NS];
-#pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            if (SCALAR) {  // one rate: the states decay together
-                live[k] = true;
-                continue;
-            }
-            bool l = false;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) l |= fabsf(h[j][k]) > thr[j];
-            live[k] = __any_sync(FULL, l);
-        }
         float dd[CPL][4], as[CPL][4], y[CPL][4];
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {

@@ -97,7 +97,7 @@ def test_workload_small_time_split(lr, name, kw, segments):
 
 # (lanes P, dstate N) -> the compiled shape (P, states per lane, channels per
 # lane) the plan must use; together these cover every compiled shape
-LANE_CASES = [(1, 4, (1, 4, 1)), (2, 7, (2, 4, 1)), (4, 13, (4, 4, 1)), (4, 40, (4, 16, 2)),
+LANE_CASES = [(1, 4, (1, 4, 1)), (2, 7, (2, 4, 1)), (2, 13, (2, 8, 1)), (4, 13, (4, 4, 1)), (4, 40, (4, 16, 2)),
               (8, 16, (8, 2, 1)), (8, 25, (8, 4, 1)), (8, 50, (8, 8, 1)), (16, 61, (16, 4, 1))]
 
 
