@@ -204,20 +204,20 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
 }
 
 // Resident CTAs per SM of a TMA-kernel shape, queried once per device.
-int cached_tma_occupancy(Shape sh) {
-    static std::atomic<int> cache[64][2] = {};  // (8,2,2), (4,4,2)
+int cached_tma_occupancy(bool f32, Shape sh) {
+    static std::atomic<int> cache[64][2][2] = {};  // device, dtype, (8,2,2) / (4,4,2)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::atomic<int>& c = cache[dev & 63][sh.P == 4 ? 1 : 0];
+    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1][sh.P == 4 ? 1 : 0];
     int v = c.load(std::memory_order_relaxed);
     if (v == 0) {
-        v = fwd_tma_occupancy(true, sh);
+        v = fwd_tma_occupancy(f32, sh);
         c.store(v, std::memory_order_relaxed);
     }
     return v;
 }
 
-// Plan of the fp32 TMA-fed kernel for 8 < N <= 16 (its shapes hold 16 state
+// Plan of the TMA-fed kernel for 8 < N <= 16 (its shapes hold 16 state
 // slots), or SSCAN_ERR_INVALID when it does not apply.  A time split fills at
 // most one wave of the GPU's resident CTA slots and keeps segments of about
 // 14 chunks or more: every segment beyond the first adds a carry correction over the
@@ -225,32 +225,51 @@ int cached_tma_occupancy(Shape sh) {
 // shorter segments cost more in corrections than they gain in local-pass
 // parallelism (measured on GB300 with 512 channels x 8192 steps: 16, 18, 19
 // and 26 segments 55, 53, 51 and 58 us; 1536 x 65536: 12 segments 603 us,
-// 19 segments 575 us).  The automatic shape is the one with the most channels per lane
-// whose segments stay at least 16 chunks long ((4,4,2)), else (8,2,2).  The
+// 19 segments 575 us).  A problem wide enough to give (4,4,2), else (8,2,2),
+// 6 warps per SM runs unsplit on that shape (8192 fp32 channels x 2048 steps:
+// (8,2,2) unsplit 123 us, (4,4,2) in 2 or 3 segments 130 / 148 us; 16384
+// channels: (4,4,2) unsplit 187 us, (8,2,2) 207 us).
+// Otherwise the shape is the one with the most channels per lane whose
+// segments stay at least 16 chunks long ((4,4,2)), else (8,2,2).  The
 // carry correction runs on the cp.async kernel, shape (4,4,1) (measured on
 // GB300: dim512 50.3 / 51.2 / 55.3 us with (4,4,1) / (8,2,1) / (2,8,1);
 // long64k 535 / 559 / 568 us).
-int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, int segments, int lanes,
-                 FwdPlan* out) {
+int plan_fwd_tma(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
+                 int lanes, FwdPlan* out) {
     if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
     const int nsm = std::max(sm_count(), 1);
     const long long TC = kChunkSteps;
     const Shape cands[] = {{4, 4, 2}, {8, 2, 2}};
     const long long min_chunks[] = {16, 0};
+    // warps per SM that an unsplit launch must give to be taken as it is
+    const long long min_warps[] = {6, 6};
+    // without a pinned plan, the first candidate whose unsplit grid is wide
+    // enough runs unsplit (a split adds carry corrections whose horizon grows
+    // with slow decays)
+    int unsplit = -1;
+    if (segments == 0)
+        for (int i = 0; i < 2 && unsplit < 0; ++i) {
+            const Shape sh = cands[i];
+            if (lanes != 0 && lanes != sh.P) continue;
+            if (batch * ceil_div(dim, tma_channels(sh)) * 4 >= min_warps[i] * nsm) unsplit = i;
+        }
     FwdPlan best{};
     bool found = false;
     for (int i = 0; i < 2 && !found; ++i) {
         const Shape sh = cands[i];
         if (!tma_has_shape(sh) || (lanes != 0 && lanes != sh.P)) continue;
+        if (unsplit >= 0 && i != unsplit) continue;
         FwdPlan pl{};
         pl.sh = sh;
         pl.tma = true;
         pl.tiles_per_batch = ceil_div(dim, tma_channels(sh));
         pl.tiles = batch * pl.tiles_per_batch;
         if (pl.tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
-        const long long slots = (long long)nsm * std::max(cached_tma_occupancy(sh), 1);
+        const long long slots = (long long)nsm * std::max(cached_tma_occupancy(f32, sh), 1);
         long long S = segments;
-        if (S == 0) {
+        if (S == 0 && unsplit >= 0) {
+            S = 1;
+        } else if (S == 0) {
             S = pl.tiles >= slots ? 1 : slots / pl.tiles;
             S = std::min(S, std::max(1LL, seqlen / (kMinTmaSegmentChunks * TC)));
         }
@@ -353,15 +372,13 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     const int vece = 16 / esz;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
                      aligned16(C) && aligned16(out) && (z == nullptr || aligned16(z));
-    // the TMA-fed kernel takes the plain fp32 scan's single or local pass when
-    // the tensor-map rules hold (16-byte aligned rows, coordinates below 2^31);
-    // bf16 stays with the cp.async kernel, whose CTA widens B/C once for all
-    // its warps (the TMA kernel's per-warp widening measured slower)
+    // the TMA-fed kernel takes the plain scan's single or local pass when the
+    // tensor-map rules hold (16-byte aligned rows, coordinates below 2^31)
     const bool plain = z == nullptr && delta_bias == nullptr && flags == 0;
     const long long lim = (1LL << 31) - 256;
     sscan::FwdPlan pl;
-    bool use_tma = f32 && vec && plain && seqlen < lim && dim < lim && batch < lim &&
-                   sscan::plan_fwd_tma(batch, dim, seqlen, dstate, segments, lanes, &pl) == SSCAN_OK;
+    bool use_tma = vec && plain && seqlen < lim && dim < lim && batch < lim &&
+                   sscan::plan_fwd_tma(f32, batch, dim, seqlen, dstate, segments, lanes, &pl) == SSCAN_OK;
     if (!use_tma) {
         const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
         if (prc != SSCAN_OK) return prc;

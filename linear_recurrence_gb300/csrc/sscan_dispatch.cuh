@@ -79,8 +79,8 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 }
 
 // Shapes of the TMA-fed kernel (sscan_fwd_tma.cuh): four warps per CTA, so
-// DT = 4 * (32 / P) * CPL channels per CTA.  It serves the plain fp32 scan
-// with 16-byte aligned rows in the single-segment and local-segment modes, for
+// DT = 4 * (32 / P) * CPL channels per CTA.  It serves the plain scan with
+// 16-byte aligned rows in the single-segment and local-segment modes, for
 // 8 < N <= 16 (measured on GB300: as fast or faster than the cp.async kernel
 // there; slower for wide states, whose B/C ring costs occupancy).
 #ifndef SSCAN_TMA_SHAPES
@@ -116,10 +116,10 @@ struct FwdPlan {
 // Returns SSCAN_OK, SSCAN_ERR_INVALID or SSCAN_ERR_CUDA.
 int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
              int lanes, long long max_segments, FwdPlan* out);
-// The plan of the fp32 TMA-fed kernel (plain scan, aligned rows, 8 < N <= 16;
+// The plan of the TMA-fed kernel (plain scan, aligned rows, 8 < N <= 16;
 // lanes 0, 4 or 8), or SSCAN_ERR_INVALID when it does not apply.
-int plan_fwd_tma(long long batch, long long dim, long long seqlen, long long N, int segments, int lanes,
-                 FwdPlan* out);
+int plan_fwd_tma(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
+                 int lanes, FwdPlan* out);
 
 // Shared implementation, included by the per-unit translation units only.
 #ifdef SSCAN_DISPATCH_IMPL

@@ -21,8 +21,13 @@
 //     has not landed.  A refill only overwrites values already read, so the
 //     count needs no fence; the data itself is published by the mbarrier's
 //     transaction count and acquired by its wait;
-//   * bf16 rows are widened by each warp into its own fp32 rows (its u/delta
-//     and a private copy of B/C), which frees the raw stage at once.
+//   * bf16: each warp widens its own u/delta rows into fp32 rows, which
+//     frees its raw stage at once; the chunk's B/C rows are widened once per
+//     CTA, by warps in turn (chunk c by warp c mod 4, one chunk ahead), into
+//     a three-slot fp32 ring with a full mbarrier (the widening warp's lanes
+//     arrive) and an empty one (every warp arrives when it is done with the
+//     slot); only the widening warp reads the raw B/C stage, so it refills
+//     that stage itself.
 // Boxes are TC + 16 bytes wide: the extra columns (the next chunk's first
 // steps, or zeros past the end) pad every shared-memory row exactly as the
 // cp.async ring does, so the reads of different rows at one step fall in
@@ -83,15 +88,21 @@ struct TmaCfg {
     static constexpr int TS = TC / 2;
     static constexpr int HROW = TS + 4;
     static constexpr int RS = align_up(P * HROW - 16, 32) + 16;
-    // bf16: a warp's fp32 rows [u CPW][delta CPW][B NSP][C NSP]
-    static constexpr int WORK_ROWS = 2 * CPW + 2 * NSP;
+    // bf16: a warp's widened fp32 rows [u CPW][delta CPW]; the chunk's B/C rows
+    // are widened once per CTA into a ring of WB slots [B NSP][C NSP]
+    static constexpr int WORK_ROWS = 2 * CPW;
+    static constexpr int WB = 3;
+    static constexpr int BCW_BYTES = kF32 ? 0 : 2 * NSP * FROW * 4;
     // items of the warp epilogue per half chunk: (channel row, 4 steps); per lane
     static constexpr int IPH = CPW * (TS / 4) / 32;
     // shared-memory map (bytes from a 128-byte aligned base)
-    static constexpr int OFF_BAR = 0;  // mbarriers [kWarps + 1][STAGES], counters [STAGES]
+    // mbarriers [kWarps + 1][STAGES], counters [STAGES], then (bf16) the
+    // widened ring's full [WB] and empty [WB] mbarriers
+    static constexpr int OFF_BAR = 0;
     static constexpr int OFF_U = 1024;  // [STAGES][kWarps][u, delta] slots
     static constexpr int OFF_BC = OFF_U + STAGES * kWarps * 2 * U_SLOT;  // [STAGES][B, C] slots
-    static constexpr int OFF_WORK = OFF_BC + STAGES * 2 * BC_SLOT;
+    static constexpr int OFF_BCW = OFF_BC + STAGES * 2 * BC_SLOT;
+    static constexpr int OFF_WORK = OFF_BCW + WB * BCW_BYTES;
     static constexpr int WORK_BYTES = kF32 ? 0 : WORK_ROWS * FROW * 4;  // per warp
     static constexpr int OFF_YP = OFF_WORK + kWarps * WORK_BYTES;
     static constexpr int YP_BYTES = CPW * RS * 4;  // per warp
@@ -99,7 +110,8 @@ struct TmaCfg {
     static_assert(TC == 32, "epilogue items assume 8 four-step blocks per chunk");
     static_assert(CPW % 8 == 0, "a warp's epilogue items must fill its lanes");
     static_assert(RS >= P * HROW && (RS / 4) % 8 == 4, "partial row stride");
-    static_assert((kWarps + 1) * STAGES * 8 + STAGES * 4 <= 1024, "barrier area");
+    static constexpr int OFF_BCW_BAR = align_up((kWarps + 1) * STAGES * 8 + STAGES * 4, 8);
+    static_assert(OFF_BCW_BAR + 2 * WB * 8 <= 1024, "barrier area");
     static_assert(RROW * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
     static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256, "tensor-map box limits");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -225,9 +237,17 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     };
     auto bc_slot = [&](int st) -> T* { return reinterpret_cast<T*>(bc_ring + st * 2 * Cfg::BC_SLOT); };
 
+    uint64_t* bcw_full = reinterpret_cast<uint64_t*>(sbase + Cfg::OFF_BAR + Cfg::OFF_BCW_BAR);  // [WB]
+    uint64_t* bcw_empty = bcw_full + Cfg::WB;                                                      // [WB]
     if (tid == 0) {
         for (int i = 0; i < (kWarps + 1) * STAGES; ++i) mbar_init(barU + i, 1);
         for (int i = 0; i < STAGES; ++i) bc_count[i] = 0;
+        if constexpr (!Cfg::kF32) {
+            for (int i = 0; i < Cfg::WB; ++i) {
+                mbar_init(bcw_full + i, 32);
+                mbar_init(bcw_empty + i, kWarps);
+            }
+        }
         mbar_fence_init();
     }
     __syncthreads();
@@ -344,47 +364,68 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
         }
     };
 
+    // bf16: widen the B/C rows of chunk c into slot c % WB of the shared fp32
+    // ring (the calling warp is chunk c's widener), then refill the raw stage
+    auto widen_bc = [&](int c) -> bool {
+        const int st = c % STAGES, ws = c % Cfg::WB;
+        bool good = mbar_wait_bounded(barBC + st, (unsigned)(c / STAGES) & 1u);
+        if (c >= Cfg::WB) good = mbar_wait_bounded(bcw_empty + ws, (unsigned)((c - Cfg::WB) / Cfg::WB) & 1u) && good;
+        good = __all_sync(FULL, good);
+        if (!good) return false;
+        float* dst = reinterpret_cast<float*>(sbase + Cfg::OFF_BCW + ws * Cfg::BCW_BYTES);
+        const bf16* rb = reinterpret_cast<const bf16*>(bc_slot(st));
+        widen_rows_warp<RROW, FROW, TC>(rb, dst, NSP, lane);
+        widen_rows_warp<RROW, FROW, TC>(
+            reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(rb) + Cfg::BC_SLOT),
+            dst + NSP * FROW, NSP, lane);
+        mbar_arrive(bcw_full + ws);
+        __syncwarp();
+        if (lane == 0 && c + STAGES < nchunks) issue_bc(c + STAGES, st);
+        return true;
+    };
+
     int i = 0;
     bool ok = true;
-    for (; i < nchunks; ++i) {
+    if constexpr (!Cfg::kF32) {
+        if (w == 0 && nchunks > 0) ok = widen_bc(0);
+        ok = __all_sync(FULL, ok);
+    }
+    for (; ok && i < nchunks; ++i) {
         const int st = i % STAGES;
         const unsigned par = (unsigned)(i / STAGES) & 1u;
-        ok = mbar_wait_bounded(barU + w * STAGES + st, par);
-        ok = mbar_wait_bounded(barBC + st, par) && ok;
-        ok = __all_sync(FULL, ok);
-        if (!ok) break;
         const int nx = i + STAGES;  // the chunk that refills this stage
         const float *su, *sd, *sB, *sC;
         if constexpr (Cfg::kF32) {
+            ok = mbar_wait_bounded(barU + w * STAGES + st, par);
+            ok = mbar_wait_bounded(barBC + st, par) && ok;
+            ok = __all_sync(FULL, ok);
+            if (!ok) break;
             su = reinterpret_cast<const float*>(u_slot(st));
             sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
             sB = reinterpret_cast<const float*>(bc_slot(st));
             sC = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(sB) + Cfg::BC_SLOT);
         } else {
-            // widen the warp's u/delta rows and the chunk's B/C rows into its
-            // own fp32 rows, then hand both raw stages back
+            // the next chunk's B/C when it is this warp's turn, one chunk ahead
+            if (i + 1 < nchunks && (i + 1) % kWarps == w && !widen_bc(i + 1)) {
+                ok = false;
+                break;
+            }
+            // the warp's own u/delta rows, widened, then the raw stage refilled
+            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par));
+            if (!ok) break;
             const bf16* ru = reinterpret_cast<const bf16*>(u_slot(st));
             widen_rows_warp<RROW, FROW, TC>(ru, work, CPW, lane);
             widen_rows_warp<RROW, FROW, TC>(
                 reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(ru) + Cfg::U_SLOT),
                 work + CPW * FROW, CPW, lane);
-            const bf16* rb = reinterpret_cast<const bf16*>(bc_slot(st));
-            widen_rows_warp<RROW, FROW, TC>(rb, work + 2 * CPW * FROW, NSP, lane);
-            widen_rows_warp<RROW, FROW, TC>(
-                reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(rb) + Cfg::BC_SLOT),
-                work + (2 * CPW + NSP) * FROW, NSP, lane);
+            __syncwarp();
+            if (lane == 0 && nx < nchunks) issue_u(nx, st);
+            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u));
+            if (!ok) break;
             su = work;
             sd = work + CPW * FROW;
-            sB = work + 2 * CPW * FROW;
-            sC = work + (2 * CPW + NSP) * FROW;
-        }
-        if constexpr (!Cfg::kF32) {
-            __syncwarp();
-            if (lane == 0) {
-                if (nx < nchunks) issue_u(nx, st);
-                const unsigned old = atomicAdd(bc_count + st, 1u);
-                if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
-            }
+            sB = reinterpret_cast<const float*>(sbase + Cfg::OFF_BCW + (i % Cfg::WB) * Cfg::BCW_BYTES);
+            sC = sB + NSP * FROW;
         }
         constexpr int TS = Cfg::TS, HROW = Cfg::HROW;
         const long long t0 = t_begin + (long long)i * TC;
@@ -397,11 +438,13 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
                 compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false>(su, sd, sB, sC, yp, rl, g, half * TS,
                                                                         Al2, As, h);
             __syncwarp();
-            if constexpr (Cfg::kF32) {
-                // after the second half, B/C of this stage are no longer read by this warp
-                if (half == 1 && lane == 0) {
+            // after the second half, B/C of this chunk are no longer read by this warp
+            if (half == 1 && lane == 0) {
+                if constexpr (Cfg::kF32) {
                     const unsigned old = atomicAdd(bc_count + st, 1u);
                     if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+                } else {
+                    mbar_arrive(bcw_empty + i % Cfg::WB);
                 }
             }
             epilogue(half, t0, su, sd);

@@ -124,7 +124,7 @@ def test_lane_shapes(lr, lanes, N, shape, dtype):
     assert tag in lr.last_plan() and "S=3" in lr.last_plan(), lr.last_plan()
 
 
-# the TMA-fed kernel (fp32, plain scan, 16-byte aligned rows, 8 < N <= 16):
+# the TMA-fed kernel (plain scan, 16-byte aligned rows, 8 < N <= 16):
 # (batch, dim, L, N, lanes, segments, use_D, use_h0)
 TMA_CASES = [
     (3, 70, 1004, 16, 8, 0, True, True),    # ragged channel tile, 12-step tail chunk
@@ -137,10 +137,14 @@ TMA_CASES = [
 
 
 @pytest.mark.parametrize("case", TMA_CASES, ids=lambda c: "x".join(map(str, c[:4])))
-def test_tma_path(lr, case):
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tma_path(lr, case, dtype):
     batch, dim, L, N, lanes, segments, use_D, use_h0 = case
+    if dtype == "bf16" and L % 8:
+        L += 8 - L % 8  # bf16 rows are 16-byte aligned when L is a multiple of 8
     w = workloads.WORKLOADS["long64k"].scaled(batch=batch, dim=dim, L=L, N=N)
-    plan = _compare(lr, w, workloads.make_inputs(w), TOL["f32"], lanes=lanes, segments=segments,
+    w = workloads.Workload(**{**w.__dict__, "dtype": dtype})
+    plan = _compare(lr, w, workloads.make_inputs(w), TOL[dtype], lanes=lanes, segments=segments,
                     use_D=use_D, use_h0=use_h0)
     assert " tma " in plan, plan
     if segments:
