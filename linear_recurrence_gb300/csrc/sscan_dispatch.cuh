@@ -126,20 +126,22 @@ int plan_fwd_tma(bool f32, long long batch, long long dim, long long seqlen, lon
 template <typename T, int NS, int P, int CPL, int OPT>
 static cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
-    auto kern = sscan_fwd_chunked<T, NS, P, CPL, OPT>;
+    const bool corr = p.mode == MODE_CORR;
+    auto kern = corr ? sscan_fwd_chunked<T, NS, P, CPL, OPT, true> : sscan_fwd_chunked<T, NS, P, CPL, OPT, false>;
     // the state slots of a shape must cover every state: the kernel stages
     // B/C rows n < N into NSP slots
     if (p.N < 1 || p.N > (long long)Cfg::NSP) return cudaErrorInvalidValue;
-    // opting in to more than 48 KB of dynamic shared memory is per device
-    static unsigned long long configured = 0;  // bit per device ordinal (< 64)
+    // opting in to more than 48 KB of dynamic shared memory is per device and
+    // kernel (one bit per device and kernel)
+    static unsigned long long configured[2] = {0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+    if (!(__atomic_load_n(&configured[corr ? 1 : 0], __ATOMIC_ACQUIRE) & bit)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+        __atomic_fetch_or(&configured[corr ? 1 : 0], bit, __ATOMIC_ACQ_REL);
     }
     kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
@@ -148,7 +150,7 @@ static cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t str
 template <typename T, int NS, int P, int CPL, int OPT>
 static int occupancy_variant() {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
-    auto kern = sscan_fwd_chunked<T, NS, P, CPL, OPT>;
+    auto kern = sscan_fwd_chunked<T, NS, P, CPL, OPT, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
         cudaSuccess)
         return 0;

@@ -597,7 +597,10 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
     }
 }
 
-template <typename T, int NS, int P, int CPL, int OPT>
+// CORR: the carry-correction instantiation (MODE_CORR launches); the single
+// and local passes use the other, so that neither path's code shapes the
+// other's register allocation and schedule.
+template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
 __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fwd_chunked(const FwdParams p) {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, NSP = Cfg::NSP, STAGES = Cfg::STAGES;
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane % P, gi = lane / P;
     const bool vec = p.vec != 0;
-    const bool corr = p.mode == MODE_CORR;
+    constexpr bool corr = CORR;
     const bool dsum_on = p.mode == MODE_LOCAL;
     // the correction stages the local outputs in the u rows: it reads them
     // through q.u and adds the carry's contribution to them
