@@ -54,6 +54,17 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" :: "n"(N) : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------
+
+// Let the next kernel on the stream, when launched as a programmatic
+// dependent, start its CTAs (they run up to their griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory
+// is visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // ---- TMA bulk copies completed on an mbarrier (sm_90 and later) ----------
 
 __device__ __forceinline__ unsigned smem_addr(const void* p) {

@@ -143,8 +143,25 @@ static cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t str
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured[corr ? 1 : 0], bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    if (!corr) {
+        kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // the correction follows the local pass on the same stream as a
+    // programmatic dependent: its CTAs may be resident before the pass ends
+    // and wait (griddepcontrol.wait) for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, int NS, int P, int CPL, int OPT>

@@ -628,6 +628,12 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
     const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + TC - 1) / TC) : 0;
     const int N = (int)p.N;
 
+    // a correction launched as a programmatic dependent of the local pass
+    // waits here for that pass's outputs and aggregates; a local pass lets the
+    // correction's CTAs start early
+    if constexpr (CORR) griddep_wait();
+    else griddep_launch_dependents();
+
     // the lane's channels and their decay rates (A * log2 e); a warp whose
     // channels each have a single rate takes the one-exponent-per-step path
     int rr[CPL];

@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
 
     uint64_t* bcw_full = reinterpret_cast<uint64_t*>(sbase + Cfg::OFF_BAR + Cfg::OFF_BCW_BAR);  // [WB]
     uint64_t* bcw_empty = bcw_full + Cfg::WB;                                                      // [WB]
+    // the carry correction that follows a local pass may start its CTAs now;
+    // it waits for this grid's completion before reading anything it wrote
+    griddep_launch_dependents();
     if (tid == 0) {
         for (int i = 0; i < (kWarps + 1) * STAGES; ++i) mbar_init(barU + i, 1);
         for (int i = 0; i < STAGES; ++i) bc_count[i] = 0;
