@@ -77,6 +77,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
 __device__ __forceinline__ void mbar_fence_init() {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
+// order this thread's earlier shared-memory writes before later bulk copies
+// into the same memory (the async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
 // one arrival (release semantics: the caller's earlier shared-memory writes
 // are visible to the threads that observe the phase complete)
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {

@@ -208,14 +208,14 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
 }
 
 // Resident CTAs per SM of a TMA-kernel shape, queried once per device.
-int cached_tma_occupancy(bool f32, Shape sh) {
-    static std::atomic<int> cache[64][2][2] = {};  // device, dtype, (8,2,2) / (4,4,2)
+int cached_tma_occupancy(bool f32, Shape sh, int variant) {
+    static std::atomic<int> cache[64][2][2][3] = {};  // device, dtype, (8,2,2) / (4,4,2), variant
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1][sh.P == 4 ? 1 : 0];
+    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1][sh.P == 4 ? 1 : 0][variant % 3];
     int v = c.load(std::memory_order_relaxed);
     if (v == 0) {
-        v = fwd_tma_occupancy(f32, sh);
+        v = fwd_tma_occupancy(f32, sh, variant);
         c.store(v, std::memory_order_relaxed);
     }
     return v;
@@ -238,8 +238,8 @@ int cached_tma_occupancy(bool f32, Shape sh) {
 // carry correction runs on the cp.async kernel, shape (4,4,1) (measured on
 // GB300: dim512 50.3 / 51.2 / 55.3 us with (4,4,1) / (8,2,1) / (2,8,1);
 // long64k 535 / 559 / 568 us).
-int plan_fwd_tma(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
-                 int lanes, FwdPlan* out) {
+int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long long seqlen, long long N,
+                 int segments, int lanes, FwdPlan* out) {
     if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
     const int nsm = std::max(sm_count(), 1);
     const long long TC = kChunkSteps;
@@ -269,7 +269,7 @@ int plan_fwd_tma(bool f32, long long batch, long long dim, long long seqlen, lon
         pl.tiles_per_batch = ceil_div(dim, tma_channels(sh));
         pl.tiles = batch * pl.tiles_per_batch;
         if (pl.tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
-        const long long slots = (long long)nsm * std::max(cached_tma_occupancy(f32, sh), 1);
+        const long long slots = (long long)nsm * std::max(cached_tma_occupancy(f32, sh, variant), 1);
         long long S = segments;
         if (S == 0 && unsplit >= 0) {
             S = 1;
@@ -376,13 +376,13 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     const int vece = 16 / esz;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
                      aligned16(C) && aligned16(out) && (z == nullptr || aligned16(z));
-    // the TMA-fed kernel takes the plain scan's single or local pass when the
-    // tensor-map rules hold (16-byte aligned rows, coordinates below 2^31)
-    const bool plain = z == nullptr && delta_bias == nullptr && flags == 0;
+    // the TMA-fed kernel takes the single or local pass when the tensor-map
+    // rules hold (16-byte aligned rows, coordinates below 2^31)
+    const int variant = (flags & SSCAN_ZOH) ? 2 : (z != nullptr || delta_bias != nullptr || flags != 0) ? 1 : 0;
     const long long lim = (1LL << 31) - 256;
     sscan::FwdPlan pl;
-    bool use_tma = vec && plain && seqlen < lim && dim < lim && batch < lim &&
-                   sscan::plan_fwd_tma(f32, batch, dim, seqlen, dstate, segments, lanes, &pl) == SSCAN_OK;
+    bool use_tma = vec && seqlen < lim && dim < lim && batch < lim &&
+                   sscan::plan_fwd_tma(f32, variant, batch, dim, seqlen, dstate, segments, lanes, &pl) == SSCAN_OK;
     if (!use_tma) {
         const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
         if (prc != SSCAN_OK) return prc;

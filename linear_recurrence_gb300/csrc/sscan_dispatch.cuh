@@ -79,8 +79,9 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 }
 
 // Shapes of the TMA-fed kernel (sscan_fwd_tma.cuh): four warps per CTA, so
-// DT = 4 * (32 / P) * CPL channels per CTA.  It serves the plain scan with
-// 16-byte aligned rows in the single-segment and local-segment modes, for
+// DT = 4 * (32 / P) * CPL channels per CTA.  It serves the scan (plain or
+// with the options) with 16-byte aligned rows in the single-segment and
+// local-segment modes, for
 // 8 < N <= 16 (measured on GB300: as fast or faster than the cp.async kernel
 // there; slower for wide states, whose B/C ring costs occupancy).
 #ifndef SSCAN_TMA_SHAPES
@@ -89,11 +90,18 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 inline int tma_channels(Shape sh) { return 4 * (32 / sh.P) * sh.CPL; }
 bool tma_has_shape(Shape sh);
 cudaError_t fwd_tma_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-int fwd_tma_occupancy(bool f32, Shape sh);
-cudaError_t fwd_tma_launch_f32(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-cudaError_t fwd_tma_launch_bf16(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
-int fwd_tma_occupancy_f32(Shape sh);
-int fwd_tma_occupancy_bf16(Shape sh);
+// resident CTAs per SM of a shape and variant (0 plain, 1 options, 2 zero-order hold)
+int fwd_tma_occupancy(bool f32, Shape sh, int variant);
+#define SSCAN_DECLARE_TMA_UNIT(SUFFIX)                                                                \
+    cudaError_t fwd_tma_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t stream); \
+    int fwd_tma_occupancy_##SUFFIX(Shape sh);
+SSCAN_DECLARE_TMA_UNIT(f32_e)
+SSCAN_DECLARE_TMA_UNIT(f32_o)
+SSCAN_DECLARE_TMA_UNIT(f32_z)
+SSCAN_DECLARE_TMA_UNIT(bf16_e)
+SSCAN_DECLARE_TMA_UNIT(bf16_o)
+SSCAN_DECLARE_TMA_UNIT(bf16_z)
+#undef SSCAN_DECLARE_TMA_UNIT
 // Encode a 3-D tensor map {L, rows, batch} of a contiguous [batch, rows, L]
 // fp32 or bf16 array with box {box_l, box_rows, 1} (false on failure).
 bool tma_encode_3d(CUtensorMap* map, const void* base, bool f32, long long L, long long rows, long long batch,
@@ -116,10 +124,10 @@ struct FwdPlan {
 // Returns SSCAN_OK, SSCAN_ERR_INVALID or SSCAN_ERR_CUDA.
 int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
              int lanes, long long max_segments, FwdPlan* out);
-// The plan of the TMA-fed kernel (plain scan, aligned rows, 8 < N <= 16;
-// lanes 0, 4 or 8), or SSCAN_ERR_INVALID when it does not apply.
-int plan_fwd_tma(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
-                 int lanes, FwdPlan* out);
+// The plan of the TMA-fed kernel (aligned rows, 8 < N <= 16; lanes 0, 4 or
+// 8; variant as fwd_variant), or SSCAN_ERR_INVALID when it does not apply.
+int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long long seqlen, long long N,
+                 int segments, int lanes, FwdPlan* out);
 
 // Shared implementation, included by the per-unit translation units only.
 #ifdef SSCAN_DISPATCH_IMPL

@@ -78,13 +78,15 @@ struct FwdParams {
 // e = e^x, log1p(e) is taken from its Maclaurin series e - e^2/2 + e^3/3 where
 // e < 1/64 (truncation below 2^-26 relative), else as ln2 * log2(1 + e), whose
 // absolute error (2^-22) is then below 1e-5 of the result; x > 20 gives x.
+// Both branches are computed and the result selected, so that lanes with
+// different arguments do not diverge.
 __device__ __forceinline__ float softplus_f(float x) {
-    if (x > 20.f) return x;
     const float e = ex2(x * 1.4426950408889634f);
-    if (e < 0.015625f) return e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
+    const float series = e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
     float l;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + e));
-    return l * 0.69314718055994531f;
+    const float r = e < 0.015625f ? series : l * 0.69314718055994531f;
+    return x > 20.f ? x : r;
 }
 
 // delta as the scan uses it: delta + bias, then softplus when asked for
@@ -98,11 +100,13 @@ __device__ __forceinline__ float delta_in(float x, float bias, bool softplus) {
 // |delta*A| < 1/16 the difference a - 1 would cancel, so there the series
 // delta*(1 + x/2 + x^2/6 + x^3/24), x = delta*A, is used (truncation below
 // 2e-7 relative); A = 0 gives delta, the Euler value.
+// Both forms are computed and one selected (no divergent branch in the
+// element loop).
 __device__ __forceinline__ float zoh_coef(float dt, float y, float a, float invA) {
     const float x = y * 0.69314718055994531f;
-    if (fabsf(x) < 0.0625f)
-        return dt * fmaf(x, fmaf(x, fmaf(x, 1.f / 24.f, 1.f / 6.f), 0.5f), 1.f);
-    return (a - 1.f) * invA;
+    const float series = dt * fmaf(x, fmaf(x, fmaf(x, 1.f / 24.f, 1.f / 6.f), 0.5f), 1.f);
+    const float direct = (a - 1.f) * invA;
+    return fabsf(x) < 0.0625f ? series : direct;
 }
 
 // silu(z) = z * sigmoid(z), the output gate

@@ -62,12 +62,20 @@ bool tma_has_shape(Shape sh) {
 }
 
 cudaError_t fwd_tma_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream) {
-    if (p.mode == MODE_CORR || !p.vec || fwd_variant(p) != 0) return cudaErrorInvalidValue;
-    return f32 ? fwd_tma_launch_f32(p, sh, grid, stream) : fwd_tma_launch_bf16(p, sh, grid, stream);
+    if (p.mode == MODE_CORR || !p.vec) return cudaErrorInvalidValue;
+    switch (fwd_variant(p)) {
+        case 2: return f32 ? fwd_tma_launch_f32_z(p, sh, grid, stream) : fwd_tma_launch_bf16_z(p, sh, grid, stream);
+        case 1: return f32 ? fwd_tma_launch_f32_o(p, sh, grid, stream) : fwd_tma_launch_bf16_o(p, sh, grid, stream);
+        default: return f32 ? fwd_tma_launch_f32_e(p, sh, grid, stream) : fwd_tma_launch_bf16_e(p, sh, grid, stream);
+    }
 }
 
-int fwd_tma_occupancy(bool f32, Shape sh) {
-    return f32 ? fwd_tma_occupancy_f32(sh) : fwd_tma_occupancy_bf16(sh);
+int fwd_tma_occupancy(bool f32, Shape sh, int variant) {
+    switch (variant) {
+        case 2: return f32 ? fwd_tma_occupancy_f32_z(sh) : fwd_tma_occupancy_bf16_z(sh);
+        case 1: return f32 ? fwd_tma_occupancy_f32_o(sh) : fwd_tma_occupancy_bf16_o(sh);
+        default: return f32 ? fwd_tma_occupancy_f32_e(sh) : fwd_tma_occupancy_bf16_e(sh);
+    }
 }
 
 }  // namespace sscan

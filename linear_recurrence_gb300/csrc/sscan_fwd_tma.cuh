@@ -45,13 +45,15 @@
 namespace sscan {
 
 // Tensor maps of one launch, 3-D with the innermost dimension first:
-// u and delta {L, dim, batch} with box {RROW, CPW, 1}; B and C {L, N, batch}
-// with box {RROW, NSP, 1}.  The box height past dim (or N) reads zeros.
+// u, delta (and z) {L, dim, batch} with box {RROW, CPW, 1}; B and C
+// {L, N, batch} with box {RROW, NSP, 1}.  The box height past dim (or N)
+// reads zeros.
 struct TmaMaps {
     CUtensorMap u;
     CUtensorMap delta;
     CUtensorMap B;
     CUtensorMap C;
+    CUtensorMap z;  // the output gate (options variant with a gate only)
 };
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -64,9 +66,11 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 #endif
 constexpr int kTmaStages = SSCAN_TMA_STAGES;
 
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT_ = 0>
 struct TmaCfg {
     using Base = FwdCfg<T, NS, P, CPL, 0>;
+    static constexpr int OPT = OPT_;  // 0 plain; 1 options; 2 options + zero-order hold
+    static constexpr int NUR = OPT > 0 ? 3 : 2;  // row sets of a warp's slot: u, delta (, z)
     static constexpr int kWarps = 4;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int GPW = Base::GPW, CPW = Base::CPW, NSP = Base::NSP, TC = Base::TC;
@@ -76,7 +80,7 @@ struct TmaCfg {
     static constexpr bool kF32 = Base::kF32;
     static constexpr int STAGES = kTmaStages;
     static constexpr int ESZ = (int)sizeof(T);
-    static constexpr int U_BOX = CPW * RROW * ESZ;   // bytes of one u (or delta) box
+    static constexpr int U_BOX = CPW * RROW * ESZ;   // bytes of one u (delta, z) box
     static constexpr int BC_BOX = NSP * RROW * ESZ;  // bytes of one B (or C) box
     static constexpr int U_SLOT = align_up(U_BOX, 128);
     static constexpr int BC_SLOT = align_up(BC_BOX, 128);
@@ -88,9 +92,10 @@ struct TmaCfg {
     static constexpr int TS = TC / 2;
     static constexpr int HROW = TS + 4;
     static constexpr int RS = align_up(P * HROW - 16, 32) + 16;
-    // bf16: a warp's widened fp32 rows [u CPW][delta CPW]; the chunk's B/C rows
-    // are widened once per CTA into a ring of WB slots [B NSP][C NSP]
-    static constexpr int WORK_ROWS = 2 * CPW;
+    // bf16: a warp's widened fp32 rows [u CPW][delta CPW] (, [z CPW]); the
+    // chunk's B/C rows are widened once per CTA into a ring of WB slots
+    // [B NSP][C NSP]
+    static constexpr int WORK_ROWS = NUR * CPW;
     static constexpr int WB = 3;
     static constexpr int BCW_BYTES = kF32 ? 0 : 2 * NSP * FROW * 4;
     // items of the warp epilogue per half chunk: (channel row, 4 steps); per lane
@@ -99,8 +104,8 @@ struct TmaCfg {
     // mbarriers [kWarps + 1][STAGES], counters [STAGES], then (bf16) the
     // widened ring's full [WB] and empty [WB] mbarriers
     static constexpr int OFF_BAR = 0;
-    static constexpr int OFF_U = 1024;  // [STAGES][kWarps][u, delta] slots
-    static constexpr int OFF_BC = OFF_U + STAGES * kWarps * 2 * U_SLOT;  // [STAGES][B, C] slots
+    static constexpr int OFF_U = 1024;  // [STAGES][kWarps][u, delta (, z)] slots
+    static constexpr int OFF_BC = OFF_U + STAGES * kWarps * NUR * U_SLOT;  // [STAGES][B, C] slots
     static constexpr int OFF_BCW = OFF_BC + STAGES * 2 * BC_SLOT;
     static constexpr int OFF_WORK = OFF_BCW + WB * BCW_BYTES;
     static constexpr int WORK_BYTES = kF32 ? 0 : WORK_ROWS * FROW * 4;  // per warp
@@ -125,11 +130,13 @@ struct TmaCfg {
 // latency overlaps the previous block's arithmetic), then per element
 // x = delta*A', a = 2^x, h = a*h + (delta*u)*B, y += C*h; the 4 partial
 // outputs of each channel go to yp[rl[j]][g] (row stride RS, lane stride
-// HROW) as one vector.  SCALAR: one decay rate per channel.
-template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR>
+// HROW) as one vector.  SCALAR: one decay rate per channel.  ZOH: the
+// zero-order-hold B-bar ((exp(delta A) - 1)/A per unit B) replaces delta*B.
+template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
 __device__ __forceinline__ void compute_half_tma(const float* su, const float* sd, const float* sB,
                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
                                                  int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                                 const float (&invA)[CPL][NS], const float (&invAs)[CPL],
                                                  float (&h)[CPL][NS]) {
     constexpr int NB = TS / 4;
     const float* bB = sB + g * FROW;
@@ -157,7 +164,7 @@ __device__ __forceinline__ void compute_half_tma(const float* su, const float* s
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 dd[j][s] = nd[j][s];
-                du[j][s] = nd[j][s] * nu[j][s];
+                du[j][s] = ZOH ? nu[j][s] : nd[j][s] * nu[j][s];
             }
 #pragma unroll
         for (int k = 0; k < NS; ++k)
@@ -171,7 +178,10 @@ __device__ __forceinline__ void compute_half_tma(const float* su, const float* s
         for (int j = 0; j < CPL; ++j)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                const float ys = dd[j][s] * As[j];
+                as[j][s] = SCALAR ? ex2(ys) : 0.f;
+                // zero-order hold with one rate: B-bar/B per (channel, step)
+                if (ZOH && SCALAR) du[j][s] *= zoh_coef(dd[j][s], ys, as[j][s], invAs[j]);
                 y[j][s] = 0.f;
             }
 #pragma unroll
@@ -180,8 +190,12 @@ __device__ __forceinline__ void compute_half_tma(const float* su, const float* s
             for (int j = 0; j < CPL; ++j)
 #pragma unroll
                 for (int k = 0; k < NS; ++k) {
-                    const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
-                    h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[k][s]);
+                    const float yk = dd[j][s] * Al2[j][k];
+                    const float a = SCALAR ? as[j][s] : ex2(yk);
+                    if (ZOH && !SCALAR)
+                        h[j][k] = fmaf(a, h[j][k], (zoh_coef(dd[j][s], yk, a, invA[j][k]) * du[j][s]) * bb[k][s]);
+                    else
+                        h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[k][s]);
                     y[j][s] = fmaf(cc[k][s], h[j][k], y[j][s]);
                 }
 #pragma unroll
@@ -202,10 +216,33 @@ __device__ __forceinline__ void widen_rows_warp(const bf16* src, float* dst, int
     }
 }
 
-template <typename T, int NS, int P, int CPL>
-__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
+// bf16 delta rows of the warp's channels [dw, dw + nrows): widen and apply the
+// delta transform (bias, softplus) to the steps inside the segment; padding
+// (channels past dim, steps past the segment) stays 0 so that it keeps the state
+template <int RROW, int FROW, int TC>
+__device__ __forceinline__ void widen_delta_rows_warp(const bf16* src, float* dst, int nrows, int lane,
+                                                      const FwdParams& p, long long dw, long long t0,
+                                                      long long t_end) {
+    constexpr int Q8 = TC / 8;
+    for (int q = lane; q < nrows * Q8; q += 32) {
+        const int r = q / Q8, c = (q % Q8) * 8;
+        float* v = dst + r * FROW + c;
+        widen8(src + r * RROW + c, v);
+        const long long dd = dw + r;
+        if (dd < p.dim) {
+            const float bias = p.delta_bias != nullptr ? __ldg(p.delta_bias + dd) : 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (t0 + c + e < t_end) v[e] = delta_in(v[e], bias, p.delta_softplus != 0);
+        }
+    }
+}
+
+template <typename T, int NS, int P, int CPL, int OPT>
+__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     sscan_fwd_tma(const FwdParams p, const __grid_constant__ TmaMaps tm) {
-    using Cfg = TmaCfg<T, NS, P, CPL>;
+    using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
+    constexpr int NUR = Cfg::NUR;
     constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
     constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW, RS = Cfg::RS, STAGES = Cfg::STAGES;
     constexpr unsigned FULL = 0xffffffffu;
@@ -233,8 +270,10 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     unsigned char* bc_ring = sbase + Cfg::OFF_BC;
     float* yp = reinterpret_cast<float*>(sbase + Cfg::OFF_YP + w * Cfg::YP_BYTES);
     auto u_slot = [&](int st) -> T* {
-        return reinterpret_cast<T*>(u_ring + (st * kWarps + w) * 2 * Cfg::U_SLOT);
+        return reinterpret_cast<T*>(u_ring + (st * kWarps + w) * NUR * Cfg::U_SLOT);
     };
+    const bool gated = OPT > 0 && p.z != nullptr;
+    const bool xform = OPT > 0 && (p.delta_softplus != 0 || p.delta_bias != nullptr);
     auto bc_slot = [&](int st) -> T* { return reinterpret_cast<T*>(bc_ring + st * 2 * Cfg::BC_SLOT); };
 
     uint64_t* bcw_full = reinterpret_cast<uint64_t*>(sbase + Cfg::OFF_BAR + Cfg::OFF_BCW_BAR);  // [WB]
@@ -255,14 +294,16 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     }
     __syncthreads();
 
-    // the warp's u/delta boxes of chunk c into stage st (lane 0 only)
+    // the warp's u/delta (and z) boxes of chunk c into stage st (lane 0 only)
     auto issue_u = [&](int c, int st) {
         T* dst = u_slot(st);
         uint64_t* bar = barU + w * STAGES + st;
-        mbar_arrive_expect_tx(bar, 2 * Cfg::U_BOX);
+        mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX);
         const int t0 = (int)(t_begin + (long long)c * TC);
         tma_load_3d(dst, &tm.u, t0, (int)dw, (int)b, bar);
         tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::U_SLOT, &tm.delta, t0, (int)dw, (int)b, bar);
+        if (gated)
+            tma_load_3d(reinterpret_cast<unsigned char*>(dst) + 2 * Cfg::U_SLOT, &tm.z, t0, (int)dw, (int)b, bar);
     };
     // the B/C boxes of chunk c into stage st (one thread)
     auto issue_bc = [&](int c, int st) {
@@ -285,6 +326,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
     long long ch[CPL];
     bool dval[CPL];
     float Al2[CPL][NS], As[CPL], h[CPL][NS];
+    float invA[CPL][NS], invAs[CPL];  // 1/A (0 where A = 0), for the zero-order hold
     bool uniform_rate = true;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
@@ -300,9 +342,11 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
             const float a = nv ? p.A[dch * p.N + n] : a_first;
             uniform_rate &= (a == a_first);
             Al2[j][k] = nv ? a * kLog2e : 0.f;
+            invA[j][k] = (nv && a != 0.f) ? 1.f / a : 0.f;
             h[j][k] = (s == 0 && p.h0 != nullptr && nv) ? p.h0[ch[j] * p.N + n] : 0.f;
         }
         As[j] = a_first * kLog2e;
+        invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
     }
     const bool scalar = __all_sync(FULL, uniform_rate);
 
@@ -325,7 +369,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
 
     // warp epilogue of one half chunk: sum the P partials, add D*u, store 4
     // steps per item (and the Kahan sums of delta of a local pass)
-    auto epilogue = [&](int half, long long t0, const float* su, const float* sd) {
+    auto epilogue = [&](int half, long long t0, const float* su, const float* sd, const float* sz) {
 #pragma unroll
         for (int k = 0; k < Cfg::IPH; ++k) {
             const int q = lane + 32 * k;
@@ -344,6 +388,12 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
             load4_smem(su + r * FROW + t4, uv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
+            if (OPT > 0 && gated) {  // out = (y + D*u) * silu(z)
+                float zv[4];
+                load4_smem(sz + r * FROW + t4, zv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] *= silu(zv[e]);
+            }
             if (dsum_on) {  // steps past the segment hold delta = 0
                 float dv[4];
                 load4_smem(sd + r * FROW + t4, dv);
@@ -397,7 +447,8 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
         const int st = i % STAGES;
         const unsigned par = (unsigned)(i / STAGES) & 1u;
         const int nx = i + STAGES;  // the chunk that refills this stage
-        const float *su, *sd, *sB, *sC;
+        const long long t0 = t_begin + (long long)i * TC;
+        const float *su, *sd, *sz, *sB, *sC;
         if constexpr (Cfg::kF32) {
             ok = mbar_wait_bounded(barU + w * STAGES + st, par);
             ok = mbar_wait_bounded(barBC + st, par) && ok;
@@ -405,41 +456,64 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
             if (!ok) break;
             su = reinterpret_cast<const float*>(u_slot(st));
             sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
+            sz = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + 2 * Cfg::U_SLOT);
             sB = reinterpret_cast<const float*>(bc_slot(st));
             sC = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(sB) + Cfg::BC_SLOT);
+            if (OPT > 0 && xform) {
+                // delta transform in place on the warp's rows: lane = step;
+                // padding (channels past dim, steps past the segment) keeps 0
+                float* wd = const_cast<float*>(sd);
+                const bool tin = t0 + lane < t_end;
+                for (int r = 0; r < CPW; ++r) {
+                    const long long dd = dw + r;
+                    if (tin && dd < p.dim) {
+                        const float bias = p.delta_bias != nullptr ? __ldg(p.delta_bias + dd) : 0.f;
+                        wd[r * FROW + lane] = delta_in(wd[r * FROW + lane], bias, p.delta_softplus != 0);
+                    }
+                }
+                __syncwarp();
+            }
         } else {
             // the next chunk's B/C when it is this warp's turn, one chunk ahead
             if (i + 1 < nchunks && (i + 1) % kWarps == w && !widen_bc(i + 1)) {
                 ok = false;
                 break;
             }
-            // the warp's own u/delta rows, widened, then the raw stage refilled
+            // the warp's own u/delta (z) rows, widened (delta transformed),
+            // then the raw stage refilled
             ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par));
             if (!ok) break;
             const bf16* ru = reinterpret_cast<const bf16*>(u_slot(st));
             widen_rows_warp<RROW, FROW, TC>(ru, work, CPW, lane);
-            widen_rows_warp<RROW, FROW, TC>(
-                reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(ru) + Cfg::U_SLOT),
-                work + CPW * FROW, CPW, lane);
+            const bf16* rd = reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(ru) + Cfg::U_SLOT);
+            if (OPT > 0 && xform)
+                widen_delta_rows_warp<RROW, FROW, TC>(rd, work + CPW * FROW, CPW, lane, p, dw, t0, t_end);
+            else
+                widen_rows_warp<RROW, FROW, TC>(rd, work + CPW * FROW, CPW, lane);
+            if (OPT > 0 && gated)
+                widen_rows_warp<RROW, FROW, TC>(
+                    reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(ru) + 2 * Cfg::U_SLOT),
+                    work + 2 * CPW * FROW, CPW, lane);
             __syncwarp();
             if (lane == 0 && nx < nchunks) issue_u(nx, st);
             ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u));
             if (!ok) break;
             su = work;
             sd = work + CPW * FROW;
+            sz = work + 2 * CPW * FROW;
             sB = reinterpret_cast<const float*>(sbase + Cfg::OFF_BCW + (i % Cfg::WB) * Cfg::BCW_BYTES);
             sC = sB + NSP * FROW;
         }
         constexpr int TS = Cfg::TS, HROW = Cfg::HROW;
-        const long long t0 = t_begin + (long long)i * TC;
+        constexpr bool ZOH = OPT == 2;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
             if (scalar)
-                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true>(su, sd, sB, sC, yp, rl, g, half * TS, Al2,
-                                                                       As, h);
+                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
+                                                                            Al2, As, invA, invAs, h);
             else
-                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false>(su, sd, sB, sC, yp, rl, g, half * TS,
-                                                                        Al2, As, h);
+                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
+                                                                             Al2, As, invA, invAs, h);
             __syncwarp();
             // after the second half, B/C of this chunk are no longer read by this warp
             if (half == 1 && lane == 0) {
@@ -450,12 +524,16 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
                     mbar_arrive(bcw_empty + i % Cfg::WB);
                 }
             }
-            epilogue(half, t0, su, sd);
+            epilogue(half, t0, su, sd, sz);
             __syncwarp();
         }
         if constexpr (Cfg::kF32) {
-            // u/delta of this stage are no longer read by this warp
-            if (lane == 0 && nx < nchunks) issue_u(nx, st);
+            // u/delta (z) of this stage are no longer read by this warp; the
+            // delta transform wrote them, so order those writes before the copy
+            if (lane == 0 && nx < nchunks) {
+                if (OPT > 0 && xform) fence_proxy_async_smem();
+                issue_u(nx, st);
+            }
         }
     }
     if (!ok) {
@@ -496,9 +574,9 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL>::kThreads)
 
 // Shared implementation of the per-dtype launch units (sscan_fwd_tma_*.cu).
 #ifdef SSCAN_TMA_IMPL
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream) {
-    using Cfg = TmaCfg<T, NS, P, CPL>;
+    using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
     if (p.N < 1 || p.N > (long long)Cfg::NSP) return cudaErrorInvalidValue;
     TmaMaps tm;
     const bool f32 = Cfg::kF32;
@@ -507,7 +585,9 @@ cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream
         !tma_encode_3d(&tm.B, p.B, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP) ||
         !tma_encode_3d(&tm.C, p.C, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP))
         return cudaErrorInvalidValue;
-    auto kern = sscan_fwd_tma<T, NS, P, CPL>;
+    if (OPT > 0 && p.z != nullptr && !tma_encode_3d(&tm.z, p.z, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW))
+        return cudaErrorInvalidValue;
+    auto kern = sscan_fwd_tma<T, NS, P, CPL, OPT>;
     static unsigned long long configured = 0;  // bit per device ordinal (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -522,10 +602,10 @@ cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream
     return cudaGetLastError();
 }
 
-template <typename T, int NS, int P, int CPL>
+template <typename T, int NS, int P, int CPL, int OPT>
 int occupancy_tma_variant() {
-    using Cfg = TmaCfg<T, NS, P, CPL>;
-    auto kern = sscan_fwd_tma<T, NS, P, CPL>;
+    using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
+    auto kern = sscan_fwd_tma<T, NS, P, CPL, OPT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;
@@ -535,9 +615,9 @@ int occupancy_tma_variant() {
 }
 
 #define SSCAN_TMA_LAUNCH_CASE(P_, NS_, CPL_) \
-    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return launch_tma_variant<UnitT, NS_, P_, CPL_>(p, grid, st);
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return launch_tma_variant<UnitT, NS_, P_, CPL_, UnitOPT>(p, grid, st);
 #define SSCAN_TMA_OCC_CASE(P_, NS_, CPL_) \
-    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_tma_variant<UnitT, NS_, P_, CPL_>();
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_tma_variant<UnitT, NS_, P_, CPL_, UnitOPT>();
 #define SSCAN_DEFINE_TMA_UNIT(SUFFIX)                                                               \
     cudaError_t fwd_tma_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t st) { \
         SSCAN_TMA_SHAPES(SSCAN_TMA_LAUNCH_CASE)                                                     \

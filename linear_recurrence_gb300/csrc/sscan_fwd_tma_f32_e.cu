@@ -1,0 +1,11 @@
+// float32-I/O instantiations of the TMA-fed selective-scan kernel: the plain scan.
+#define SSCAN_TMA_IMPL
+#include "sscan_fwd_tma.cuh"
+
+namespace sscan {
+
+using UnitT = float;
+constexpr int UnitOPT = 0;
+SSCAN_DEFINE_TMA_UNIT(f32_e)
+
+}  // namespace sscan

@@ -63,6 +63,8 @@ def test_options_single_and_split(lr, opt, dtype, L):
     w, x, o = _problem(dtype, L)
     plan = _run_and_compare(lr, w, x, o, OPTIONS[opt])
     assert "single" in plan
+    # aligned rows take the TMA-fed kernel, the others the cp.async kernel
+    assert (" tma " in plan) == (L % 8 == 0), plan
     plan = _run_and_compare(lr, w, x, o, OPTIONS[opt], segments=3)
     assert "S=3" in plan
     if OPTIONS[opt]["zoh"]:
