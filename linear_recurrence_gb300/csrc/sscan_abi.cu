@@ -435,8 +435,12 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
-        p.tiles_per_batch = (int)pl.corr_tiles_per_batch;
-        e = launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
+        if (use_tma) {
+            e = launch_fwd_tma(f32, p, sh, tiles * (S - 1), st);
+        } else {
+            p.tiles_per_batch = (int)pl.corr_tiles_per_batch;
+            e = launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
+        }
     }
     cudaError_t ef = cudaFreeAsync(scratch, st);
     if (e != cudaSuccess) return fail_cuda(e);

@@ -80,8 +80,8 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 
 // Shapes of the TMA-fed kernel (sscan_fwd_tma.cuh): four warps per CTA, so
 // DT = 4 * (32 / P) * CPL channels per CTA.  It serves the scan (plain or
-// with the options) with 16-byte aligned rows in the single-segment and
-// local-segment modes, for
+// with the options) with 16-byte aligned rows in every mode (single, local,
+// carry correction), for
 // 8 < N <= 16 (measured on GB300: as fast or faster than the cp.async kernel
 // there; slower for wide states, whose B/C ring costs occupancy).
 #ifndef SSCAN_TMA_SHAPES

@@ -62,7 +62,7 @@ bool tma_has_shape(Shape sh) {
 }
 
 cudaError_t fwd_tma_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream) {
-    if (p.mode == MODE_CORR || !p.vec) return cudaErrorInvalidValue;
+    if (!p.vec) return cudaErrorInvalidValue;
     switch (fwd_variant(p)) {
         case 2: return f32 ? fwd_tma_launch_f32_z(p, sh, grid, stream) : fwd_tma_launch_bf16_z(p, sh, grid, stream);
         case 1: return f32 ? fwd_tma_launch_f32_o(p, sh, grid, stream) : fwd_tma_launch_bf16_o(p, sh, grid, stream);

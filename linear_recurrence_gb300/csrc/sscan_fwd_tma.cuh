@@ -115,7 +115,9 @@ struct TmaCfg {
     static_assert(TC == 32, "epilogue items assume 8 four-step blocks per chunk");
     static_assert(CPW % 8 == 0, "a warp's epilogue items must fill its lanes");
     static_assert(RS >= P * HROW && (RS / 4) % 8 == 4, "partial row stride");
-    static constexpr int OFF_BCW_BAR = align_up((kWarps + 1) * STAGES * 8 + STAGES * 4, 8);
+    // after the mbarriers: the B/C release counters [STAGES] and the last
+    // chunk whose B/C copy was issued
+    static constexpr int OFF_BCW_BAR = align_up((kWarps + 1) * STAGES * 8 + STAGES * 4 + 4, 8);
     static_assert(OFF_BCW_BAR + 2 * WB * 8 <= 1024, "barrier area");
     static_assert(RROW * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
     static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256, "tensor-map box limits");
@@ -205,6 +207,49 @@ __device__ __forceinline__ void compute_half_tma(const float* su, const float* s
     }
 }
 
+// Steps [T0, T0 + TS) of the carry correction for the calling lane: the
+// homogeneous recurrence h = exp(delta*A)*h from the carried state and its
+// C-contraction, stored as partial outputs like compute_half_tma.  live[k]
+// (warp-uniform) skips the state slots whose carry has decayed below the
+// threshold in every lane of the warp.
+template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR>
+__device__ __forceinline__ void decay_half_tma(const float* sd, const float* sC, float* yp, const int (&rl)[CPL],
+                                               int g, int T0, const float (&Al2)[CPL][NS],
+                                               const float (&As)[CPL], const bool (&live)[NS],
+                                               float (&h)[CPL][NS]) {
+    const float* bC = sC + g * FROW;
+#pragma unroll 2
+    for (int t4 = T0; t4 < T0 + TS; t4 += 4) {
+        float dd[CPL][4], as[CPL][4], y[CPL][4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            load4_smem(sd + rl[j] * FROW + t4, dd[j]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                y[j][s] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            if (!live[k]) continue;
+            float cc[4];
+            load4_smem(bC + k * P * FROW + t4, cc);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    h[j][k] *= SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
+                    y[j][s] = fmaf(cc[s], h[j][k], y[j][s]);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            *reinterpret_cast<float4*>(yp + rl[j] * RS + g * HROW + (t4 - T0)) =
+                make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+    }
+}
+
 // bf16: widen rows [0, nrows) of TC (+ padding) elements, stride RROW, into
 // fp32 rows of stride FROW; one 16-byte piece (8 values) per item.
 template <int RROW, int FROW, int TC>
@@ -238,7 +283,10 @@ __device__ __forceinline__ void widen_delta_rows_warp(const bf16* src, float* ds
     }
 }
 
-template <typename T, int NS, int P, int CPL, int OPT>
+// CORR: the carry-correction instantiation (MODE_CORR: segment s >= 1 adds
+// the decaying contribution of its entry state to the local outputs; the u
+// tensor map then covers those outputs).
+template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
 __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     sscan_fwd_tma(const FwdParams p, const __grid_constant__ TmaMaps tm) {
     using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
@@ -257,7 +305,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int g = lane % P, gi = lane / P;
     const int tile = blockIdx.x / p.seg_count;
-    const int s = blockIdx.x % p.seg_count;  // single or local mode: segment index
+    const int s = (CORR ? 1 : 0) + blockIdx.x % p.seg_count;  // segment index
     const long long b = tile / p.tiles_per_batch;
     const long long d0 = (long long)(tile % p.tiles_per_batch) * Cfg::DT;
     const long long dw = d0 + (long long)w * CPW;  // the warp's first channel
@@ -280,10 +328,13 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     uint64_t* bcw_empty = bcw_full + Cfg::WB;                                                      // [WB]
     // the carry correction that follows a local pass may start its CTAs now;
     // it waits for this grid's completion before reading anything it wrote
-    griddep_launch_dependents();
+    if constexpr (CORR) griddep_wait();
+    else griddep_launch_dependents();
+    int* bc_hi = reinterpret_cast<int*>(bc_count + STAGES);  // last chunk whose B/C copy was issued
     if (tid == 0) {
         for (int i = 0; i < (kWarps + 1) * STAGES; ++i) mbar_init(barU + i, 1);
         for (int i = 0; i < STAGES; ++i) bc_count[i] = 0;
+        *bc_hi = -1;
         if constexpr (!Cfg::kF32) {
             for (int i = 0; i < Cfg::WB; ++i) {
                 mbar_init(bcw_full + i, 32);
@@ -294,8 +345,11 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     }
     __syncthreads();
 
-    // the warp's u/delta (and z) boxes of chunk c into stage st (lane 0 only)
+    // the warp's u/delta (and z) boxes of chunk c into stage st (lane 0 only);
+    // a correction's u rows are the local outputs
+    int u_hi = -1;  // last chunk whose u/delta copy this warp issued
     auto issue_u = [&](int c, int st) {
+        u_hi = c;
         T* dst = u_slot(st);
         uint64_t* bar = barU + w * STAGES + st;
         mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX);
@@ -305,13 +359,14 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         if (gated)
             tma_load_3d(reinterpret_cast<unsigned char*>(dst) + 2 * Cfg::U_SLOT, &tm.z, t0, (int)dw, (int)b, bar);
     };
-    // the B/C boxes of chunk c into stage st (one thread)
+    // the B/C boxes of chunk c into stage st (one thread); a correction needs C only
     auto issue_bc = [&](int c, int st) {
         T* dst = bc_slot(st);
         uint64_t* bar = barBC + st;
-        mbar_arrive_expect_tx(bar, 2 * Cfg::BC_BOX);
+        if constexpr (CORR) atomicMax(bc_hi, c);
+        mbar_arrive_expect_tx(bar, (CORR ? 1 : 2) * Cfg::BC_BOX);
         const int t0 = (int)(t_begin + (long long)c * TC);
-        tma_load_3d(dst, &tm.B, t0, 0, (int)b, bar);
+        if constexpr (!CORR) tma_load_3d(dst, &tm.B, t0, 0, (int)b, bar);
         tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::BC_SLOT, &tm.C, t0, 0, (int)b, bar);
     };
     if (lane == 0) {
@@ -343,16 +398,43 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
             uniform_rate &= (a == a_first);
             Al2[j][k] = nv ? a * kLog2e : 0.f;
             invA[j][k] = (nv && a != 0.f) ? 1.f / a : 0.f;
-            h[j][k] = (s == 0 && p.h0 != nullptr && nv) ? p.h0[ch[j] * p.N + n] : 0.f;
+            h[j][k] = (!CORR && s == 0 && p.h0 != nullptr && nv) ? p.h0[ch[j] * p.N + n] : 0.f;
         }
         As[j] = a_first * kLog2e;
         invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
+        if constexpr (CORR) {  // the carried state entering segment s
+            fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
+            if (!dval[j]) {
+#pragma unroll
+                for (int k = 0; k < NS; ++k) h[j][k] = 0.f;
+            }
+        }
     }
     const bool scalar = __all_sync(FULL, uniform_rate);
+    // correction: the carry is followed until every state of the CTA has
+    // fallen below 2^-24 of its entry magnitude; the last segment's final
+    // state is the carry decayed over the segment plus its local end state
+    float thr[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) m = fmaxf(m, fabsf(h[j][k]));
+        thr[j] = m * 0x1p-24f;
+        if (CORR && dval[j] && s == p.S - 1 && p.final_state != nullptr) {
+            const float dsg = p.seg_dsum[ch[j] * p.S + s];
+            const float* sst = p.seg_state + (ch[j] * p.S + s) * p.N;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const int n = k * P + g;
+                if (n < N) p.final_state[ch[j] * p.N + n] = fmaf(ex2(Al2[j][k] * dsg), h[j][k], sst[n]);
+            }
+        }
+    }
 
     // epilogue slots per half chunk: item q = lane + 32k covers channel row
     // q/4, steps 4(q%4)..+3 of the half
-    const bool dsum_on = p.mode == MODE_LOCAL;
+    const bool dsum_on = !CORR && p.mode == MODE_LOCAL;
     // Kahan sums of delta per slot (a slot is the same channel row and 4-step
     // offset in both halves)
     float dsum[Cfg::IPH], dcomp[Cfg::IPH];
@@ -386,13 +468,19 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
             }
             float uv[4];
             load4_smem(su + r * FROW + t4, uv);
+            if constexpr (!CORR) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
-            if (OPT > 0 && gated) {  // out = (y + D*u) * silu(z)
+                for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
+            }
+            if (OPT > 0 && gated) {  // out = (y + D*u) * silu(z); a correction is gated alike
                 float zv[4];
                 load4_smem(sz + r * FROW + t4, zv);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) v[e] *= silu(zv[e]);
+            }
+            if constexpr (CORR) {  // the local outputs, staged in the u rows
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] += uv[e];
             }
             if (dsum_on) {  // steps past the segment hold delta = 0
                 float dv[4];
@@ -427,7 +515,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         if (!good) return false;
         float* dst = reinterpret_cast<float*>(sbase + Cfg::OFF_BCW + ws * Cfg::BCW_BYTES);
         const bf16* rb = reinterpret_cast<const bf16*>(bc_slot(st));
-        widen_rows_warp<RROW, FROW, TC>(rb, dst, NSP, lane);
+        if constexpr (!CORR) widen_rows_warp<RROW, FROW, TC>(rb, dst, NSP, lane);
         widen_rows_warp<RROW, FROW, TC>(
             reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(rb) + Cfg::BC_SLOT),
             dst + NSP * FROW, NSP, lane);
@@ -453,7 +541,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
             ok = mbar_wait_bounded(barU + w * STAGES + st, par);
             ok = mbar_wait_bounded(barBC + st, par) && ok;
             ok = __all_sync(FULL, ok);
-            if (!ok) break;
+            if (!ok && !CORR) break;
             su = reinterpret_cast<const float*>(u_slot(st));
             sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
             sz = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + 2 * Cfg::U_SLOT);
@@ -477,12 +565,12 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
             // the next chunk's B/C when it is this warp's turn, one chunk ahead
             if (i + 1 < nchunks && (i + 1) % kWarps == w && !widen_bc(i + 1)) {
                 ok = false;
-                break;
+                if constexpr (!CORR) break;
             }
             // the warp's own u/delta (z) rows, widened (delta transformed),
             // then the raw stage refilled
-            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par));
-            if (!ok) break;
+            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par)) && ok;
+            if (!ok && !CORR) break;
             const bf16* ru = reinterpret_cast<const bf16*>(u_slot(st));
             widen_rows_warp<RROW, FROW, TC>(ru, work, CPW, lane);
             const bf16* rd = reinterpret_cast<const bf16*>(reinterpret_cast<const unsigned char*>(ru) + Cfg::U_SLOT);
@@ -496,8 +584,8 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
                     work + 2 * CPW * FROW, CPW, lane);
             __syncwarp();
             if (lane == 0 && nx < nchunks) issue_u(nx, st);
-            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u));
-            if (!ok) break;
+            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u)) && ok;
+            if (!ok && !CORR) break;
             su = work;
             sd = work + CPW * FROW;
             sz = work + 2 * CPW * FROW;
@@ -506,14 +594,42 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         }
         constexpr int TS = Cfg::TS, HROW = Cfg::HROW;
         constexpr bool ZOH = OPT == 2;
+        bool live[NS];  // correction: state slots still above the threshold somewhere in the warp
+        if constexpr (CORR) {
+            bool any = false;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                bool l = false;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) l |= fabsf(h[j][k]) > thr[j];
+                live[k] = scalar ? true : __any_sync(FULL, l);
+                any |= l;
+            }
+            // a wait that gave up in any warp ends the CTA's correction; so
+            // does the decay of every state of every lane (CTA-wide votes, so
+            // that every warp leaves the loop at the same chunk)
+            if (__syncthreads_or(!ok)) {
+                ok = false;
+                break;
+            }
+            if (!__syncthreads_or(any)) break;
+        }
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-            if (scalar)
+            if constexpr (CORR) {
+                if (scalar)
+                    decay_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true>(sd, sC, yp, rl, g, half * TS, Al2, As, live,
+                                                                         h);
+                else
+                    decay_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false>(sd, sC, yp, rl, g, half * TS, Al2, As,
+                                                                          live, h);
+            } else if (scalar) {
                 compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
                                                                             Al2, As, invA, invAs, h);
-            else
+            } else {
                 compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
                                                                              Al2, As, invA, invAs, h);
+            }
             __syncwarp();
             // after the second half, B/C of this chunk are no longer read by this warp
             if (half == 1 && lane == 0) {
@@ -548,6 +664,26 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         }
         return;
     }
+    if constexpr (CORR) {
+        // stopped early: wait (bounded) for the copies already issued for the
+        // chunks not consumed (chunk i's were), so that none lands in the
+        // shared memory of a CTA that has left
+        __syncthreads();  // no warp issues copies any more
+        if (lane == 0 && i < nchunks) {
+            // per ring slot, the last copy issued into it (earlier phases of
+            // the slot have completed); chunks up to i were consumed
+            bool good = true;
+            const int bhi = *bc_hi;
+            for (int st = 0; st < STAGES; ++st) {
+                const int cu = u_hi - ((u_hi - st) % STAGES + STAGES) % STAGES;  // largest c <= u_hi, c = st
+                if (cu > i) good = mbar_wait_bounded(barU + w * STAGES + st, (unsigned)(cu / STAGES) & 1u) && good;
+                const int cb = bhi - ((bhi - st) % STAGES + STAGES) % STAGES;
+                if (w == 0 && cb > i) good = mbar_wait_bounded(barBC + st, (unsigned)(cb / STAGES) & 1u) && good;
+            }
+            if (!good) atomicExch(p.status, (int)SSCAN_ERR_TIMEOUT);
+        }
+        return;
+    }
 
     if (dsum_on) {  // the segment's sum of delta per channel: 4 slots in 4 lanes
 #pragma unroll
@@ -578,34 +714,51 @@ template <typename T, int NS, int P, int CPL, int OPT>
 cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream) {
     using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
     if (p.N < 1 || p.N > (long long)Cfg::NSP) return cudaErrorInvalidValue;
+    const bool corr = p.mode == MODE_CORR;
     TmaMaps tm;
     const bool f32 = Cfg::kF32;
-    if (!tma_encode_3d(&tm.u, p.u, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
+    // a correction stages the local outputs where a local pass stages u
+    if (!tma_encode_3d(&tm.u, corr ? p.out : p.u, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
         !tma_encode_3d(&tm.delta, p.delta, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
         !tma_encode_3d(&tm.B, p.B, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP) ||
         !tma_encode_3d(&tm.C, p.C, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP))
         return cudaErrorInvalidValue;
     if (OPT > 0 && p.z != nullptr && !tma_encode_3d(&tm.z, p.z, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW))
         return cudaErrorInvalidValue;
-    auto kern = sscan_fwd_tma<T, NS, P, CPL, OPT>;
-    static unsigned long long configured = 0;  // bit per device ordinal (< 64)
+    auto kern = corr ? sscan_fwd_tma<T, NS, P, CPL, OPT, true> : sscan_fwd_tma<T, NS, P, CPL, OPT, false>;
+    static unsigned long long configured[2] = {0, 0};  // bit per device ordinal (< 64), per kernel
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
-    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+    if (!(__atomic_load_n(&configured[corr ? 1 : 0], __ATOMIC_ACQUIRE) & bit)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+        __atomic_fetch_or(&configured[corr ? 1 : 0], bit, __ATOMIC_ACQ_REL);
     }
-    kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p, tm);
-    return cudaGetLastError();
+    if (!corr) {
+        kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p, tm);
+        return cudaGetLastError();
+    }
+    // the correction follows the local pass as a programmatic dependent
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, tm);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, int NS, int P, int CPL, int OPT>
 int occupancy_tma_variant() {
     using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
-    auto kern = sscan_fwd_tma<T, NS, P, CPL, OPT>;
+    auto kern = sscan_fwd_tma<T, NS, P, CPL, OPT, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;
