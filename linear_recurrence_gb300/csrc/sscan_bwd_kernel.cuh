@@ -92,7 +92,10 @@ struct BwdCfg {
     static constexpr int RAW_BYTES = RAW_ELEMS * (int)sizeof(T);
     static constexpr int STAGES = 2;
     static constexpr int WORK_FLOATS = kF32 ? 0 : ROWS * FROW;
-    static constexpr int HB_FLOATS = TC * NS * kThreads;   // lane-private recomputed states
+    // recomputed states of a chunk: in registers for up to two states per
+    // lane (32 registers), else lane-private shared memory
+    static constexpr bool kHReg = NS <= 2;
+    static constexpr int HB_FLOATS = kHReg ? 0 : TC * NS * kThreads;
     // per-step partial sums: du, ddelta over the P lanes of a channel
     // [2][DT][P][FROW] (channel stride RS), dB, dC over the channels
     // [2][NSP][DT][FROW] (state stride RSB); RS/4 and RSB/4 odd keep the
@@ -413,6 +416,88 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
             continue;
         }
 
+        if constexpr (Cfg::kHReg) {
+        // recompute the chunk's states from its boundary state, kept in
+        // registers (hr[t][k]: h after step t of the chunk)
+        float hs[NS], hr[TC][NS];
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int n = k * P + g;
+            hs[k] = (dval && n < N) ? ck[(long long)c * p.N + n] : 0.f;
+            h[k] = hs[k];
+        }
+#pragma unroll
+        for (int t4 = 0; t4 < TC; t4 += 4) {
+            float uu[4], dd[4];
+            load4_smem(su + t4, uu);
+            load4_smem(sd + t4, dd);
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                float bb[4];
+                load4_smem(sB + k * P * FROW + t4, bb);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    h[k] = fmaf(ex2(dd[s] * Al2[k]), h[k], (dd[s] * uu[s]) * bb[s]);
+                    hr[t4 + s][k] = h[k];
+                }
+            }
+        }
+
+        // reverse sweep, 4 steps at a time.  Per step the sums over the lane's
+        // states: sdd = sum g*h_prev*a*A, sgb = sum g*B (ddelta adds u*sgb,
+        // du = delta*sgb + D*dy)
+#pragma unroll
+        for (int t4 = TC - 4; t4 >= 0; t4 -= 4) {
+            float uu[4], dd[4], dyv[4], du4[4];
+            load4_smem(su + t4, uu);
+            load4_smem(sd + t4, dd);
+            load4_smem(sy + t4, dyv);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) du4[s] = dd[s] * uu[s];
+            float sgb[4] = {0.f, 0.f, 0.f, 0.f}, sdd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                float bb[4], cc[4];
+                load4_smem(sB + k * P * FROW + t4, bb);
+                load4_smem(sC + k * P * FROW + t4, cc);
+                float pbv[4], pcv[4];
+#pragma unroll
+                for (int s = 3; s >= 0; --s) {
+                    const int t = t4 + s;
+                    const float hprev = t > 0 ? hr[t > 0 ? t - 1 : 0][k] : hs[k];
+                    const float a = ex2(dd[s] * Al2[k]);
+                    const float gt = fmaf(cc[s], dyv[s], G[k]);
+                    const float gha = (gt * hprev) * a;
+                    dAacc[k] = fmaf(gha, dd[s], dAacc[k]);
+                    sdd[s] = fmaf(gha, A[k], sdd[s]);
+                    sgb[s] = fmaf(gt, bb[s], sgb[s]);
+                    pbv[s] = gt * du4[s];
+                    pcv[s] = dyv[s] * hr[t][k];
+                    G[k] = a * gt;
+                }
+                const int n = k * P + g;
+                *reinterpret_cast<float4*>(pb + n * RSB + r * FROW + t4) = make_float4(pbv[0], pbv[1], pbv[2], pbv[3]);
+                *reinterpret_cast<float4*>(pb + NSP * RSB + n * RSB + r * FROW + t4) =
+                    make_float4(pcv[0], pcv[1], pcv[2], pcv[3]);
+            }
+            float sdu[4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                sdd[s] = fmaf(uu[s], sgb[s], sdd[s]);
+                sdu[s] = dd[s] * sgb[s];
+            }
+            if (g == 0) {
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    sdu[s] = fmaf(Dd, dyv[s], sdu[s]);
+                    dDacc = fmaf(dyv[s], uu[s], dDacc);
+                }
+            }
+            *reinterpret_cast<float4*>(pu + r * RS + g * FROW + t4) = make_float4(sdu[0], sdu[1], sdu[2], sdu[3]);
+            *reinterpret_cast<float4*>(pu + DT * RS + r * RS + g * FROW + t4) =
+                make_float4(sdd[0], sdd[1], sdd[2], sdd[3]);
+        }
+        } else {
         // recompute the chunk's states from its boundary state (lane-private,
         // 4 steps of a state per float4: hb[(t4/4 * NS + k) * NT + tid])
         float hs[NS];
@@ -498,6 +583,7 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(
             *reinterpret_cast<float4*>(pu + r * RS + g * FROW + t4) = make_float4(sdu[0], sdu[1], sdu[2], sdu[3]);
             *reinterpret_cast<float4*>(pu + DT * RS + r * RS + g * FROW + t4) =
                 make_float4(sdd[0], sdd[1], sdd[2], sdd[3]);
+        }
         }
         __syncthreads();  // every partial of the chunk is in place
 
