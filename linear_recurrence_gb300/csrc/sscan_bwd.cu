@@ -5,6 +5,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/sscan.h"
 #include "sscan_bwd_kernel.cuh"
@@ -58,6 +59,39 @@ cudaError_t launch_dtype(const BwdParams& p, BwdShape s, long long grid, cudaStr
     if (s.NS == 4 && s.P == 8) return launch_bwd<T, 4, 8>(p, grid, st);
     if (s.NS == 4 && s.P == 16) return launch_bwd<T, 4, 16>(p, grid, st);
     return cudaErrorInvalidValue;
+}
+
+template <typename T, int NS, int P>
+int occupancy_bwd() {
+    using Cfg = BwdCfg<T, NS, P>;
+    auto kern = sscan::sscan_bwd_chunked<T, NS, P>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Cfg::kThreads, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Resident CTAs per SM of the backward kernel of a shape, queried once per
+// device and dtype.
+template <typename T>
+int occupancy_dtype(BwdShape s) {
+    static std::atomic<int> cache[64][5] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int idx = s.P == 16 ? 4 : s.NS == 4 ? 3 : s.P == 8 ? 2 : s.NS == 2 ? 1 : 0;
+    std::atomic<int>& c = cache[dev & 63][idx];
+    int v = c.load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (s.NS == 1 && s.P == 4) v = occupancy_bwd<T, 1, 4>();
+        else if (s.NS == 2 && s.P == 4) v = occupancy_bwd<T, 2, 4>();
+        else if (s.NS == 2 && s.P == 8) v = occupancy_bwd<T, 2, 8>();
+        else if (s.NS == 4 && s.P == 8) v = occupancy_bwd<T, 4, 8>();
+        else v = occupancy_bwd<T, 4, 16>();
+        c.store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 inline bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
@@ -117,13 +151,17 @@ extern "C" int sscan_bwd(const void* u, const void* delta, const float* A, const
     const long long TC = sscan::kBwdChunk;
     const long long nchunks = (seqlen + TC - 1) / TC;
     // time split: about 12 warps per SM (4 per CTA), segments of 8 chunks or more
+    // few channels: split time so that the grid fills one wave of the
+    // resident CTA slots (a partial second wave would double the time of the
+    // CTAs in it)
     long long S = 1;
     {
         int dev = 0, nsm = 0;
         if (cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && nsm > 0) {
-            const long long target = 3LL * nsm;  // CTAs
-            if (grid < target) S = (target + grid - 1) / grid;
+            const int occ = dtype == SSCAN_F32 ? occupancy_dtype<float>(s) : occupancy_dtype<sscan::bf16>(s);
+            const long long slots = (long long)nsm * std::max(occ, 1);
+            if (grid < slots) S = slots / grid;
             S = std::min(S, std::max(1LL, nchunks / 8));
         }
     }

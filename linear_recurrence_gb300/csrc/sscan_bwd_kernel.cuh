@@ -95,6 +95,12 @@ struct BwdCfg {
     // recomputed states of a chunk: in registers for up to two states per
     // lane (32 registers), else lane-private shared memory
     static constexpr bool kHReg = NS <= 2;
+#ifndef SSCAN_BWD_MIN_BLOCKS
+#define SSCAN_BWD_MIN_BLOCKS 3
+#endif
+    // resident CTAs per SM asked of the compiler (register cap) where the
+    // shared memory allows them
+    static constexpr int kMinBlocks = kHReg ? SSCAN_BWD_MIN_BLOCKS : 1;
     static constexpr int HB_FLOATS = kHReg ? 0 : TC * NS * kThreads;
     // per-step partial sums: du, ddelta over the P lanes of a channel
     // [2][DT][P][FROW] (channel stride RS), dB, dC over the channels
@@ -192,7 +198,8 @@ __device__ __forceinline__ void bwd_widen(const T* st, float* wk, int N, int tid
 }
 
 template <typename T, int NS, int P>
-__global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads) sscan_bwd_chunked(const BwdParams p) {
+__global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads, BwdCfg<T, NS, P>::kMinBlocks)
+    sscan_bwd_chunked(const BwdParams p) {
     using Cfg = BwdCfg<T, NS, P>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, NSP = Cfg::NSP, FROW = Cfg::FROW, RROW = Cfg::RROW;
     constexpr int STAGES = Cfg::STAGES, NT = Cfg::kThreads, RS = Cfg::RS, RSB = Cfg::RSB;
