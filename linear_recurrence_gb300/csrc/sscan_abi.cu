@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <string.h>
 
 #include <algorithm>
 #include <atomic>
@@ -201,6 +202,7 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
     if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
     pl.tma = false;
     pl.corr_sh = pl.sh;
+    pl.corr_tma = false;
     pl.corr_tiles_per_batch = pl.tiles_per_batch;
     pl.corr_tiles = pl.tiles;
     *out = pl;
@@ -229,7 +231,7 @@ int cached_tma_occupancy(bool f32, Shape sh, int variant) {
 // shorter segments cost more in corrections than they gain in local-pass
 // parallelism (measured on GB300 with 512 channels x 8192 steps: 16, 18, 19
 // and 26 segments 55, 53, 51 and 58 us; 1536 x 65536: 12 segments 603 us,
-// 19 segments 575 us).  A problem wide enough to give (4,4,2), else (8,2,2),
+// 19 segments 575 us, on an earlier build).  A problem wide enough to give (4,4,2), else (8,2,2),
 // 6 warps per SM runs unsplit on that shape (8192 fp32 channels x 2048 steps:
 // (8,2,2) unsplit 123 us, (4,4,2) in 2 or 3 segments 130 / 148 us; 16384
 // channels: (4,4,2) unsplit 187 us, (8,2,2) 207 us).
@@ -288,8 +290,15 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
         }
     }
     if (!found) return SSCAN_ERR_INVALID;
-    best.corr_sh = Shape{4, 4, 1};
-    best.corr_tiles_per_batch = ceil_div(dim, shape_channels(best.corr_sh));
+    // the correction: for long segments (long sequences, where long memories
+    // make long decay horizons) on the TMA-fed kernel, shape (4,4,2); for short
+    // ones on the cp.async kernel, shape (8,2,1), whose smaller CTAs start and
+    // stop sooner (measured on GB300: 512 channels x 8192 steps in 19 segments
+    // 47.1 / 49.2 / 53.2 us with (8,2,1) / TMA (8,2,2) / TMA (4,4,2);
+    // 1536 x 65536 in 19 segments 554 / 548 / 509 us)
+    best.corr_tma = best.S > 1 && best.Tseg >= 32 * TC;
+    best.corr_sh = best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
+    best.corr_tiles_per_batch = ceil_div(dim, best.corr_tma ? tma_channels(best.corr_sh) : shape_channels(best.corr_sh));
     best.corr_tiles = batch * best.corr_tiles_per_batch;
     if (best.corr_tiles * best.S > (1LL << 30)) return SSCAN_ERR_INVALID;
     *out = best;
@@ -405,10 +414,16 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     p.status = status;
 
     snprintf(g_rec.plan, sizeof(g_rec.plan),
-             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s%s",
+             "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s%s%s",
              f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
              use_tma ? "tma " : "", S == 1 ? "single" : "local+correct", delta_bias ? " bias" : "",
-             p.delta_softplus ? " softplus" : "", p.zoh ? " zoh" : "", z ? " gate" : "");
+             p.delta_softplus ? " softplus" : "", p.zoh ? " zoh" : "", z ? " gate" : "",
+             S == 1 ? "" : pl.corr_tma ? " corr=tma" : " corr=cp.async");
+    if (S > 1) {  // the correction's shape
+        const size_t n = strlen(g_rec.plan);
+        snprintf(g_rec.plan + n, sizeof(g_rec.plan) - n, "(%d,%d,%d)", pl.corr_sh.P, pl.corr_sh.NS,
+                 pl.corr_sh.CPL);
+    }
 
     cudaError_t e;
     if (S == 1) {
@@ -435,12 +450,9 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
-        if (use_tma) {
-            e = launch_fwd_tma(f32, p, sh, tiles * (S - 1), st);
-        } else {
-            p.tiles_per_batch = (int)pl.corr_tiles_per_batch;
-            e = launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
-        }
+        p.tiles_per_batch = (int)pl.corr_tiles_per_batch;
+        e = pl.corr_tma ? launch_fwd_tma(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st)
+                        : launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
     }
     cudaError_t ef = cudaFreeAsync(scratch, st);
     if (e != cudaSuccess) return fail_cuda(e);

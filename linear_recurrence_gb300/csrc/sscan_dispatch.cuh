@@ -115,7 +115,8 @@ struct FwdPlan {
     long long S;      // time segments
     long long Tseg;   // steps per segment
     bool tma;         // the single/local pass runs on the TMA-fed kernel
-    Shape corr_sh;    // cp.async-kernel shape of the carry correction
+    Shape corr_sh;    // shape of the carry correction
+    bool corr_tma;    // the correction runs on the TMA-fed kernel (else cp.async)
     long long corr_tiles_per_batch;
     long long corr_tiles;
 };

@@ -73,6 +73,15 @@ def test_options_single_and_split(lr, opt, dtype, L):
         assert " gate" in plan
 
 
+@pytest.mark.parametrize("opt", ["all", "gate", "bias_softplus"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_options_long_segments(lr, opt, dtype):
+    # segments of 2048 steps: local pass and carry correction on the TMA kernel
+    w, x, o = _problem(dtype, 4096, batch=1, dim=40, seed=11)
+    plan = _run_and_compare(lr, w, x, o, OPTIONS[opt], segments=2)
+    assert " tma " in plan and "S=2 " in plan, plan
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_zoh_shared_rate_and_zero_rates(lr, dtype):
     # a decay rate shared by all states (one exponent per channel and step)

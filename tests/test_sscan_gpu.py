@@ -133,6 +133,8 @@ TMA_CASES = [
     (2, 64, 996, 9, 8, 3, True, False),     # no h0, short last segment
     (1, 300, 64, 16, 0, 0, True, True),     # two chunks, warps wholly past dim
     (4, 17, 8, 16, 8, 0, True, True),       # a partial first chunk only
+    (1, 40, 4096, 16, 4, 3, True, True),    # long segments: the correction on the TMA kernel
+    (2, 24, 3200, 12, 8, 2, True, False),   # the same with a short last segment, no h0
 ]
 
 
