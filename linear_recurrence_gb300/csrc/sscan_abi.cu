@@ -211,10 +211,10 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
 
 // Resident CTAs per SM of a TMA-kernel shape, queried once per device.
 int cached_tma_occupancy(bool f32, Shape sh, int variant) {
-    static std::atomic<int> cache[64][2][2][3] = {};  // device, dtype, (8,2,2) / (4,4,2), variant
+    static std::atomic<int> cache[64][2][3][3] = {};  // device, dtype, (8,2,2) / (4,4,2) / (4,16,2), variant
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1][sh.P == 4 ? 1 : 0][variant % 3];
+    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1][sh.P == 8 ? 0 : sh.NS == 4 ? 1 : 2][variant % 3];
     int v = c.load(std::memory_order_relaxed);
     if (v == 0) {
         v = fwd_tma_occupancy(f32, sh, variant);
@@ -242,11 +242,12 @@ int cached_tma_occupancy(bool f32, Shape sh, int variant) {
 // long64k 535 / 559 / 568 us).
 int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long long seqlen, long long N,
                  int segments, int lanes, FwdPlan* out) {
-    if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
+    if (N <= 8 || N > 64 || (N > 16 && N <= 32)) return SSCAN_ERR_INVALID;
+    const bool wide = N > 32;  // 64 state slots: shape (4,16,2)
     const int nsm = std::max(sm_count(), 1);
     const long long TC = kChunkSteps;
-    const Shape cands[] = {{4, 4, 2}, {8, 2, 2}};
-    const long long min_chunks[] = {16, 0};
+    const Shape cands[] = {wide ? Shape{4, 16, 2} : Shape{4, 4, 2}, {8, 2, 2}};
+    const long long min_chunks[] = {wide ? 0 : 16, 0};
     // warps per SM that an unsplit launch must give to be taken as it is
     const long long min_warps[] = {6, 6};
     // without a pinned plan, the first candidate whose unsplit grid is wide
@@ -254,14 +255,14 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
     // with slow decays)
     int unsplit = -1;
     if (segments == 0)
-        for (int i = 0; i < 2 && unsplit < 0; ++i) {
+        for (int i = 0; i < (wide ? 1 : 2) && unsplit < 0; ++i) {
             const Shape sh = cands[i];
             if (lanes != 0 && lanes != sh.P) continue;
             if (batch * ceil_div(dim, tma_channels(sh)) * 4 >= min_warps[i] * nsm) unsplit = i;
         }
     FwdPlan best{};
     bool found = false;
-    for (int i = 0; i < 2 && !found; ++i) {
+    for (int i = 0; i < (wide ? 1 : 2) && !found; ++i) {
         const Shape sh = cands[i];
         if (!tma_has_shape(sh) || (lanes != 0 && lanes != sh.P)) continue;
         if (unsplit >= 0 && i != unsplit) continue;
@@ -283,7 +284,7 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
         pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
         pl.S = ceil_div(seqlen, pl.Tseg);
         if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
-        const bool last = i == 1 || lanes != 0 || segments != 0;
+        const bool last = i == (wide ? 0 : 1) || lanes != 0 || segments != 0;
         if (pl.S == 1 || pl.Tseg >= min_chunks[i] * TC || last) {
             best = pl;
             found = true;
@@ -296,8 +297,8 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
     // stop sooner (measured on GB300: 512 channels x 8192 steps in 19 segments
     // 47.1 / 49.2 / 53.2 us with (8,2,1) / TMA (8,2,2) / TMA (4,4,2);
     // 1536 x 65536 in 19 segments 554 / 548 / 509 us)
-    best.corr_tma = best.S > 1 && best.Tseg >= 32 * TC;
-    best.corr_sh = best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
+    best.corr_tma = best.S > 1 && (wide || best.Tseg >= 32 * TC);
+    best.corr_sh = wide ? Shape{4, 16, 2} : best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
     best.corr_tiles_per_batch = ceil_div(dim, best.corr_tma ? tma_channels(best.corr_sh) : shape_channels(best.corr_sh));
     best.corr_tiles = batch * best.corr_tiles_per_batch;
     if (best.corr_tiles * best.S > (1LL << 30)) return SSCAN_ERR_INVALID;

@@ -85,7 +85,7 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 // 8 < N <= 16 (measured on GB300: as fast or faster than the cp.async kernel
 // there; slower for wide states, whose B/C ring costs occupancy).
 #ifndef SSCAN_TMA_SHAPES
-#define SSCAN_TMA_SHAPES(X) X(8, 2, 2) X(4, 4, 2)
+#define SSCAN_TMA_SHAPES(X) X(8, 2, 2) X(4, 4, 2) X(4, 16, 2)
 #endif
 inline int tma_channels(Shape sh) { return 4 * (32 / sh.P) * sh.CPL; }
 bool tma_has_shape(Shape sh);

@@ -96,7 +96,7 @@ struct TmaCfg {
     // chunk's B/C rows are widened once per CTA into a ring of WB slots
     // [B NSP][C NSP]
     static constexpr int WORK_ROWS = NUR * CPW;
-    static constexpr int WB = 3;
+    static constexpr int WB = NS > 4 ? 2 : 3;  // two slots for wide states (shared memory)
     static constexpr int BCW_BYTES = kF32 ? 0 : 2 * NSP * FROW * 4;
     // items of the warp epilogue per half chunk: (channel row, 4 steps); per lane
     static constexpr int IPH = CPW * (TS / 4) / 32;
@@ -135,7 +135,7 @@ struct TmaCfg {
 // HROW) as one vector.  SCALAR: one decay rate per channel.  ZOH: the
 // zero-order-hold B-bar ((exp(delta A) - 1)/A per unit B) replaces delta*B.
 template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
-__device__ __forceinline__ void compute_half_tma(const float* su, const float* sd, const float* sB,
+__device__ __forceinline__ void compute_half_narrow(const float* su, const float* sd, const float* sB,
                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
                                                  int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
                                                  const float (&invA)[CPL][NS], const float (&invAs)[CPL],
@@ -205,6 +205,95 @@ __device__ __forceinline__ void compute_half_tma(const float* su, const float* s
             *reinterpret_cast<float4*>(yp + rl[j] * RS + g * HROW + (t4 - T0)) =
                 make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
     }
+}
+
+// As compute_half_narrow for wide lanes (NS > 4 states): the u/delta vectors
+// are read one block ahead; the B/C vectors are read per quad of states inside
+// the block (all of them at once would need 8*NS registers).
+template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
+__device__ __forceinline__ void compute_half_wide(const float* su, const float* sd, const float* sB,
+                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
+                                                  int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                                  const float (&invA)[CPL][NS], const float (&invAs)[CPL],
+                                                  float (&h)[CPL][NS]) {
+    constexpr int NB = TS / 4;
+    constexpr int QS = 4, NQ = NS / QS;
+    static_assert(NS % QS == 0, "states come in whole quads");
+    const float* bB = sB + g * FROW;
+    const float* bC = sC + g * FROW;
+    float nu[CPL][4], nd[CPL][4];
+    auto load_block = [&](int t4) {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            load4_smem(su + rl[j] * FROW + t4, nu[j]);
+            load4_smem(sd + rl[j] * FROW + t4, nd[j]);
+        }
+    };
+    load_block(T0);
+#pragma unroll 2
+    for (int blk = 0; blk < NB; ++blk) {
+        const int t4 = T0 + 4 * blk;
+        float dd[CPL][4], du[CPL][4], as[CPL][4], y[CPL][4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                dd[j][s] = nd[j][s];
+                du[j][s] = ZOH ? nu[j][s] : nd[j][s] * nu[j][s];
+            }
+        if (blk + 1 < NB) load_block(t4 + 4);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const float ys = dd[j][s] * As[j];
+                as[j][s] = SCALAR ? ex2(ys) : 0.f;
+                if (ZOH && SCALAR) du[j][s] *= zoh_coef(dd[j][s], ys, as[j][s], invAs[j]);
+                y[j][s] = 0.f;
+            }
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float bb[QS][4], cc[QS][4];
+#pragma unroll
+            for (int kk = 0; kk < QS; ++kk) {
+                load4_smem(bB + (q * QS + kk) * P * FROW + t4, bb[kk]);
+                load4_smem(bC + (q * QS + kk) * P * FROW + t4, cc[kk]);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int kk = 0; kk < QS; ++kk) {
+                        const int k = q * QS + kk;
+                        const float yk = dd[j][s] * Al2[j][k];
+                        const float a = SCALAR ? as[j][s] : ex2(yk);
+                        if (ZOH && !SCALAR)
+                            h[j][k] = fmaf(a, h[j][k], (zoh_coef(dd[j][s], yk, a, invA[j][k]) * du[j][s]) * bb[kk][s]);
+                        else
+                            h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[kk][s]);
+                        y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
+                    }
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+            *reinterpret_cast<float4*>(yp + rl[j] * RS + g * HROW + (t4 - T0)) =
+                make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
+    }
+}
+
+template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
+__device__ __forceinline__ void compute_half_tma(const float* su, const float* sd, const float* sB,
+                                                 const float* sC, float* yp, const int (&rl)[CPL], int g,
+                                                 int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
+                                                 const float (&invA)[CPL][NS], const float (&invAs)[CPL],
+                                                 float (&h)[CPL][NS]) {
+    if constexpr (NS <= 4)
+        compute_half_narrow<NS, P, CPL, FROW, RS, HROW, TS, SCALAR, ZOH>(su, sd, sB, sC, yp, rl, g, T0, Al2, As,
+                                                                         invA, invAs, h);
+    else
+        compute_half_wide<NS, P, CPL, FROW, RS, HROW, TS, SCALAR, ZOH>(su, sd, sB, sC, yp, rl, g, T0, Al2, As,
+                                                                       invA, invAs, h);
 }
 
 // Steps [T0, T0 + TS) of the carry correction for the calling lane: the
