@@ -28,10 +28,10 @@
 //     arrive) and an empty one (every warp arrives when it is done with the
 //     slot); only the widening warp reads the raw B/C stage, so it refills
 //     that stage itself.
-// Boxes are TC + 16 bytes wide: the extra columns (the next chunk's first
-// steps, or zeros past the end) pad every shared-memory row exactly as the
-// cp.async ring does, so the reads of different rows at one step fall in
-// different banks.  Every mbarrier wait is bounded (about a second); a wait
+// fp32 boxes are TC + 16 bytes wide: the extra columns (the next chunk's
+// first steps, or zeros past the end) pad every shared-memory row exactly as
+// the cp.async ring does, so the reads of different rows at one step fall in
+// different banks; bf16 boxes are TC wide (their rows are only widened).  Every mbarrier wait is bounded (about a second); a wait
 // that gives up records SSCAN_ERR_TIMEOUT in the status word, waits (again
 // bounded) for the copies still in flight, and ends the warp's work.
 #pragma once
@@ -75,7 +75,11 @@ struct TmaCfg {
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int GPW = Base::GPW, CPW = Base::CPW, NSP = Base::NSP, TC = Base::TC;
     static constexpr int DT = kWarps * CPW;  // channels per CTA
-    static constexpr int RROW = Base::RROW;  // raw row: TC + 16 bytes of elements
+    // raw row: fp32 rows are read in place, so they keep the TC + 16 bytes
+    // of the bank-spreading pad; bf16 rows are only widened (whole 16-byte
+    // pieces of consecutive rows) and take no pad, which keeps the wide-state
+    // CTA within half an SM's shared memory
+    static constexpr int RROW = Base::kF32 ? Base::RROW : TC;
     static constexpr int FROW = Base::FROW;  // fp32 row: TC + 4
     static constexpr bool kF32 = Base::kF32;
     static constexpr int STAGES = kTmaStages;
