@@ -54,6 +54,13 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" :: "n"(N) : "memory");
 }
 
+// Four fp32 additions to global memory as one vector reduction (no return
+// value); p must be 16-byte aligned.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // ---- programmatic dependent launch ---------------------------------------
 
 // Let the next kernel on the stream, when launched as a programmatic

@@ -22,8 +22,9 @@
 // state into lane-private shared memory, then sweeps the chunk in reverse,
 // carrying G = a_{t+1}*g_{t+1} in registers.  Per-step sums over a channel's
 // states (du, ddelta) and over the CTA's channels (dB, dC) go through shared
-// memory partials; dB and dC are accumulated into float32 outputs with
-// atomic adds, dA and dD once per lane at the end.
+// memory partials; dB and dC are accumulated into float32 outputs with one
+// vector reduction per (tile, state, 4 steps), dA and dD with atomic adds once
+// per lane at the end.
 //
 // Few channels and long sequences are split into S time segments, each its
 // own CTA.  A first launch (mode 1) computes per segment the forward
@@ -647,9 +648,13 @@ __global__ void __launch_bounds__(BwdCfg<T, NS, P>::kThreads, BwdCfg<T, NS, P>::
                 for (int e = 0; e < 4; ++e) v[e] += x[e];
             }
             float* o = (which ? p.dC : p.dB) + (b * p.N + n) * p.L + t;
+            if (t + 4 <= p.L && (reinterpret_cast<uintptr_t>(o) & 15u) == 0) {
+                red_add_v4(o, v[0], v[1], v[2], v[3]);  // one L2 reduction for the 4 steps
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (t + e < p.L) atomicAdd(o + e, v[e]);
+                for (int e = 0; e < 4; ++e)
+                    if (t + e < p.L) atomicAdd(o + e, v[e]);
+            }
         }
         // the next chunk's copy, partials and recompute start after this barrier
         __syncthreads();
