@@ -632,11 +632,10 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
     const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + TC - 1) / TC) : 0;
     const int N = (int)p.N;
 
-    // a correction launched as a programmatic dependent of the local pass
-    // waits here for that pass's outputs and aggregates; a local pass lets the
-    // correction's CTAs start early
-    if constexpr (CORR) griddep_wait();
-    else griddep_launch_dependents();
+    // a local pass lets the correction (launched as its programmatic
+    // dependent) start its CTAs early: they read the decay rates, then wait
+    // for the pass's outputs and aggregates
+    if constexpr (!CORR) griddep_launch_dependents();
 
     // the lane's channels and their decay rates (A * log2 e); a warp whose
     // channels each have a single rate takes the one-exponent-per-step path
@@ -664,6 +663,10 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
         As[j] = a_first * kLog2e;
         invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
+    }
+    if constexpr (CORR) griddep_wait();
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
         if (corr) {
             fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
             if (!dval[j]) {

@@ -420,9 +420,9 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     uint64_t* bcw_full = reinterpret_cast<uint64_t*>(sbase + Cfg::OFF_BAR + Cfg::OFF_BCW_BAR);  // [WB]
     uint64_t* bcw_empty = bcw_full + Cfg::WB;                                                      // [WB]
     // the carry correction that follows a local pass may start its CTAs now;
-    // it waits for this grid's completion before reading anything it wrote
-    if constexpr (CORR) griddep_wait();
-    else griddep_launch_dependents();
+    // it sets up (barriers, decay rates) while the pass runs and waits for the
+    // pass's completion before reading anything the pass wrote
+    if constexpr (!CORR) griddep_launch_dependents();
     int* bc_hi = reinterpret_cast<int*>(bc_count + STAGES);  // last chunk whose B/C copy was issued
     if (tid == 0) {
         for (int i = 0; i < (kWarps + 1) * STAGES; ++i) mbar_init(barU + i, 1);
@@ -462,12 +462,15 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         if constexpr (!CORR) tma_load_3d(dst, &tm.B, t0, 0, (int)b, bar);
         tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::BC_SLOT, &tm.C, t0, 0, (int)b, bar);
     };
-    if (lane == 0) {
-        for (int c = 0; c < STAGES && c < nchunks; ++c) {
-            issue_u(c, c);
-            if (w == 0) issue_bc(c, c);
+    auto issue_first = [&]() {
+        if (lane == 0) {
+            for (int c = 0; c < STAGES && c < nchunks; ++c) {
+                issue_u(c, c);
+                if (w == 0) issue_bc(c, c);
+            }
         }
-    }
+    };
+    if constexpr (!CORR) issue_first();
 
     // the lane's channels (rows rl[j] of the warp) and their decay rates
     int rl[CPL];
@@ -495,7 +498,13 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         }
         As[j] = a_first * kLog2e;
         invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
-        if constexpr (CORR) {  // the carried state entering segment s
+    }
+    if constexpr (CORR) {
+        // the local pass's outputs and aggregates are complete from here on
+        griddep_wait();
+        issue_first();
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {  // the carried state entering segment s
             fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
             if (!dval[j]) {
 #pragma unroll
