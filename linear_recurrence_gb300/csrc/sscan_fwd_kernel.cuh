@@ -234,10 +234,11 @@ struct Smem {
 
 // Vector path: issue this thread's 16-byte cp.async pieces of chunk [t0, t0+TC)
 // into stage st.  Out-of-range pieces are zero-filled (delta = 0 keeps the state).
+// load_d = false leaves out the delta (and z) rows.
 template <typename T, int NS, int P, int CPL, int OPT>
 __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long b, long long d0,
                                             long long t0, long long t_end, int tid, bool load_u,
-                                            bool load_b, bool load_c) {
+                                            bool load_b, bool load_c, bool load_d = true) {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, RROW = Cfg::RROW, NSP = Cfg::NSP, PPR = Cfg::PPR, VE = Cfg::VECE;
     const T* gu = static_cast<const T*>(p.u);
@@ -252,6 +253,7 @@ __device__ __forceinline__ void issue_chunk(const FwdParams& p, T* st, long long
         const bool ok = dd < p.dim && t < t_end;
         const long long off = (b * p.dim + (ok ? dd : 0)) * p.L + (ok ? t : 0);
         if (load_u) cp_async16(st + r * RROW + pc * VE, gu + off, ok ? 16 : 0);
+        if (!load_d) continue;
         cp_async16(st + (DT + r) * RROW + pc * VE, gd + off, ok ? 16 : 0);
         if constexpr (OPT > 0)
             if (gz != nullptr) cp_async16(st + (Cfg::ZROW0 + r) * RROW + pc * VE, gz + off, ok ? 16 : 0);
@@ -664,7 +666,18 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         As[j] = a_first * kLog2e;
         invAs[j] = a_first != 0.f ? 1.f / a_first : 0.f;
     }
-    if constexpr (CORR) griddep_wait();
+    if constexpr (CORR) {
+        // the first chunks' inputs (delta, z, C) are in flight before the wait;
+        // their local outputs join the same copy groups after it
+        if (vec) {
+#pragma unroll
+            for (int j = 0; j < STAGES - 1; ++j)
+                if (j < nchunks)
+                    issue_chunk<T, NS, P, CPL, OPT>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid,
+                                                    false, false, load_c);
+        }
+        griddep_wait();
+    }
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         if (corr) {
@@ -724,13 +737,14 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
     }
 
-    // prologue: chunks 0 .. STAGES-2 in flight
+    // prologue: chunks 0 .. STAGES-2 in flight (a correction issued their
+    // inputs before its wait and adds the local outputs now)
     if (vec) {
 #pragma unroll
         for (int j = 0; j < STAGES - 1; ++j) {
             if (j < nchunks)
                 issue_chunk<T, NS, P, CPL, OPT>(q, sm.stage(j), b, d0, t_begin + (long long)j * TC, t_end, tid,
-                                           load_u, load_b, load_c);
+                                           load_u, corr ? false : load_b, corr ? false : load_c, !corr);
             cp_async_commit();
         }
     }

@@ -462,15 +462,27 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         if constexpr (!CORR) tma_load_3d(dst, &tm.B, t0, 0, (int)b, bar);
         tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::BC_SLOT, &tm.C, t0, 0, (int)b, bar);
     };
-    auto issue_first = [&]() {
+    if constexpr (!CORR) {
         if (lane == 0) {
             for (int c = 0; c < STAGES && c < nchunks; ++c) {
                 issue_u(c, c);
                 if (w == 0) issue_bc(c, c);
             }
         }
-    };
-    if constexpr (!CORR) issue_first();
+    } else if (lane == 0) {
+        // a correction's first chunks: the inputs (delta, z, C) before the
+        // wait on the local pass, the local outputs (its u rows) after it
+        for (int c = 0; c < STAGES && c < nchunks; ++c) {
+            u_hi = c;
+            uint64_t* bar = barU + w * STAGES + c;
+            mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX);
+            const int t0 = (int)(t_begin + (long long)c * TC);
+            unsigned char* dst = reinterpret_cast<unsigned char*>(u_slot(c));
+            tma_load_3d(dst + Cfg::U_SLOT, &tm.delta, t0, (int)dw, (int)b, bar);
+            if (gated) tma_load_3d(dst + 2 * Cfg::U_SLOT, &tm.z, t0, (int)dw, (int)b, bar);
+            if (w == 0) issue_bc(c, c);
+        }
+    }
 
     // the lane's channels (rows rl[j] of the warp) and their decay rates
     int rl[CPL];
@@ -502,7 +514,10 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     if constexpr (CORR) {
         // the local pass's outputs and aggregates are complete from here on
         griddep_wait();
-        issue_first();
+        if (lane == 0)
+            for (int c = 0; c < STAGES && c < nchunks; ++c)
+                tma_load_3d(u_slot(c), &tm.u, (int)(t_begin + (long long)c * TC), (int)dw, (int)b,
+                            barU + w * STAGES + c);
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {  // the carried state entering segment s
             fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
