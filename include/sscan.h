@@ -67,7 +67,8 @@ enum {
  *
  * Scratch: long sequences with few channels are split in time; the split
  * needs batch*dim*segments*(dstate+1) floats of scratch, taken stream-ordered
- * from CUDA's default memory pool and returned on the same stream.
+ * from the library's memory pool on the current device (which keeps up to
+ * 1 GiB mapped while idle) and returned on the same stream.
  */
 int sscan_fwd(const void *u, const void *delta, const float *A, const void *B,
               const void *C, const float *D, const float *h0, void *out,
@@ -195,7 +196,7 @@ int sscan_step(const void *u, const void *delta, const float *A, const void *B,
  * engine's per-request plugin hook running under a fixed memory budget, a
  * real-time loop in which an allocation could synchronise the device or wait
  * on the allocator, a runtime that hands out all memory up front.  sscan_fwd
- * takes the scratch of a time-split launch from CUDA's stream-ordered pool;
+ * takes the scratch of a time-split launch from a stream-ordered pool;
  * this entry point keeps that scratch in a fixed device array of
  * SSCAN_NOALLOC_SCRATCH_BYTES instead and calls no allocating routine.  The
  * caller still passes every input and output.

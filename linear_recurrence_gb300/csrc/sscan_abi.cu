@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "../../include/sscan.h"
 #include "pscan_kernel.cuh"
@@ -83,6 +84,41 @@ int* device_status_ptr() {
 }  // namespace
 
 namespace sscan {
+
+// The default stream-ordered pool returns its memory to the driver whenever
+// the host synchronises, and the next allocation maps it again (measured on
+// GB300: 80-125 us added to the first call after a synchronisation); this
+// pool keeps what it holds up to kScratchRetainBytes.
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (pools[dev & 63] == nullptr) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t created = nullptr;
+            e = cudaMemPoolCreate(&created, &props);
+            if (e != cudaSuccess) return e;
+            unsigned long long keep = kScratchRetainBytes;
+            e = cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep);
+            if (e != cudaSuccess) {
+                cudaMemPoolDestroy(created);
+                return e;
+            }
+            pools[dev & 63] = created;
+        }
+        pool = pools[dev & 63];
+    }
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
 // Call record of an entry point defined in another translation unit.
 void record_call(int launches, cudaStream_t stream, const char* plan) {
     g_rec.launches = launches;
@@ -438,7 +474,7 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     const size_t nseg = (size_t)(batch * dim) * (size_t)S;
     const size_t scratch_bytes = nseg * (size_t)(dstate + 1) * sizeof(float);
     void* scratch = nullptr;
-    e = cudaMallocAsync(&scratch, scratch_bytes, st);
+    e = sscan::scratch_alloc(&scratch, scratch_bytes, st);
     if (e != cudaSuccess) return fail_cuda(e);
     p.seg_state = static_cast<float*>(scratch);
     p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
@@ -519,7 +555,7 @@ int pscan(const float* a, const float* b, float* h, const float* h0, int64_t row
         return e == cudaSuccess ? SSCAN_OK : fail_cuda(e);
     }
     void* scratch = nullptr;
-    e = cudaMallocAsync(&scratch, (size_t)(rows * S) * 2 * sizeof(float), st);
+    e = sscan::scratch_alloc(&scratch, (size_t)(rows * S) * 2 * sizeof(float), st);
     if (e != cudaSuccess) return fail_cuda(e);
     p.agg_a = static_cast<float*>(scratch);
     p.agg_b = p.agg_a + rows * S;

@@ -13,6 +13,7 @@
 namespace sscan {
 void record_call(int launches, cudaStream_t stream, const char* plan);
 void record_error(cudaError_t e);
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream);  // sscan_abi.cu
 }  // namespace sscan
 
 namespace {
@@ -172,7 +173,7 @@ extern "C" int sscan_bwd(const void* u, const void* delta, const float* A, const
     const size_t nseg = (size_t)(batch * dim) * (size_t)S;
     const size_t scratch_floats = nckpt + (S > 1 ? nseg * (2 * (size_t)dstate + 1) : 0);
     void* scratch = nullptr;
-    e = cudaMallocAsync(&scratch, scratch_floats * sizeof(float), st);
+    e = sscan::scratch_alloc(&scratch, scratch_floats * sizeof(float), st);
     if (e != cudaSuccess) {
         sscan::record_error(e);
         return SSCAN_ERR_CUDA;

@@ -107,6 +107,13 @@ SSCAN_DECLARE_TMA_UNIT(bf16_z)
 bool tma_encode_3d(CUtensorMap* map, const void* base, bool f32, long long L, long long rows, long long batch,
                    int box_l, int box_rows);
 
+// Stream-ordered scratch of the time-split passes (defined in sscan_abi.cu):
+// from a per-device pool of this library that keeps up to
+// kScratchRetainBytes mapped while idle, so that a call after a host
+// synchronisation does not map its scratch again.
+constexpr unsigned long long kScratchRetainBytes = 1ull << 30;
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream);
+
 // A launch plan of the forward pass (defined in sscan_abi.cu).
 struct FwdPlan {
     Shape sh;
