@@ -273,9 +273,7 @@ int cached_tma_occupancy(bool f32, Shape sh, int variant) {
 // channels: (4,4,2) unsplit 187 us, (8,2,2) 207 us).
 // Otherwise the shape is the one with the most channels per lane whose
 // segments stay at least 16 chunks long ((4,4,2)), else (8,2,2).  The
-// carry correction runs on the cp.async kernel, shape (4,4,1) (measured on
-// GB300: dim512 50.3 / 51.2 / 55.3 us with (4,4,1) / (8,2,1) / (2,8,1);
-// long64k 535 / 559 / 568 us).
+// carry correction's shape is chosen below.
 int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long long seqlen, long long N,
                  int segments, int lanes, FwdPlan* out) {
     if (N <= 8 || N > 64 || (N > 16 && N <= 32)) return SSCAN_ERR_INVALID;
@@ -331,8 +329,11 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
     // make long decay horizons) on the TMA-fed kernel, shape (4,4,2); for short
     // ones on the cp.async kernel, shape (8,2,1), whose smaller CTAs start and
     // stop sooner (measured on GB300: 512 channels x 8192 steps in 19 segments
-    // 47.1 / 49.2 / 53.2 us with (8,2,1) / TMA (8,2,2) / TMA (4,4,2);
-    // 1536 x 65536 in 19 segments 554 / 548 / 509 us)
+    // 47.1 / 49.2 / 53.2 us with (8,2,1) / TMA (8,2,2) / TMA (4,4,2), and
+    // 46.9 / 49.0 / 51.0 us with (8,2,1) / (4,4,1) / (2,8,1), whose fewer
+    // lanes per channel let decayed states drop out sooner but give fewer
+    // warps; 1536 x 65536 in 19 segments 554 / 548 / 509 us with the first
+    // three, 531 / 557 us with (4,4,1) / (2,8,1))
     best.corr_tma = best.S > 1 && (wide || best.Tseg >= 32 * TC);
     best.corr_sh = wide ? Shape{4, 16, 2} : best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
     best.corr_tiles_per_batch = ceil_div(dim, best.corr_tma ? tma_channels(best.corr_sh) : shape_channels(best.corr_sh));
