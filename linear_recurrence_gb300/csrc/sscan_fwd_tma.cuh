@@ -38,6 +38,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "../../include/sscan.h"
 #include "sscan_dispatch.cuh"
 #include "sscan_fwd_kernel.cuh"
@@ -80,11 +82,18 @@ struct TmaCfg {
     // pieces of consecutive rows) and take no pad, which keeps the wide-state
     // CTA within half an SM's shared memory
     static constexpr int RROW = Base::kF32 ? Base::RROW : TC;
+    // bf16 with 64 state slots (plain scan): the lanes read their u/delta
+    // rows straight from the raw stage (converting 4 values per read), which
+    // saves the per-warp fp32 copy and buys a third widened B/C slot; those
+    // raw rows keep the 16-byte pad, so that the 8 channel rows a warp reads
+    // at one step fall in distinct banks
+    static constexpr bool kRawU = !Base::kF32 && NS > 4 && OPT_ == 0;
+    static constexpr int RROW_U = kRawU ? Base::RROW : RROW;  // raw u/delta (z) row
     static constexpr int FROW = Base::FROW;  // fp32 row: TC + 4
     static constexpr bool kF32 = Base::kF32;
     static constexpr int STAGES = kTmaStages;
     static constexpr int ESZ = (int)sizeof(T);
-    static constexpr int U_BOX = CPW * RROW * ESZ;   // bytes of one u (delta, z) box
+    static constexpr int U_BOX = CPW * RROW_U * ESZ;  // bytes of one u (delta, z) box
     static constexpr int BC_BOX = NSP * RROW * ESZ;  // bytes of one B (or C) box
     static constexpr int U_SLOT = align_up(U_BOX, 128);
     static constexpr int BC_SLOT = align_up(BC_BOX, 128);
@@ -100,7 +109,7 @@ struct TmaCfg {
     // chunk's B/C rows are widened once per CTA into a ring of WB slots
     // [B NSP][C NSP]
     static constexpr int WORK_ROWS = NUR * CPW;
-    static constexpr int WB = NS > 4 ? 2 : 3;  // two slots for wide states (shared memory)
+    static constexpr int WB = NS > 4 && !kRawU ? 2 : 3;  // two slots where shared memory is short
     static constexpr int BCW_BYTES = kF32 ? 0 : 2 * NSP * FROW * 4;
     // items of the warp epilogue per half chunk: (channel row, 4 steps); per lane
     static constexpr int IPH = CPW * (TS / 4) / 32;
@@ -112,7 +121,7 @@ struct TmaCfg {
     static constexpr int OFF_BC = OFF_U + STAGES * kWarps * NUR * U_SLOT;  // [STAGES][B, C] slots
     static constexpr int OFF_BCW = OFF_BC + STAGES * 2 * BC_SLOT;
     static constexpr int OFF_WORK = OFF_BCW + WB * BCW_BYTES;
-    static constexpr int WORK_BYTES = kF32 ? 0 : WORK_ROWS * FROW * 4;  // per warp
+    static constexpr int WORK_BYTES = kF32 || kRawU ? 0 : WORK_ROWS * FROW * 4;  // per warp
     static constexpr int OFF_YP = OFF_WORK + kWarps * WORK_BYTES;
     static constexpr int YP_BYTES = CPW * RS * 4;  // per warp
     static constexpr int SMEM_BYTES = OFF_YP + kWarps * YP_BYTES + 128;  // + base alignment
@@ -123,8 +132,8 @@ struct TmaCfg {
     // chunk whose B/C copy was issued
     static constexpr int OFF_BCW_BAR = align_up((kWarps + 1) * STAGES * 8 + STAGES * 4 + 4, 8);
     static_assert(OFF_BCW_BAR + 2 * WB * 8 <= 1024, "barrier area");
-    static_assert(RROW * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
-    static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256, "tensor-map box limits");
+    static_assert(RROW * ESZ % 16 == 0 && RROW_U * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
+    static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256 && RROW_U <= 256, "tensor-map box limits");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -138,8 +147,8 @@ struct TmaCfg {
 // outputs of each channel go to yp[rl[j]][g] (row stride RS, lane stride
 // HROW) as one vector.  SCALAR: one decay rate per channel.  ZOH: the
 // zero-order-hold B-bar ((exp(delta A) - 1)/A per unit B) replaces delta*B.
-template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
-__device__ __forceinline__ void compute_half_narrow(const float* su, const float* sd, const float* sB,
+template <typename TU, int UROW, int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
+__device__ __forceinline__ void compute_half_narrow(const TU* su, const TU* sd, const float* sB,
                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
                                                  int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
                                                  const float (&invA)[CPL][NS], const float (&invAs)[CPL],
@@ -151,8 +160,8 @@ __device__ __forceinline__ void compute_half_narrow(const float* su, const float
     auto load_block = [&](int t4) {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            load4_smem(su + rl[j] * FROW + t4, nu[j]);
-            load4_smem(sd + rl[j] * FROW + t4, nd[j]);
+            load4_smem(su + rl[j] * UROW + t4, nu[j]);
+            load4_smem(sd + rl[j] * UROW + t4, nd[j]);
         }
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
@@ -214,8 +223,8 @@ __device__ __forceinline__ void compute_half_narrow(const float* su, const float
 // As compute_half_narrow for wide lanes (NS > 4 states): the u/delta vectors
 // are read one block ahead; the B/C vectors are read per quad of states inside
 // the block (all of them at once would need 8*NS registers).
-template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
-__device__ __forceinline__ void compute_half_wide(const float* su, const float* sd, const float* sB,
+template <typename TU, int UROW, int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
+__device__ __forceinline__ void compute_half_wide(const TU* su, const TU* sd, const float* sB,
                                                   const float* sC, float* yp, const int (&rl)[CPL], int g,
                                                   int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
                                                   const float (&invA)[CPL][NS], const float (&invAs)[CPL],
@@ -229,8 +238,8 @@ __device__ __forceinline__ void compute_half_wide(const float* su, const float* 
     auto load_block = [&](int t4) {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            load4_smem(su + rl[j] * FROW + t4, nu[j]);
-            load4_smem(sd + rl[j] * FROW + t4, nd[j]);
+            load4_smem(su + rl[j] * UROW + t4, nu[j]);
+            load4_smem(sd + rl[j] * UROW + t4, nd[j]);
         }
     };
     load_block(T0);
@@ -286,17 +295,17 @@ __device__ __forceinline__ void compute_half_wide(const float* su, const float* 
     }
 }
 
-template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
-__device__ __forceinline__ void compute_half_tma(const float* su, const float* sd, const float* sB,
+template <typename TU, int UROW, int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR, bool ZOH>
+__device__ __forceinline__ void compute_half_tma(const TU* su, const TU* sd, const float* sB,
                                                  const float* sC, float* yp, const int (&rl)[CPL], int g,
                                                  int T0, const float (&Al2)[CPL][NS], const float (&As)[CPL],
                                                  const float (&invA)[CPL][NS], const float (&invAs)[CPL],
                                                  float (&h)[CPL][NS]) {
     if constexpr (NS <= 4)
-        compute_half_narrow<NS, P, CPL, FROW, RS, HROW, TS, SCALAR, ZOH>(su, sd, sB, sC, yp, rl, g, T0, Al2, As,
+        compute_half_narrow<TU, UROW, NS, P, CPL, FROW, RS, HROW, TS, SCALAR, ZOH>(su, sd, sB, sC, yp, rl, g, T0, Al2, As,
                                                                          invA, invAs, h);
     else
-        compute_half_wide<NS, P, CPL, FROW, RS, HROW, TS, SCALAR, ZOH>(su, sd, sB, sC, yp, rl, g, T0, Al2, As,
+        compute_half_wide<TU, UROW, NS, P, CPL, FROW, RS, HROW, TS, SCALAR, ZOH>(su, sd, sB, sC, yp, rl, g, T0, Al2, As,
                                                                        invA, invAs, h);
 }
 
@@ -305,8 +314,8 @@ __device__ __forceinline__ void compute_half_tma(const float* su, const float* s
 // C-contraction, stored as partial outputs like compute_half_tma.  live[k]
 // (warp-uniform) skips the state slots whose carry has decayed below the
 // threshold in every lane of the warp.
-template <int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR>
-__device__ __forceinline__ void decay_half_tma(const float* sd, const float* sC, float* yp, const int (&rl)[CPL],
+template <typename TU, int UROW, int NS, int P, int CPL, int FROW, int RS, int HROW, int TS, bool SCALAR>
+__device__ __forceinline__ void decay_half_tma(const TU* sd, const float* sC, float* yp, const int (&rl)[CPL],
                                                int g, int T0, const float (&Al2)[CPL][NS],
                                                const float (&As)[CPL], const bool (&live)[NS],
                                                float (&h)[CPL][NS]) {
@@ -316,7 +325,7 @@ __device__ __forceinline__ void decay_half_tma(const float* sd, const float* sC,
         float dd[CPL][4], as[CPL][4], y[CPL][4];
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            load4_smem(sd + rl[j] * FROW + t4, dd[j]);
+            load4_smem(sd + rl[j] * UROW + t4, dd[j]);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
@@ -386,6 +395,10 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     constexpr int NUR = Cfg::NUR;
     constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
     constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW, RS = Cfg::RS, STAGES = Cfg::STAGES;
+    // the lanes' u/delta rows: fp32 (own or widened) rows, or raw bf16 ones
+    constexpr bool kRawU = Cfg::kRawU;
+    using UT = typename std::conditional<kRawU, bf16, float>::type;
+    constexpr int UROW = kRawU ? Cfg::RROW_U : FROW;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(16) unsigned char smem_dyn[];
     // 128-byte aligned base, offset from the shared array itself so that the
@@ -568,7 +581,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
 
     // warp epilogue of one half chunk: sum the P partials, add D*u, store 4
     // steps per item (and the Kahan sums of delta of a local pass)
-    auto epilogue = [&](int half, long long t0, const float* su, const float* sd, const float* sz) {
+    auto epilogue = [&](int half, long long t0, const UT* su, const UT* sd, const float* sz) {
 #pragma unroll
         for (int k = 0; k < Cfg::IPH; ++k) {
             const int q = lane + 32 * k;
@@ -584,7 +597,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
                 for (int e = 0; e < 4; ++e) v[e] += x[e];
             }
             float uv[4];
-            load4_smem(su + r * FROW + t4, uv);
+            load4_smem(su + r * UROW + t4, uv);
             if constexpr (!CORR) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) v[e] = fmaf(Dr[k], uv[e], v[e]);
@@ -601,7 +614,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
             }
             if (dsum_on) {  // steps past the segment hold delta = 0
                 float dv[4];
-                load4_smem(sd + r * FROW + t4, dv);
+                load4_smem(sd + r * UROW + t4, dv);
                 const float yk = ((dv[0] + dv[1]) + (dv[2] + dv[3])) - dcomp[k];
                 const float tk = dsum[k] + yk;
                 dcomp[k] = (tk - dsum[k]) - yk;
@@ -653,14 +666,15 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         const unsigned par = (unsigned)(i / STAGES) & 1u;
         const int nx = i + STAGES;  // the chunk that refills this stage
         const long long t0 = t_begin + (long long)i * TC;
-        const float *su, *sd, *sz, *sB, *sC;
+        const UT *su, *sd;
+        const float *sz, *sB, *sC;
         if constexpr (Cfg::kF32) {
             ok = mbar_wait_bounded(barU + w * STAGES + st, par);
             ok = mbar_wait_bounded(barBC + st, par) && ok;
             ok = __all_sync(FULL, ok);
             if (!ok && !CORR) break;
-            su = reinterpret_cast<const float*>(u_slot(st));
-            sd = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
+            su = reinterpret_cast<const UT*>(u_slot(st));
+            sd = reinterpret_cast<const UT*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
             sz = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + 2 * Cfg::U_SLOT);
             sB = reinterpret_cast<const float*>(bc_slot(st));
             sC = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(sB) + Cfg::BC_SLOT);
@@ -678,6 +692,23 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
                 }
                 __syncwarp();
             }
+        } else if constexpr (kRawU) {
+            // the next chunk's B/C when it is this warp's turn, one chunk ahead
+            if (i + 1 < nchunks && (i + 1) % kWarps == w && !widen_bc(i + 1)) {
+                ok = false;
+                if constexpr (!CORR) break;
+            }
+            // the warp's raw u/delta rows, read in place; the stage is
+            // refilled after the chunk
+            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par)) && ok;
+            if (!ok && !CORR) break;
+            su = reinterpret_cast<const UT*>(u_slot(st));
+            sd = reinterpret_cast<const UT*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
+            sz = nullptr;
+            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u)) && ok;
+            if (!ok && !CORR) break;
+            sB = reinterpret_cast<const float*>(sbase + Cfg::OFF_BCW + (i % Cfg::WB) * Cfg::BCW_BYTES);
+            sC = sB + NSP * FROW;
         } else {
             // the next chunk's B/C when it is this warp's turn, one chunk ahead
             if (i + 1 < nchunks && (i + 1) % kWarps == w && !widen_bc(i + 1)) {
@@ -735,16 +766,16 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
         for (int half = 0; half < 2; ++half) {
             if constexpr (CORR) {
                 if (scalar)
-                    decay_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true>(sd, sC, yp, rl, g, half * TS, Al2, As, live,
+                    decay_half_tma<UT, UROW, NS, P, CPL, FROW, RS, HROW, TS, true>(sd, sC, yp, rl, g, half * TS, Al2, As, live,
                                                                          h);
                 else
-                    decay_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false>(sd, sC, yp, rl, g, half * TS, Al2, As,
+                    decay_half_tma<UT, UROW, NS, P, CPL, FROW, RS, HROW, TS, false>(sd, sC, yp, rl, g, half * TS, Al2, As,
                                                                           live, h);
             } else if (scalar) {
-                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, true, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
+                compute_half_tma<UT, UROW, NS, P, CPL, FROW, RS, HROW, TS, true, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
                                                                             Al2, As, invA, invAs, h);
             } else {
-                compute_half_tma<NS, P, CPL, FROW, RS, HROW, TS, false, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
+                compute_half_tma<UT, UROW, NS, P, CPL, FROW, RS, HROW, TS, false, ZOH>(su, sd, sB, sC, yp, rl, g, half * TS,
                                                                              Al2, As, invA, invAs, h);
             }
             __syncwarp();
@@ -760,7 +791,7 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
             epilogue(half, t0, su, sd, sz);
             __syncwarp();
         }
-        if constexpr (Cfg::kF32) {
+        if constexpr (Cfg::kF32 || kRawU) {
             // u/delta (z) of this stage are no longer read by this warp; the
             // delta transform wrote them, so order those writes before the copy
             if (lane == 0 && nx < nchunks) {
@@ -835,12 +866,12 @@ cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream
     TmaMaps tm;
     const bool f32 = Cfg::kF32;
     // a correction stages the local outputs where a local pass stages u
-    if (!tma_encode_3d(&tm.u, corr ? p.out : p.u, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
-        !tma_encode_3d(&tm.delta, p.delta, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW) ||
+    if (!tma_encode_3d(&tm.u, corr ? p.out : p.u, f32, p.L, p.dim, p.batch, Cfg::RROW_U, Cfg::CPW) ||
+        !tma_encode_3d(&tm.delta, p.delta, f32, p.L, p.dim, p.batch, Cfg::RROW_U, Cfg::CPW) ||
         !tma_encode_3d(&tm.B, p.B, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP) ||
         !tma_encode_3d(&tm.C, p.C, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP))
         return cudaErrorInvalidValue;
-    if (OPT > 0 && p.z != nullptr && !tma_encode_3d(&tm.z, p.z, f32, p.L, p.dim, p.batch, Cfg::RROW, Cfg::CPW))
+    if (OPT > 0 && p.z != nullptr && !tma_encode_3d(&tm.z, p.z, f32, p.L, p.dim, p.batch, Cfg::RROW_U, Cfg::CPW))
         return cudaErrorInvalidValue;
     auto kern = corr ? sscan_fwd_tma<T, NS, P, CPL, OPT, true> : sscan_fwd_tma<T, NS, P, CPL, OPT, false>;
     static unsigned long long configured[2] = {0, 0};  // bit per device ordinal (< 64), per kernel
