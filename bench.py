@@ -12,7 +12,11 @@ ranks (every rank runs its own copy of the workload: weak scaling).
 
 ``e2e`` is the same metric through the public Python call with pinned host
 buffers: per step the inputs are copied host->device, the scan runs, and the
-output and final state are copied back, all inside the timed region.
+output and final state are copied back, all inside the timed region.  Steps
+follow one another on three streams (copy in, compute, copy out) with two
+buffer sets, so that one step's inputs travel while the previous step's
+outputs come back; ``e2e.serial_value`` is the same with every step's copies
+and call in order on one stream.
 
 ``--impl reference`` times the double-precision CPU oracle (the reference
 implementation of this build) on the host cores, on a bounded channel sample
@@ -297,9 +301,68 @@ def bench_workload(w, steps, warmup, dev, stream, flush, e2e=False):
                 out_h.copy_(y, non_blocking=True)
                 fs_h.copy_(hT, non_blocking=True)
 
-        te, _, _ = time_device(e2e_step, max(3, steps // 2), 2, flush, stream)
-        res.update({"t_e2e": te, "h2d": h2d, "d2h": d2h})
+        te_serial, _, _ = time_device(e2e_step, max(3, steps // 2), 2, flush, stream)
+        te = time_e2e_pipelined(x, g, steps, warmup, dev, stream)
+        res.update({"t_e2e": te, "t_e2e_serial": te_serial, "h2d": h2d, "d2h": d2h})
     return res
+
+
+def time_e2e_pipelined(x, g, steps, warmup, dev, stream):
+    """Seconds per step of a stream of sscan_fwd calls fed from pinned host
+    memory: every step copies all its inputs host->device, runs the call and
+    copies y and the final state back, on three streams (copy in, compute,
+    copy out) with two buffer sets, so that step k+1's inputs travel while
+    step k's outputs come back (the link carries both directions at once).
+    Timed with CUDA events from the first copy to the last copy out."""
+    import torch
+    import linear_recurrence_gb300 as lr
+    host = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+    sets = []
+    for _ in range(2):
+        dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in x.items()}
+        out = torch.empty_like(g["u"])
+        fs = torch.empty((g["u"].shape[0], g["u"].shape[1], g["A"].shape[1]), dtype=torch.float32, device=dev)
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        ev = {n: torch.cuda.Event() for n in ("in_ready", "done", "out_read")}
+        sets.append((dbuf, out, fs, out_h, fs_h, ev))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    used = [False, False]
+
+    def step(k):
+        i = k % 2
+        dbuf, out, fs, out_h, fs_h, ev = sets[i]
+        with torch.cuda.stream(s_in):
+            if used[i]:
+                s_in.wait_event(ev["done"])      # step k-2 no longer reads these inputs
+            for n, v in host.items():
+                if v is not None:
+                    dbuf[n].copy_(v, non_blocking=True)
+            ev["in_ready"].record(s_in)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev["in_ready"])
+            if used[i]:
+                stream.wait_event(ev["out_read"])  # step k-2's outputs have left
+            lr.sscan_fwd(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
+                         dbuf["h0"], out=out, final_state=fs, stream=stream)
+            ev["done"].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"])
+            out_h.copy_(out, non_blocking=True)
+            fs_h.copy_(fs, non_blocking=True)
+            ev["out_read"].record(s_out)
+        used[i] = True
+
+    for k in range(max(warmup, 2)):
+        step(k)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for k in range(steps):
+        step(k)
+    end.record(s_out)  # after every copy out, hence after every step's work
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) * 1e-3 / steps
 
 
 def bench_fused(w, steps, warmup, dev, stream, flush, pk):
@@ -537,7 +600,9 @@ def main():
                 "roofline": rf,
                 "cpu_baseline": cpu,
                 "e2e": {"value": ws * w.channels * w.L / te, "unit": UNIT,
-                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                        "pipelining": "copy-in, compute and copy-out streams, two buffer sets",
+                        "serial_value": ws * w.channels * w.L / max_over_ranks(res["t_e2e_serial"], ws, dev)},
                 "gpu_launches": res["launches"],
                 "clocks": clk.summary()}
         line.update(extra)
