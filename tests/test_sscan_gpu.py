@@ -135,6 +135,8 @@ TMA_CASES = [
     (4, 17, 8, 16, 8, 0, True, True),       # a partial first chunk only
     (1, 40, 4096, 16, 4, 3, True, True),    # long segments: the correction on the TMA kernel
     (2, 24, 3200, 12, 8, 2, True, False),   # the same with a short last segment, no h0
+    (2, 72, 1000, 64, 4, 0, True, True),    # 64 state slots: ragged tile and tail chunk
+    (1, 40, 3000, 50, 4, 3, True, False),   # 50 of 64 slots, time split: the wide correction
 ]
 
 
