@@ -113,6 +113,12 @@ struct TmaCfg {
     static constexpr int BCW_BYTES = kF32 ? 0 : 2 * NSP * FROW * 4;
     // items of the warp epilogue per half chunk: (channel row, 4 steps); per lane
     static constexpr int IPH = CPW * (TS / 4) / 32;
+    // resident CTAs per SM the register allocation is asked to allow: for the
+    // narrow shapes the number their shared memory allows (without it the
+    // compiler kept to 96 registers; measured on GB300: dim512 47.0 -> 46.1
+    // us, bf16_2k 131.6 -> 129.8, long64k 506.5 -> 501.2); wide lanes take
+    // no such request (sscan_fwd_tma_wide)
+    static constexpr int MIN_BLOCKS = NS > 4 ? 1 : P == 4 ? 3 : 4;
     // shared-memory map (bytes from a 128-byte aligned base)
     // mbarriers [kWarps + 1][STAGES], counters [STAGES], then (bf16) the
     // widened ring's full [WB] and empty [WB] mbarriers
@@ -387,10 +393,10 @@ __device__ __forceinline__ void widen_delta_rows_warp(const bf16* src, float* ds
 
 // CORR: the carry-correction instantiation (MODE_CORR: segment s >= 1 adds
 // the decaying contribution of its entry state to the local outputs; the u
-// tensor map then covers those outputs).
+// tensor map then covers those outputs).  The body of the kernels below; tm
+// is their __grid_constant__ parameter.
 template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
-__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
-    sscan_fwd_tma(const FwdParams p, const __grid_constant__ TmaMaps tm) {
+__device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const TmaMaps& tm) {
     using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
     constexpr int NUR = Cfg::NUR;
     constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
@@ -856,6 +862,30 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     }
 }
 
+// Narrow lanes (up to 4 states): the register allocation is asked for the
+// resident CTAs that shared memory allows (TmaCfg::MIN_BLOCKS).
+template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
+__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads, TmaCfg<T, NS, P, CPL, OPT>::MIN_BLOCKS)
+    sscan_fwd_tma(const FwdParams p, const __grid_constant__ TmaMaps tm) {
+    sscan_fwd_tma_body<T, NS, P, CPL, OPT, CORR>(p, tm);
+}
+
+// Wide lanes (16 states): no such request; every one tried (two or three
+// CTAs per SM) gave a slower schedule at the same or more registers
+// (wide64 458 / 462 us against 452 us).
+template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
+__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
+    sscan_fwd_tma_wide(const FwdParams p, const __grid_constant__ TmaMaps tm) {
+    sscan_fwd_tma_body<T, NS, P, CPL, OPT, CORR>(p, tm);
+}
+
+// The kernel of a shape and pass.
+template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
+constexpr auto tma_kernel() {
+    if constexpr (NS > 4) return sscan_fwd_tma_wide<T, NS, P, CPL, OPT, CORR>;
+    else return sscan_fwd_tma<T, NS, P, CPL, OPT, CORR>;
+}
+
 // Shared implementation of the per-dtype launch units (sscan_fwd_tma_*.cu).
 #ifdef SSCAN_TMA_IMPL
 template <typename T, int NS, int P, int CPL, int OPT>
@@ -873,7 +903,7 @@ cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream
         return cudaErrorInvalidValue;
     if (OPT > 0 && p.z != nullptr && !tma_encode_3d(&tm.z, p.z, f32, p.L, p.dim, p.batch, Cfg::RROW_U, Cfg::CPW))
         return cudaErrorInvalidValue;
-    auto kern = corr ? sscan_fwd_tma<T, NS, P, CPL, OPT, true> : sscan_fwd_tma<T, NS, P, CPL, OPT, false>;
+    auto kern = corr ? tma_kernel<T, NS, P, CPL, OPT, true>() : tma_kernel<T, NS, P, CPL, OPT, false>();
     static unsigned long long configured[2] = {0, 0};  // bit per device ordinal (< 64), per kernel
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -906,7 +936,7 @@ cudaError_t launch_tma_variant(const FwdParams& p, int grid, cudaStream_t stream
 template <typename T, int NS, int P, int CPL, int OPT>
 int occupancy_tma_variant() {
     using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
-    auto kern = sscan_fwd_tma<T, NS, P, CPL, OPT, false>;
+    auto kern = tma_kernel<T, NS, P, CPL, OPT, false>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;
