@@ -18,9 +18,9 @@ buffer sets, so that one step's inputs travel while the previous step's
 outputs come back; ``e2e.serial_value`` is the same with every step's copies
 and call in order on one stream.
 
-``--impl reference`` times the double-precision CPU oracle (the reference
-implementation of this build) on the host cores, on a bounded channel sample
-of the same workload; only rank 0 runs it.
+``--impl reference`` times the double-precision CPU oracle (the plain
+sequential definition the GPU path is checked against) on the host cores, on
+a bounded channel sample of the same workload; only rank 0 runs it.
 """
 from __future__ import annotations
 
