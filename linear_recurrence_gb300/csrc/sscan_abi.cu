@@ -259,16 +259,17 @@ int cached_tma_occupancy(bool f32, Shape sh, int variant) {
     return v;
 }
 
-// Plan of the TMA-fed kernel for 8 < N <= 16 (its shapes hold 16 state
-// slots), or SSCAN_ERR_INVALID when it does not apply.  A time split fills at
-// most one wave of the GPU's resident CTA slots and keeps segments of about
-// 14 chunks or more: every segment beyond the first adds a carry correction over the
-// decay horizon of its entry state (a few chunks for typical step sizes), so
-// shorter segments cost more in corrections than they gain in local-pass
-// parallelism (measured on GB300 with 512 channels x 8192 steps: 16, 18, 19
-// and 26 segments 55, 53, 51 and 58 us; 1536 x 65536: 12 segments 603 us,
-// 19 segments 575 us, on an earlier build).  A problem wide enough to give (4,4,2), else (8,2,2),
-// 6 warps per SM runs unsplit on that shape (8192 fp32 channels x 2048 steps:
+// Plan of the TMA-fed kernel for 8 < N <= 16 (shapes of 16 state slots) or
+// 32 < N <= 64 (shape (4,16,2), 64 slots), or SSCAN_ERR_INVALID when it does
+// not apply.  A time split fills at most one wave of the GPU's resident CTA
+// slots and keeps segments of about 14 chunks or more: every segment beyond
+// the first adds a carry correction over the decay horizon of its entry state
+// (a few chunks for typical step sizes), so shorter segments cost more in
+// corrections than they gain in local-pass parallelism (measured on GB300 with
+// 512 channels x 8192 steps: 16, 19, 21 and 23 segments 48.8, 46.1, 52.8 and
+// 56.4 us; 1536 x 65536: 16, 19, 22 and 25 segments 576, 501, 731 and 615
+// us).  A problem wide enough to give (4,4,2), else (8,2,2), 6 warps per SM
+// runs unsplit on that shape (8192 fp32 channels x 2048 steps:
 // (8,2,2) unsplit 123 us, (4,4,2) in 2 or 3 segments 130 / 148 us; 16384
 // channels: (4,4,2) unsplit 187 us, (8,2,2) 207 us).
 // Otherwise the shape is the one with the most channels per lane whose
@@ -423,8 +424,8 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     const int vece = 16 / esz;
     const bool vec = (seqlen % vece) == 0 && aligned16(u) && aligned16(delta) && aligned16(B) &&
                      aligned16(C) && aligned16(out) && (z == nullptr || aligned16(z));
-    // the TMA-fed kernel takes the single or local pass when the tensor-map
-    // rules hold (16-byte aligned rows, coordinates below 2^31)
+    // the TMA-fed kernel takes the pass when the tensor-map rules hold
+    // (16-byte aligned rows, coordinates below 2^31) and it has a shape for N
     const int variant = (flags & SSCAN_ZOH) ? 2 : (z != nullptr || delta_bias != nullptr || flags != 0) ? 1 : 0;
     const long long lim = (1LL << 31) - 256;
     sscan::FwdPlan pl;

@@ -81,9 +81,9 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 // Shapes of the TMA-fed kernel (sscan_fwd_tma.cuh): four warps per CTA, so
 // DT = 4 * (32 / P) * CPL channels per CTA.  It serves the scan (plain or
 // with the options) with 16-byte aligned rows in every mode (single, local,
-// carry correction), for
-// 8 < N <= 16 (measured on GB300: as fast or faster than the cp.async kernel
-// there; slower for wide states, whose B/C ring costs occupancy).
+// carry correction), for 8 < N <= 16 ((8,2,2), (4,4,2)) and 32 < N <= 64
+// ((4,16,2)); the cp.async kernel takes the other state counts (measured on
+// GB300 where both apply: the TMA kernel as fast or faster).
 #ifndef SSCAN_TMA_SHAPES
 #define SSCAN_TMA_SHAPES(X) X(8, 2, 2) X(4, 4, 2) X(4, 16, 2)
 #endif

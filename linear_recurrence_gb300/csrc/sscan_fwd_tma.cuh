@@ -2,9 +2,10 @@
 // rows that satisfy the tensor-map rules (16-byte aligned rows, sizes below
 // 2^31).  It computes exactly what sscan_fwd_chunked computes (the recurrence
 // of "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战" section 2.3
-// with the initial/final state of its section 7.1), for the plain scan in the
-// single-segment and local-segment modes; the carry correction of a time
-// split and the fused options stay with sscan_fwd_chunked.
+// with the initial/final state of its section 7.1), fp32 and bf16, the plain
+// scan and the options (delta bias and softplus, the output gate, the
+// zero-order hold), in the single-segment and local-segment modes and, as its
+// CORR instantiation, the carry correction of a time split.
 //
 // What changes against the cp.async kernel is who waits for whom:
 //   * every warp owns its channels end to end.  Its u/delta rows arrive by
@@ -22,18 +23,21 @@
 //     count needs no fence; the data itself is published by the mbarrier's
 //     transaction count and acquired by its wait;
 //   * bf16: each warp widens its own u/delta rows into fp32 rows, which
-//     frees its raw stage at once; the chunk's B/C rows are widened once per
-//     CTA, by warps in turn (chunk c by warp c mod 4, one chunk ahead), into
-//     a three-slot fp32 ring with a full mbarrier (the widening warp's lanes
-//     arrive) and an empty one (every warp arrives when it is done with the
-//     slot); only the widening warp reads the raw B/C stage, so it refills
-//     that stage itself.
-// fp32 boxes are TC + 16 bytes wide: the extra columns (the next chunk's
-// first steps, or zeros past the end) pad every shared-memory row exactly as
-// the cp.async ring does, so the reads of different rows at one step fall in
-// different banks; bf16 boxes are TC wide (their rows are only widened).  Every mbarrier wait is bounded (about a second); a wait
-// that gives up records SSCAN_ERR_TIMEOUT in the status word, waits (again
-// bounded) for the copies still in flight, and ends the warp's work.
+//     frees its raw stage at once (with 16 states per lane and the plain
+//     scan the lanes read the raw rows instead, converting as they read); the
+//     chunk's B/C rows are widened once per CTA, by warps in turn (chunk c by
+//     warp c mod 4, one chunk ahead), into an fp32 ring of WB slots with a
+//     full mbarrier (the widening warp's lanes arrive) and an empty one (every
+//     warp arrives when it is done with the slot); only the widening warp
+//     reads the raw B/C stage, so it refills that stage itself.
+// fp32 boxes (and the raw bf16 u/delta boxes read in place) are TC + 16 bytes
+// wide: the extra columns (the next chunk's first steps, or zeros past the
+// end) pad every shared-memory row exactly as the cp.async ring does, so the
+// reads of different rows at one step fall in different banks; the other bf16
+// boxes are TC wide (their rows are only widened).  Every mbarrier wait is
+// bounded (about a second); a wait that gives up records SSCAN_ERR_TIMEOUT in
+// the status word, waits (again bounded) for the copies still in flight, and
+// ends the warp's work.
 #pragma once
 
 #include <cuda.h>
