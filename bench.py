@@ -307,13 +307,15 @@ def bench_workload(w, steps, warmup, dev, stream, flush, e2e=False):
     return res
 
 
-def time_e2e_pipelined(x, g, steps, warmup, dev, stream):
+def time_e2e_pipelined(x, g, steps, warmup, dev, stream, outputs=None):
     """Seconds per step of a stream of sscan_fwd calls fed from pinned host
     memory: every step copies all its inputs host->device, runs the call and
     copies y and the final state back, on three streams (copy in, compute,
     copy out) with two buffer sets, so that step k+1's inputs travel while
     step k's outputs come back (the link carries both directions at once).
-    Timed with CUDA events from the first copy to the last copy out."""
+    Timed with CUDA events from the first copy to the last copy out.  A dict
+    passed as ``outputs`` receives the host copies of the last step's y and
+    final state."""
     import torch
     import linear_recurrence_gb300 as lr
     host = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
@@ -362,6 +364,9 @@ def time_e2e_pipelined(x, g, steps, warmup, dev, stream):
         step(k)
     end.record(s_out)  # after every copy out, hence after every step's work
     torch.cuda.synchronize()
+    if outputs is not None:
+        last = sets[(steps - 1) % 2]
+        outputs["y"], outputs["final_state"] = last[3], last[4]
     return start.elapsed_time(end) * 1e-3 / steps
 
 

@@ -357,3 +357,21 @@ def test_workload_full_size_sampled(lr, name):
     ey, eh = _rel_err(ys, yr), _rel_err(hs, hr)
     assert ey <= TOL[w.dtype] and eh <= TOL[w.dtype], f"{name} [{plan}]: {ey:.3e} {eh:.3e}"
     assert np.all(np.isfinite(y))
+
+
+def test_pipelined_end_to_end_steps_return_the_scan(lr):
+    """The benchmark's end-to-end leg (each step copies its inputs in from
+    pinned host memory, runs the call and copies y and the final state back,
+    on three streams with two buffer sets) returns exactly what one direct call
+    computes, on a time-split workload."""
+    import bench
+    w = workloads.WORKLOADS["dim512"].scaled(dim=96, L=2048)
+    x = workloads.make_inputs(w)
+    g = _dev(x)
+    got = {}
+    bench.time_e2e_pipelined(x, g, 5, 2, torch.device("cuda"), torch.cuda.current_stream(), outputs=got)
+    y, hT = lr.sscan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["h0"])
+    torch.cuda.synchronize()
+    assert lr.get_last_error() == 0
+    assert torch.equal(got["y"], y.cpu()) and torch.equal(got["final_state"], hT.cpu())
+
