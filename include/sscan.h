@@ -227,6 +227,23 @@ const char *sscan_status_string(int status);
  * Clears the recorded error. */
 int sscan_get_last_error(void);
 
+/*
+ * sscan_debug_expire_next_wait -- a test aid for the timeout path of the
+ * error contract above; the pages have no counterpart.  It arms the calling
+ * thread's next sscan_fwd / sscan_fwd_ex / sscan_fwd_fused call.  If that
+ * call's first pass runs on the TMA-fed kernels (16-byte aligned rows and a
+ * dstate they serve), the barrier of the first B/C ring stage of each of its
+ * CTAs is made to expect 16 bytes that no copy delivers, and every bounded
+ * wait of that pass gives up after wait_limit_us microseconds (instead of
+ * about a second).  The waits on that stage then run out as a real stall
+ * would: the kernel waits (bounded) for the copies it still has in flight,
+ * records SSCAN_ERR_TIMEOUT in the device status word and ends, and
+ * sscan_get_last_error() reports SSCAN_ERR_TIMEOUT.  No fault is involved and
+ * the context stays usable; the outputs of that call are undefined.  The
+ * next call consumes the setting whichever kernel it runs; 0 disarms it.
+ */
+void sscan_debug_expire_next_wait(unsigned int wait_limit_us);
+
 /* Largest dstate that sscan_fwd accepts. */
 int sscan_max_dstate(void);
 

@@ -49,6 +49,7 @@ SIGNATURES = {
     "sscan_status_string": (ctypes.c_char_p, [_int]),
     "sscan_get_last_error": (_int, []),
     "sscan_max_dstate": (_int, []),
+    "sscan_debug_expire_next_wait": (None, [ctypes.c_uint]),
     "sscan_last_launch_count": (_int, []),
     "sscan_last_plan": (ctypes.c_char_p, []),
 }
@@ -98,6 +99,12 @@ def get_last_error() -> int:
 
 def max_dstate() -> int:
     return int(lib().sscan_max_dstate())
+
+
+def debug_expire_next_wait(wait_limit_us: int) -> None:
+    """Test aid: make the bounded waits of this thread's next forward call
+    run out after ``wait_limit_us`` (see include/sscan.h)."""
+    lib().sscan_debug_expire_next_wait(int(wait_limit_us))
 
 
 def last_launch_count() -> int:

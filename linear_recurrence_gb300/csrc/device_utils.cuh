@@ -115,16 +115,22 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 // Wait for the phase with the given parity to complete; gives up (returns
-// false) after about a second of wall time, so that a wait that can never end
-// cannot hang the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+// false) after limit_ns of wall time (about a second by default), so that a
+// wait that can never end cannot hang the GPU.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - start > 1000000000ull) return false;
+        if (global_ns() - start > limit_ns) return false;
         __nanosleep(64);
     }
+}
+// Raise the transaction bytes the current phase expects, without an arrival.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
 }
 // One box of a tiled tensor map (3-D coordinates: innermost first) into
 // shared memory, completing on bar.  The tensor map must live in constant or

@@ -27,6 +27,10 @@ struct CallRecord {
     char plan[256] = "none";
 };
 thread_local CallRecord g_rec;
+// sscan_debug_expire_next_wait: the bound (microseconds) of the waits of this
+// thread's next forward call, whose first B/C stage is made to never complete
+// (0: not armed)
+thread_local unsigned g_expire_wait_us = 0;
 
 int sm_count() {
     static std::atomic<int> cached[64] = {};  // per device ordinal; host threads may race
@@ -59,6 +63,15 @@ cudaError_t launch_fwd_tma(bool f32, const FwdParams& p, Shape sh, long long gri
     if (grid <= 0) return cudaSuccess;
     ++g_rec.launches;
     return sscan::fwd_tma_launch(f32, p, sh, (int)grid, st);
+}
+cudaError_t launch_fwd_shfl(bool f32, const FwdParams& p, Shape sh, long long grid, cudaStream_t st) {
+    if (grid <= 0) return cudaSuccess;
+    ++g_rec.launches;
+    return sscan::fwd_shfl_launch(f32, p, sh, (int)grid, st);
+}
+cudaError_t launch_fold(const FwdParams& p, cudaStream_t st) {
+    ++g_rec.launches;
+    return sscan::fwd_fold_launch(p, st);
 }
 
 // Device status word of the kernels' bounded waits (SSCAN_OK or
@@ -237,13 +250,17 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
     pl.S = ceil_div(seqlen, pl.Tseg);
     if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
     pl.tma = false;
+    pl.shfl = false;
     pl.corr_sh = pl.sh;
     pl.corr_tma = false;
+    pl.corr_shfl = false;
     pl.corr_tiles_per_batch = pl.tiles_per_batch;
     pl.corr_tiles = pl.tiles;
     *out = pl;
     return SSCAN_OK;
 }
+
+void choose_correction(FwdPlan& best, bool wide, long long batch, long long dim);
 
 // Resident CTAs per SM of a TMA-kernel shape, queried once per device.
 int cached_tma_occupancy(bool f32, Shape sh, int variant) {
@@ -326,6 +343,19 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
         }
     }
     if (!found) return SSCAN_ERR_INVALID;
+    best.shfl = false;
+    choose_correction(best, wide, batch, dim);
+    if (best.corr_tiles * best.S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    *out = best;
+    return SSCAN_OK;
+}
+
+// The carry correction of a TMA-fed plan: for long segments (long sequences,
+// where long memories make long decay horizons) on the TMA-fed kernel, shape
+// (4,4,2) (64 state slots: (4,16,2)); for short ones on the cp.async kernel,
+// shape (8,2,1), whose smaller CTAs start and stop sooner.
+void choose_correction(FwdPlan& best, bool wide, long long batch, long long dim) {
+    const long long TC = kChunkSteps;
     // the correction: for long segments (long sequences, where long memories
     // make long decay horizons) on the TMA-fed kernel, shape (4,4,2); for short
     // ones on the cp.async kernel, shape (8,2,1), whose smaller CTAs start and
@@ -339,8 +369,72 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
     best.corr_sh = wide ? Shape{4, 16, 2} : best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
     best.corr_tiles_per_batch = ceil_div(dim, best.corr_tma ? tma_channels(best.corr_sh) : shape_channels(best.corr_sh));
     best.corr_tiles = batch * best.corr_tiles_per_batch;
-    if (best.corr_tiles * best.S > (1LL << 30)) return SSCAN_ERR_INVALID;
-    *out = best;
+    best.corr_shfl = false;
+}
+
+// Resident CTAs per SM of a shuffle-kernel shape, queried once per device.
+int cached_shfl_occupancy(bool f32, Shape sh) {
+    static std::atomic<int> cache[64][2] = {};  // device, dtype
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::atomic<int>& c = cache[dev & 63][f32 ? 0 : 1];
+    int v = c.load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = fwd_shfl_occupancy(f32, sh);
+        c.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Shortest segment of an automatic plan that takes the shuffle kernel in a
+// time split (measured on GB300: 1536 channels x 65536 steps in 25 segments of
+// 2624 steps 467 us against 510 us on (4,4,2); 512 channels x 8192 steps in
+// 64 segments of 128 steps 55 us against 46 us on (8,2,2)).
+constexpr long long kShflMinAutoSegmentSteps = 1024;
+
+// Shortest automatic segment of a shuffle plan, in chunks.
+#ifndef SSCAN_MIN_SHFL_SEGMENT_CHUNKS
+#define SSCAN_MIN_SHFL_SEGMENT_CHUNKS 2
+#endif
+constexpr long long kMinShflSegmentChunks = SSCAN_MIN_SHFL_SEGMENT_CHUNKS;
+
+// Plan of the shuffle variant of the TMA-fed kernel (plain scan).  Its lanes
+// hold two channels of 8 states each, so a problem has a quarter of the lanes
+// of the (8,2,2) shape: a time split fills one wave of the GPU's resident CTA
+// slots (each segment beyond the first adds a carry correction over the decay
+// horizon of its entry state).
+int plan_fwd_shfl(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
+                  int lanes, long long max_segments, FwdPlan* out) {
+    if (N <= 8 || N > 16) return SSCAN_ERR_INVALID;
+    const Shape sh{2, 8, 2};
+    if (!shfl_has_shape(sh) || (lanes != 0 && lanes != sh.P)) return SSCAN_ERR_INVALID;
+    const int nsm = std::max(sm_count(), 1);
+    const long long TC = kChunkSteps;
+    FwdPlan pl{};
+    pl.sh = sh;
+    pl.tma = true;
+    pl.shfl = true;
+    pl.tiles_per_batch = ceil_div(dim, tma_channels(sh));
+    pl.tiles = batch * pl.tiles_per_batch;
+    if (pl.tiles > (1LL << 30)) return SSCAN_ERR_INVALID;
+    const long long slots = (long long)nsm * std::max(cached_shfl_occupancy(f32, sh), 1);
+    long long S = segments;
+    if (S == 0) {
+        S = pl.tiles >= slots ? 1 : slots / pl.tiles;
+        S = std::min(S, std::max(1LL, seqlen / (kMinShflSegmentChunks * TC)));
+        S = std::min(S, std::max(1LL, max_segments));
+    }
+    S = std::max(1LL, std::min(S, ceil_div(seqlen, TC)));
+    pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
+    pl.S = ceil_div(seqlen, pl.Tseg);
+    if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
+    // the correction runs on the same kernel's correction instantiation
+    pl.corr_tma = pl.S > 1;
+    pl.corr_shfl = pl.S > 1;
+    pl.corr_sh = sh;
+    pl.corr_tiles_per_batch = pl.tiles_per_batch;
+    pl.corr_tiles = pl.tiles;
+    *out = pl;
     return SSCAN_OK;
 }
 }  // namespace sscan
@@ -358,6 +452,8 @@ const char* sscan_status_string(int status) {
 }
 
 int sscan_max_dstate(void) { return sscan::kMaxDstate; }
+
+void sscan_debug_expire_next_wait(unsigned int wait_limit_us) { g_expire_wait_us = wait_limit_us; }
 
 int sscan_last_launch_count(void) { return g_rec.launches; }
 
@@ -429,8 +525,18 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     const int variant = (flags & SSCAN_ZOH) ? 2 : (z != nullptr || delta_bias != nullptr || flags != 0) ? 1 : 0;
     const long long lim = (1LL << 31) - 256;
     sscan::FwdPlan pl;
-    bool use_tma = vec && seqlen < lim && dim < lim && batch < lim &&
-                   sscan::plan_fwd_tma(f32, variant, batch, dim, seqlen, dstate, segments, lanes, &pl) == SSCAN_OK;
+    const bool tma_ok = vec && seqlen < lim && dim < lim && batch < lim;
+    // the plain scan on the shuffle variant where it has a shape, else the
+    // TMA-fed kernel's other shapes, else the cp.async kernel
+    // (automatic plans: when it runs unsplit or in segments long enough that
+    // the carry corrections stay a small part of the work; pinned plans: lanes
+    // 2, or a pinned split with lanes 0)
+    bool use_shfl = false;
+    if (tma_ok && variant == 0 && (lanes == 0 || lanes == 2) &&
+        sscan::plan_fwd_shfl(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl) == SSCAN_OK)
+        use_shfl = lanes == 2 || segments != 0 || pl.S == 1 || pl.Tseg >= sscan::kShflMinAutoSegmentSteps;
+    const bool use_tma = use_shfl || (tma_ok && sscan::plan_fwd_tma(f32, variant, batch, dim, seqlen, dstate,
+                                                                    segments, lanes, &pl) == SSCAN_OK);
     if (!use_tma) {
         const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, lanes, 1LL << 40, &pl);
         if (prc != SSCAN_OK) return prc;
@@ -451,13 +557,19 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     p.delta_softplus = (flags & SSCAN_DELTA_SOFTPLUS) ? 1 : 0;
     p.zoh = (flags & SSCAN_ZOH) ? 1 : 0;
     p.status = status;
+    // the test aid applies to the first pass of this call only
+    const unsigned expire_us = g_expire_wait_us;
+    g_expire_wait_us = 0;
+    p.wait_ns = (unsigned long long)expire_us * 1000ull;
+    p.expire_wait = expire_us != 0 ? 1 : 0;
 
     snprintf(g_rec.plan, sizeof(g_rec.plan),
              "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s%s%s",
              f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
-             use_tma ? "tma " : "", S == 1 ? "single" : "local+correct", delta_bias ? " bias" : "",
+             use_shfl ? "tma shfl " : use_tma ? "tma " : "", S == 1 ? "single" : S == 2 ? "local+correct" : "local+fold+correct",
+             delta_bias ? " bias" : "",
              p.delta_softplus ? " softplus" : "", p.zoh ? " zoh" : "", z ? " gate" : "",
-             S == 1 ? "" : pl.corr_tma ? " corr=tma" : " corr=cp.async");
+             S == 1 ? "" : pl.corr_shfl ? " corr=tma shfl" : pl.corr_tma ? " corr=tma" : " corr=cp.async");
     if (S > 1) {  // the correction's shape
         const size_t n = strlen(g_rec.plan);
         snprintf(g_rec.plan + n, sizeof(g_rec.plan) - n, "(%d,%d,%d)", pl.corr_sh.P, pl.corr_sh.NS,
@@ -468,30 +580,40 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     if (S == 1) {
         p.mode = sscan::MODE_SINGLE;
         p.seg_count = 1;
-        e = use_tma ? launch_fwd_tma(f32, p, sh, tiles, st) : launch_fwd(f32, p, sh, tiles, st);
+        e = use_shfl  ? launch_fwd_shfl(f32, p, sh, tiles, st)
+            : use_tma ? launch_fwd_tma(f32, p, sh, tiles, st)
+                      : launch_fwd(f32, p, sh, tiles, st);
         if (e != cudaSuccess) return fail_cuda(e);
         return SSCAN_OK;
     }
 
     const size_t nseg = (size_t)(batch * dim) * (size_t)S;
-    const size_t scratch_bytes = nseg * (size_t)(dstate + 1) * sizeof(float);
+    const size_t scratch_bytes = nseg * (size_t)sscan::split_floats_per_segment(dstate) * sizeof(float);
     void* scratch = nullptr;
     e = sscan::scratch_alloc(&scratch, scratch_bytes, st);
     if (e != cudaSuccess) return fail_cuda(e);
     p.seg_state = static_cast<float*>(scratch);
     p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
+    p.seg_dmin = p.seg_dsum + nseg;
     // pass 1: every segment from its local start, writing y and its aggregate;
-    // pass 2: add the carried state's decaying contribution (bf16 outputs are
-    // rounded twice, the second time with the carry added)
+    // pass 2: fold the aggregates into the state entering each segment (and
+    // the final state); pass 3: add the carried state's decaying contribution
+    // (bf16 outputs are rounded twice, the second time with the carry added)
     p.mode = sscan::MODE_LOCAL;
     p.seg_count = (int)S;
-    e = use_tma ? launch_fwd_tma(f32, p, sh, tiles * S, st) : launch_fwd(f32, p, sh, tiles * S, st);
+    e = use_shfl  ? launch_fwd_shfl(f32, p, sh, tiles * S, st)
+        : use_tma ? launch_fwd_tma(f32, p, sh, tiles * S, st)
+                  : launch_fwd(f32, p, sh, tiles * S, st);
+    p.wait_ns = 0;
+    p.expire_wait = 0;
+    if (e == cudaSuccess && S > 2) e = launch_fold(p, st);
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
         p.tiles_per_batch = (int)pl.corr_tiles_per_batch;
-        e = pl.corr_tma ? launch_fwd_tma(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st)
-                        : launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
+        e = pl.corr_shfl  ? launch_fwd_shfl(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st)
+            : pl.corr_tma ? launch_fwd_tma(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st)
+                          : launch_fwd(f32, p, pl.corr_sh, pl.corr_tiles * (S - 1), st);
     }
     cudaError_t ef = cudaFreeAsync(scratch, st);
     if (e != cudaSuccess) return fail_cuda(e);

@@ -88,6 +88,19 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 #define SSCAN_TMA_SHAPES(X) X(8, 2, 2) X(4, 4, 2) X(4, 16, 2)
 #endif
 inline int tma_channels(Shape sh) { return 4 * (32 / sh.P) * sh.CPL; }
+// Shapes of the shuffle kernels (the TMA-fed kernel's plain scan with
+// outputs summed by shuffles): 16 state slots as 2 lanes x 8 states, two
+// channels per lane.
+#ifndef SSCAN_TMA_SHFL_SHAPES
+#define SSCAN_TMA_SHFL_SHAPES(X) X(2, 8, 2)
+#endif
+bool shfl_has_shape(Shape sh);
+cudaError_t fwd_shfl_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+int fwd_shfl_occupancy(bool f32, Shape sh);
+cudaError_t fwd_shfl_launch_f32(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+cudaError_t fwd_shfl_launch_bf16(const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
+int fwd_shfl_occupancy_f32(Shape sh);
+int fwd_shfl_occupancy_bf16(Shape sh);
 bool tma_has_shape(Shape sh);
 cudaError_t fwd_tma_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream);
 // resident CTAs per SM of a shape and variant (0 plain, 1 options, 2 zero-order hold)
@@ -107,6 +120,15 @@ SSCAN_DECLARE_TMA_UNIT(bf16_z)
 bool tma_encode_3d(CUtensorMap* map, const void* base, bool f32, long long L, long long rows, long long batch,
                    int box_l, int box_rows);
 
+// The fold pass of a time split into three or more segments (sscan_fold.cu):
+// from the local pass's aggregates, the state entering each segment s >= 1,
+// written over aggregate slot s - 1; launched as a programmatic dependent of
+// the local pass.
+cudaError_t fwd_fold_launch(const FwdParams& p, cudaStream_t stream);
+// Scratch floats per (channel, segment) of a time split: the end state (N),
+// the sum of delta and min(0, smallest delta).
+inline long long split_floats_per_segment(long long N) { return N + 2; }
+
 // Stream-ordered scratch of the time-split passes (defined in sscan_abi.cu):
 // from a per-device pool of this library that keeps up to
 // kScratchRetainBytes mapped while idle, so that a call after a host
@@ -122,8 +144,10 @@ struct FwdPlan {
     long long S;      // time segments
     long long Tseg;   // steps per segment
     bool tma;         // the single/local pass runs on the TMA-fed kernel
+    bool shfl;        // ... in its shuffle variant (plain scan)
     Shape corr_sh;    // shape of the carry correction
     bool corr_tma;    // the correction runs on the TMA-fed kernel (else cp.async)
+    bool corr_shfl;   // ... in its shuffle variant
     long long corr_tiles_per_batch;
     long long corr_tiles;
 };
@@ -134,6 +158,10 @@ int plan_fwd(bool f32, long long batch, long long dim, long long seqlen, long lo
              int lanes, long long max_segments, FwdPlan* out);
 // The plan of the TMA-fed kernel (aligned rows, 8 < N <= 16; lanes 0, 4 or
 // 8; variant as fwd_variant), or SSCAN_ERR_INVALID when it does not apply.
+// plan_fwd_shfl: the plan of its shuffle variant (plain scan, aligned rows,
+// 8 < N <= 16, lanes 0 or 2).
+int plan_fwd_shfl(bool f32, long long batch, long long dim, long long seqlen, long long N, int segments,
+                  int lanes, long long max_segments, FwdPlan* out);
 int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long long seqlen, long long N,
                  int segments, int lanes, FwdPlan* out);
 

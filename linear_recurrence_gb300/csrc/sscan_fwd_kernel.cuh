@@ -59,6 +59,8 @@ struct FwdParams {
     float* final_state;
     float* seg_state;  // [batch*dim, S, N]  state at the end of each segment
     float* seg_dsum;   // [batch*dim, S]     sum of delta over each segment
+    float* seg_dmin;   // [batch*dim, S]     min(0, smallest delta of the segment): a carry
+                       //                    may grow where it is negative
     long long batch, dim, L, N;
     long long Tseg;    // steps per segment (multiple of the chunk)
     int S;             // segments per channel
@@ -72,6 +74,11 @@ struct FwdParams {
     int zoh;                  // zero-order-hold B-bar (the kernel's ZOH variant)
     int* status;              // device status word: a bounded wait that gives up
                               // stores SSCAN_ERR_TIMEOUT there
+    // test aid (TMA-fed kernels): when set, each bounded wait gives up after
+    // wait_ns, and the first B/C stage's barrier expects 16 bytes that no copy
+    // delivers, so that its waits run out and the timeout path runs
+    unsigned long long wait_ns;
+    int expire_wait;
 };
 
 // softplus(x) = log(1 + e^x) from the MUFU exponent and logarithm: with
@@ -173,43 +180,6 @@ struct FwdCfg {
     static_assert((DT * TC / 4) % kThreads == 0 || (DT * TC / 4) < kThreads, "epilogue items");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
-
-// State entering segment s (s >= 1) for the lane's states n = k*P + g of one
-// channel: the fold of the aggregates of segments 0 .. s-1 (segment 0's entry
-// holds its true end state because it started from h0).  FB segments' loads
-// are issued before their folds so the chain waits on memory once per FB.
-template <int NS, int P>
-__device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, int s, int g,
-                                              const float (&Al2)[NS], float (&h)[NS]) {
-    constexpr int FB = NS <= 2 ? 16 : NS <= 4 ? 8 : 4;
-    const float* st = p.seg_state + ch * p.S * p.N;
-    const float* ds = p.seg_dsum + ch * p.S;
-#pragma unroll
-    for (int k = 0; k < NS; ++k) {
-        const long long n = (long long)k * P + g;
-        h[k] = n < p.N ? st[n] : 0.f;
-    }
-    for (int sp = 1; sp < s; sp += FB) {
-        float dv[FB], bv[FB][NS];
-#pragma unroll
-        for (int q = 0; q < FB; ++q) {
-            const bool on = sp + q < s;
-            dv[q] = on ? ds[sp + q] : 0.f;
-#pragma unroll
-            for (int k = 0; k < NS; ++k) {
-                const long long n = (long long)k * P + g;
-                bv[q][k] = (on && n < p.N) ? st[(long long)(sp + q) * p.N + n] : 0.f;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < FB; ++q) {
-            if (sp + q < s) {
-#pragma unroll
-                for (int k = 0; k < NS; ++k) h[k] = fmaf(ex2(Al2[k] * dv[q]), h[k], bv[q][k]);
-            }
-        }
-    }
-}
 
 // Shared memory: raw ring [STAGES][ROWS][RROW] (T, cp.async targets), then the
 // fp32 work rows [ROWS][FROW] (bf16 only), then the partial outputs [DT][RS].
@@ -536,7 +506,8 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
                                             const float* zrows, long long b, long long d0, long long t0,
                                             long long t_end, int tid, bool corr, bool vec, bool dsum_on,
                                             float (&ds)[FwdCfg<T, NS, P, CPL, OPT>::IPT],
-                                            float (&dc)[FwdCfg<T, NS, P, CPL, OPT>::IPT]) {
+                                            float (&dc)[FwdCfg<T, NS, P, CPL, OPT>::IPT],
+                                            float (&dm)[FwdCfg<T, NS, P, CPL, OPT>::IPT]) {
     using Cfg = FwdCfg<T, NS, P, CPL, OPT>;
     constexpr int DT = Cfg::DT, TC = Cfg::TC, FROW = Cfg::FROW, RS = Cfg::RS;
     T* go = static_cast<T*>(p.out);
@@ -554,6 +525,7 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, const float* yp,
             const float tk = ds[k] + yk;
             dc[k] = (tk - ds[k]) - yk;
             ds[k] = tk;
+            dm[k] = fminf(dm[k], fminf(fminf(dv[0], dv[1]), fminf(dv[2], dv[3])));
         }
         float v[4];
         load4_smem(yp + r * RS + t4, v);
@@ -678,14 +650,24 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
         griddep_wait();
     }
+    // correction: a carried state is dropped once it has decayed below the
+    // threshold only while every decay factor exp(delta*A) of the CTA's
+    // channels in this segment is at most 1 (every A <= 0, no negative delta)
+    bool grows = false;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         if (corr) {
-            fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
-            if (!dval[j]) {
+            // the state entering segment s, folded from the aggregates of the
+            // segments before it by the fold pass (slot s - 1; with two
+            // segments slot 0 holds it already: segment 0 started from h0)
+            const float* ent = p.seg_state + (ch[j] * p.S + (s - 1)) * p.N;
 #pragma unroll
-                for (int k = 0; k < NS; ++k) h[j][k] = 0.f;
+            for (int k = 0; k < NS; ++k) {
+                const int n = k * P + g;
+                h[j][k] = (dval[j] && n < N) ? ent[n] : 0.f;
+                grows |= Al2[j][k] > 0.f;
             }
+            if (dval[j]) grows |= p.seg_dmin[ch[j] * p.S + s] < 0.f;
         } else {
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
@@ -702,20 +684,23 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
     float thr[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) thr[j] = 0.f;
+    const bool cut = corr && !__syncthreads_or(grows);
     if (corr) {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             float m = 0.f;
 #pragma unroll
             for (int k = 0; k < NS; ++k) m = fmaxf(m, fabsf(h[j][k]));
-            thr[j] = m * 0x1p-24f;
+            thr[j] = cut ? m * 0x1p-24f : 0.f;
+            // the last segment's final state: the entry state decayed over the
+            // segment plus the segment's local end state
             if (dval[j] && s == p.S - 1 && p.final_state != nullptr) {
-                const float ds = p.seg_dsum[ch[j] * p.S + s];
+                const float dsg = p.seg_dsum[ch[j] * p.S + s];
                 const float* sst = p.seg_state + (ch[j] * p.S + s) * p.N;
 #pragma unroll
                 for (int k = 0; k < NS; ++k) {
                     const int n = k * P + g;
-                    if (n < N) p.final_state[ch[j] * p.N + n] = fmaf(ex2(Al2[j][k] * ds), h[j][k], sst[n]);
+                    if (n < N) p.final_state[ch[j] * p.N + n] = fmaf(ex2(Al2[j][k] * dsg), h[j][k], sst[n]);
                 }
             }
         }
@@ -750,8 +735,9 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
     }
 
     float ds[Cfg::IPT], dc[Cfg::IPT];  // Kahan sums of delta per epilogue item slot
+    float dm[Cfg::IPT];                // and min(0, smallest delta)
 #pragma unroll
-    for (int k = 0; k < Cfg::IPT; ++k) ds[k] = dc[k] = 0.f;
+    for (int k = 0; k < Cfg::IPT; ++k) ds[k] = dc[k] = dm[k] = 0.f;
     for (int i = 0; i < nchunks; ++i) {
         const long long t0 = t_begin + (long long)i * TC;
         if (vec) {
@@ -761,7 +747,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
             load_chunk_scalar<T, NS, P, CPL, OPT>(q, sm.rows(i), b, d0, t0, t_end, tid, load_u, load_b, load_c);
         }
         if (corr) {
-            bool live = false;
+            bool live = !cut;
 #pragma unroll
             for (int j = 0; j < CPL; ++j)
 #pragma unroll
@@ -800,7 +786,7 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
         }
         __syncthreads();  // every lane's partials of the chunk are in place
         store_chunk<T, NS, P, CPL, OPT>(p, sm.yp, rows, (OPT > 0 && p.z != nullptr) ? rows + Cfg::ZROW0 * Cfg::FROW : nullptr, b,
-                                   d0, t0, t_end, tid, corr, vec, dsum_on, ds, dc);
+                                   d0, t0, t_end, tid, corr, vec, dsum_on, ds, dc, dm);
     }
     cp_async_wait<0>();
     if (corr) return;
@@ -811,15 +797,22 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
 #pragma unroll
         for (int k = 0; k < Cfg::IPT; ++k) {
             const int q = tid + k * Cfg::kThreads;
-            if (q < DT * SL) sm.yp[q] = ds[k];
+            if (q < DT * SL) {
+                sm.yp[q] = ds[k];
+                sm.yp[DT * SL + q] = dm[k];
+            }
         }
         __syncthreads();
         for (int r = tid; r < DT; r += Cfg::kThreads) {
             if (d0 + r >= p.dim) continue;
-            float sum = 0.f;
+            float sum = 0.f, mn = 0.f;
 #pragma unroll
-            for (int j = 0; j < SL; ++j) sum += sm.yp[j * DT + r];
+            for (int j = 0; j < SL; ++j) {
+                sum += sm.yp[j * DT + r];
+                mn = fminf(mn, sm.yp[DT * SL + j * DT + r]);
+            }
             p.seg_dsum[(b * p.dim + d0 + r) * p.S + s] = sum;
+            p.seg_dmin[(b * p.dim + d0 + r) * p.S + s] = mn;
         }
     }
 #pragma unroll

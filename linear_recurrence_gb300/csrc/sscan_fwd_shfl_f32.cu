@@ -1,0 +1,11 @@
+// float32-I/O instantiations of the TMA-fed selective-scan kernel with
+// outputs summed by warp shuffles (plain scan, single and local passes).
+#define SSCAN_TMA_IMPL
+#include "sscan_fwd_tma.cuh"
+
+namespace sscan {
+
+using UnitT = float;
+SSCAN_DEFINE_SHFL_UNIT(f32)
+
+}  // namespace sscan

@@ -70,6 +70,21 @@ cudaError_t fwd_tma_launch(bool f32, const FwdParams& p, Shape sh, int grid, cud
     }
 }
 
+bool shfl_has_shape(Shape sh) {
+#define SSCAN_SHFL_HAS(P_, NS_, CPL_) \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return true;
+    SSCAN_TMA_SHFL_SHAPES(SSCAN_SHFL_HAS)
+#undef SSCAN_SHFL_HAS
+    return false;
+}
+
+cudaError_t fwd_shfl_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream) {
+    if (!p.vec) return cudaErrorInvalidValue;
+    return f32 ? fwd_shfl_launch_f32(p, sh, grid, stream) : fwd_shfl_launch_bf16(p, sh, grid, stream);
+}
+
+int fwd_shfl_occupancy(bool f32, Shape sh) { return f32 ? fwd_shfl_occupancy_f32(sh) : fwd_shfl_occupancy_bf16(sh); }
+
 int fwd_tma_occupancy(bool f32, Shape sh, int variant) {
     switch (variant) {
         case 2: return f32 ? fwd_tma_occupancy_f32_z(sh) : fwd_tma_occupancy_bf16_z(sh);

@@ -64,6 +64,15 @@ struct TmaMaps {
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// Steps per chunk of the shuffle kernels, and the most resident CTAs per SM
+// their register allocation is asked for (8 states per lane).
+#ifndef SSCAN_SHFL_CHUNK
+#define SSCAN_SHFL_CHUNK 32
+#endif
+#ifndef SSCAN_SHFL_MAX_BLOCKS
+#define SSCAN_SHFL_MAX_BLOCKS 4
+#endif
+
 // Depth of the u/delta and B/C rings.  Two stages measured faster than three
 // on GB300: the smaller footprint fits one more CTA per SM, and a chunk of
 // compute (over a microsecond per warp) covers the TMA latency.
@@ -72,28 +81,35 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 #endif
 constexpr int kTmaStages = SSCAN_TMA_STAGES;
 
-template <typename T, int NS, int P, int CPL, int OPT_ = 0>
+template <typename T, int NS, int P, int CPL, int OPT_ = 0, bool SH_ = false>
 struct TmaCfg {
     using Base = FwdCfg<T, NS, P, CPL, 0>;
     static constexpr int OPT = OPT_;  // 0 plain; 1 options; 2 options + zero-order hold
+    // SH: the lanes sum a channel's P partial outputs by warp shuffles and
+    // store the outputs themselves (no partial-output buffer, no epilogue)
+    static constexpr bool SH = SH_;
     static constexpr int NUR = OPT > 0 ? 3 : 2;  // row sets of a warp's slot: u, delta (, z)
     static constexpr int kWarps = 4;
     static constexpr int kThreads = 32 * kWarps;
-    static constexpr int GPW = Base::GPW, CPW = Base::CPW, NSP = Base::NSP, TC = Base::TC;
+    static constexpr int GPW = Base::GPW, CPW = Base::CPW, NSP = Base::NSP;
+    // steps per chunk: the shuffle kernels may take shorter chunks (a smaller
+    // ring, more resident CTAs)
+    static constexpr int TC = SH ? SSCAN_SHFL_CHUNK : Base::TC;
+    static constexpr int VECE = 16 / (int)sizeof(T);  // elements per 16 bytes
     static constexpr int DT = kWarps * CPW;  // channels per CTA
     // raw row: fp32 rows are read in place, so they keep the TC + 16 bytes
     // of the bank-spreading pad; bf16 rows are only widened (whole 16-byte
     // pieces of consecutive rows) and take no pad, which keeps the wide-state
     // CTA within half an SM's shared memory
-    static constexpr int RROW = Base::kF32 ? Base::RROW : TC;
+    static constexpr int RROW = Base::kF32 ? TC + VECE : TC;
     // bf16 with 64 state slots (plain scan): the lanes read their u/delta
     // rows straight from the raw stage (converting 4 values per read), which
     // saves the per-warp fp32 copy and buys a third widened B/C slot; those
     // raw rows keep the 16-byte pad, so that the 8 channel rows a warp reads
     // at one step fall in distinct banks
     static constexpr bool kRawU = !Base::kF32 && NS > 4 && OPT_ == 0;
-    static constexpr int RROW_U = kRawU ? Base::RROW : RROW;  // raw u/delta (z) row
-    static constexpr int FROW = Base::FROW;  // fp32 row: TC + 4
+    static constexpr int RROW_U = kRawU ? TC + VECE : RROW;  // raw u/delta (z) row
+    static constexpr int FROW = TC + 4;  // fp32 row
     static constexpr bool kF32 = Base::kF32;
     static constexpr int STAGES = kTmaStages;
     static constexpr int ESZ = (int)sizeof(T);
@@ -133,14 +149,20 @@ struct TmaCfg {
     static constexpr int OFF_WORK = OFF_BCW + WB * BCW_BYTES;
     static constexpr int WORK_BYTES = kF32 || kRawU ? 0 : WORK_ROWS * FROW * 4;  // per warp
     static constexpr int OFF_YP = OFF_WORK + kWarps * WORK_BYTES;
-    static constexpr int YP_BYTES = CPW * RS * 4;  // per warp
+    static constexpr int YP_BYTES = SH ? 0 : CPW * RS * 4;  // per warp
     static constexpr int SMEM_BYTES = OFF_YP + kWarps * YP_BYTES + 128;  // + base alignment
-    static_assert(TC == 32, "epilogue items assume 8 four-step blocks per chunk");
+    // shuffle kernels: the register allocation is asked for the resident CTAs
+    // that shared memory allows (228 KB per SM, 1 KB reserved per CTA), at most
+    // 4, and at most 2 for 16 states per lane, whose registers would spill at 3
+    static constexpr int SH_FIT = (228 * 1024) / (SMEM_BYTES + 1024);
+    static constexpr int SH_CAP = NS >= 16 ? 2 : SSCAN_SHFL_MAX_BLOCKS;
+    static constexpr int SH_MIN_BLOCKS = SH_FIT < 1 ? 1 : SH_FIT > SH_CAP ? SH_CAP : SH_FIT;
+    static_assert(SH || TC == 32, "epilogue items assume 8 four-step blocks per chunk");
     static_assert(CPW % 8 == 0, "a warp's epilogue items must fill its lanes");
     static_assert(RS >= P * HROW && (RS / 4) % 8 == 4, "partial row stride");
-    // after the mbarriers: the B/C release counters [STAGES] and the last
-    // chunk whose B/C copy was issued
-    static constexpr int OFF_BCW_BAR = align_up((kWarps + 1) * STAGES * 8 + STAGES * 4 + 4, 8);
+    // after the mbarriers: the B/C release counters [STAGES] and, per stage,
+    // the last chunk whose B/C copy was issued into it
+    static constexpr int OFF_BCW_BAR = align_up((kWarps + 1) * STAGES * 8 + 2 * STAGES * 4, 8);
     static_assert(OFF_BCW_BAR + 2 * WB * 8 <= 1024, "barrier area");
     static_assert(RROW * ESZ % 16 == 0 && RROW_U * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
     static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256 && RROW_U <= 256, "tensor-map box limits");
@@ -319,6 +341,184 @@ __device__ __forceinline__ void compute_half_tma(const TU* su, const TU* sd, con
                                                                        invA, invAs, h);
 }
 
+// SH kernels: one chunk of the recurrence for the calling lane, with its
+// outputs finished in registers instead of a shared partial-output buffer.
+// Per 4-step block: the lane's u/delta vectors (read one block ahead), the
+// B/C vectors of its states per quad, then per element x = delta*A',
+// a = 2^x, h = a*h + (delta*u)*B, y += C*h.  The lanes of a channel pair
+// hold the pair in opposite register order (rl), so one exchange between
+// lanes P/2 apart gives each lane the other's partial sums of the channel it
+// keeps (y[0] += partner's y[1]); the remaining P/2 lanes of the channel then
+// exchange all four sums (butterfly), after which every lane holds the full
+// sums of its kept channel rl[0], and the lanes with (g & (P/2 - 1)) == 0
+// store them with D*u added.  A local pass also takes the Kahan sum of the
+// kept channel's delta (steps past L hold delta = 0).
+template <typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
+__device__ __forceinline__ void compute_chunk_shfl(const TU* su, const TU* sd, const float* sB, const float* sC,
+                                                   const int (&rl)[2], int g, const float (&Al2)[2][NS],
+                                                   const float (&As)[2], float (&h)[2][NS], float Dk, T* orow,
+                                                   bool store, int nvalid, bool dsum_on, float& dsum,
+                                                   float& dcomp, float& dmin) {
+    constexpr int CPL = 2;
+    constexpr int NB = TC / 4, QS = 4, NQ = NS / QS;
+    constexpr unsigned FULL = 0xffffffffu;
+    static_assert(P >= 2 && 32 % P == 0 && NS % QS == 0, "lane pairs and whole quads of states");
+    const float* bB = sB + g * FROW;
+    const float* bC = sC + g * FROW;
+    float nu[CPL][4], nd[CPL][4];
+    auto load_block = [&](int t4) {
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            load4_smem(su + rl[j] * UROW + t4, nu[j]);
+            load4_smem(sd + rl[j] * UROW + t4, nd[j]);
+        }
+    };
+    load_block(0);
+#pragma unroll 2
+    for (int blk = 0; blk < NB; ++blk) {
+        const int t4 = 4 * blk;
+        float dd[CPL][4], du[CPL][4], uk[4], as[CPL][4], y[CPL][4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                dd[j][s] = nd[j][s];
+                du[j][s] = nd[j][s] * nu[j][s];
+            }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) uk[s] = nu[0][s];
+        if (blk + 1 < NB) load_block(t4 + 4);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                y[j][s] = 0.f;
+            }
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float bb[QS][4], cc[QS][4];
+#pragma unroll
+            for (int kk = 0; kk < QS; ++kk) {
+                load4_smem(bB + (q * QS + kk) * P * FROW + t4, bb[kk]);
+                load4_smem(bC + (q * QS + kk) * P * FROW + t4, cc[kk]);
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int kk = 0; kk < QS; ++kk) {
+                        const int k = q * QS + kk;
+                        const float a = SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
+                        h[j][k] = fmaf(a, h[j][k], du[j][s] * bb[kk][s]);
+                        y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
+                    }
+        }
+        // the channel's P partial sums
+#pragma unroll
+        for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[1][s], P / 2);
+#pragma unroll
+        for (int m = P / 4; m >= 1; m /= 2)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[0][s], m);
+        if (dsum_on) {
+            const float yk = ((dd[0][0] + dd[0][1]) + (dd[0][2] + dd[0][3])) - dcomp;
+            const float tk = dsum + yk;
+            dcomp = (tk - dsum) - yk;
+            dsum = tk;
+            dmin = fminf(dmin, fminf(fminf(dd[0][0], dd[0][1]), fminf(dd[0][2], dd[0][3])));
+        }
+        if (store && t4 < nvalid) {
+            float v[4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) v[s] = fmaf(Dk, uk[s], y[0][s]);
+            if constexpr (sizeof(T) == 4) {
+                *reinterpret_cast<float4*>(orow + t4) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                const unsigned lo = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[0])) |
+                                    ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[1])) << 16);
+                const unsigned hi = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[2])) |
+                                    ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[3])) << 16);
+                *reinterpret_cast<uint2*>(orow + t4) = make_uint2(lo, hi);
+            }
+        }
+    }
+}
+
+// SH kernels, carry correction: one chunk of the homogeneous recurrence
+// h = exp(delta*A)*h from the carried state, its C-contraction summed over the
+// channel's lanes as in compute_chunk_shfl, added to the local outputs (staged
+// in the u rows, sy) and stored.  live[k] (warp-uniform) skips the state slots
+// whose carry has decayed below the threshold in every lane of the warp.
+template <typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
+__device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, const float* sC, const int (&rl)[2],
+                                                 int g, const float (&Al2)[2][NS], const float (&As)[2],
+                                                 const bool (&live)[NS], float (&h)[2][NS], T* orow, bool store,
+                                                 int nvalid) {
+    constexpr int CPL = 2;
+    constexpr int NB = TC / 4, QS = 4, NQ = NS / QS;
+    constexpr unsigned FULL = 0xffffffffu;
+    const float* bC = sC + g * FROW;
+#pragma unroll 2
+    for (int blk = 0; blk < NB; ++blk) {
+        const int t4 = 4 * blk;
+        float dd[CPL][4], as[CPL][4], y[CPL][4], yl[4];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            load4_smem(sd + rl[j] * UROW + t4, dd[j]);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                y[j][s] = 0.f;
+            }
+        }
+        load4_smem(sy + rl[0] * UROW + t4, yl);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            bool lq = false;
+#pragma unroll
+            for (int kk = 0; kk < QS; ++kk) lq |= live[q * QS + kk];
+            if (!lq) continue;
+            float cc[QS][4];
+#pragma unroll
+            for (int kk = 0; kk < QS; ++kk) load4_smem(bC + (q * QS + kk) * P * FROW + t4, cc[kk]);
+#pragma unroll
+            for (int kk = 0; kk < QS; ++kk) {
+                const int k = q * QS + kk;
+                if (!live[k]) continue;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) {
+                        h[j][k] *= SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
+                        y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
+                    }
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[1][s], P / 2);
+#pragma unroll
+        for (int m = P / 4; m >= 1; m /= 2)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[0][s], m);
+        if (store && t4 < nvalid) {
+            float v[4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) v[s] = yl[s] + y[0][s];
+            if constexpr (sizeof(T) == 4) {
+                *reinterpret_cast<float4*>(orow + t4) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                const unsigned lo = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[0])) |
+                                    ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[1])) << 16);
+                const unsigned hi = (unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[2])) |
+                                    ((unsigned)__bfloat16_as_ushort(from_f32<bf16>(v[3])) << 16);
+                *reinterpret_cast<uint2*>(orow + t4) = make_uint2(lo, hi);
+            }
+        }
+    }
+}
+
 // Steps [T0, T0 + TS) of the carry correction for the calling lane: the
 // homogeneous recurrence h = exp(delta*A)*h from the carried state and its
 // C-contraction, stored as partial outputs like compute_half_tma.  live[k]
@@ -399,9 +599,10 @@ __device__ __forceinline__ void widen_delta_rows_warp(const bf16* src, float* ds
 // the decaying contribution of its entry state to the local outputs; the u
 // tensor map then covers those outputs).  The body of the kernels below; tm
 // is their __grid_constant__ parameter.
-template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
+template <typename T, int NS, int P, int CPL, int OPT, bool CORR, bool SH = false>
 __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const TmaMaps& tm) {
-    using Cfg = TmaCfg<T, NS, P, CPL, OPT>;
+    using Cfg = TmaCfg<T, NS, P, CPL, OPT, SH>;
+    static_assert(!SH || (CPL == 2 && P >= 2 && OPT == 0), "shuffle kernels: plain scan, lane pairs");
     constexpr int NUR = Cfg::NUR;
     constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
     constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW, RS = Cfg::RS, STAGES = Cfg::STAGES;
@@ -446,17 +647,21 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     // it sets up (barriers, decay rates) while the pass runs and waits for the
     // pass's completion before reading anything the pass wrote
     if constexpr (!CORR) griddep_launch_dependents();
-    int* bc_hi = reinterpret_cast<int*>(bc_count + STAGES);  // last chunk whose B/C copy was issued
+    int* bc_last = reinterpret_cast<int*>(bc_count + STAGES);  // [STAGES] last chunk whose B/C copy went there
+    const uint64_t lim = p.wait_ns != 0 ? (uint64_t)p.wait_ns : kWaitLimitNs;
     if (tid == 0) {
         for (int i = 0; i < (kWarps + 1) * STAGES; ++i) mbar_init(barU + i, 1);
         for (int i = 0; i < STAGES; ++i) bc_count[i] = 0;
-        *bc_hi = -1;
+        for (int i = 0; i < STAGES; ++i) bc_last[i] = -1;
         if constexpr (!Cfg::kF32) {
             for (int i = 0; i < Cfg::WB; ++i) {
                 mbar_init(bcw_full + i, 32);
                 mbar_init(bcw_empty + i, kWarps);
             }
         }
+        // test aid: bytes that no copy delivers keep the first B/C stage
+        // from completing, so that the waits on it run out
+        if (p.expire_wait) mbar_expect_tx(barBC, 16);
         mbar_fence_init();
     }
     __syncthreads();
@@ -479,7 +684,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     auto issue_bc = [&](int c, int st) {
         T* dst = bc_slot(st);
         uint64_t* bar = barBC + st;
-        if constexpr (CORR) atomicMax(bc_hi, c);
+        bc_last[st] = c;
         mbar_arrive_expect_tx(bar, (CORR ? 1 : 2) * Cfg::BC_BOX);
         const int t0 = (int)(t_begin + (long long)c * TC);
         if constexpr (!CORR) tma_load_3d(dst, &tm.B, t0, 0, (int)b, bar);
@@ -516,7 +721,12 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     bool uniform_rate = true;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
-        rl[j] = j * GPW + gi;
+        // shuffle kernels: lane group gi owns the adjacent channel rows 2gi and
+        // 2gi + 1 (the eight lanes of a quarter-warp then read eight distinct
+        // padded rows, in distinct banks), and the lanes in the upper half of
+        // the channel's lanes hold the pair in the opposite order
+        if constexpr (SH) rl[j] = 2 * gi + (j ^ ((g & (P / 2)) ? 1 : 0));
+        else rl[j] = j * GPW + gi;
         const long long dch = dw + rl[j];
         dval[j] = dch < p.dim;
         ch[j] = b * p.dim + (dval[j] ? dch : 0);
@@ -541,26 +751,39 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
             for (int c = 0; c < STAGES && c < nchunks; ++c)
                 tma_load_3d(u_slot(c), &tm.u, (int)(t_begin + (long long)c * TC), (int)dw, (int)b,
                             barU + w * STAGES + c);
+    }
+    // correction: the carried state entering segment s, folded from the
+    // aggregates of the segments before it by the fold pass (slot s - 1;
+    // with two segments slot 0 holds it already: segment 0 started from h0); it
+    // is followed until every state of the CTA has fallen below 2^-24 of its
+    // entry magnitude, a cut-off taken only while every decay factor
+    // exp(delta*A) of the CTA's channels in this segment is at most 1 (every
+    // A <= 0, no negative delta)
+    bool grows = false;
+    if constexpr (CORR) {
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {  // the carried state entering segment s
-            fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
-            if (!dval[j]) {
+        for (int j = 0; j < CPL; ++j) {
+            const float* ent = p.seg_state + (ch[j] * p.S + (s - 1)) * p.N;
 #pragma unroll
-                for (int k = 0; k < NS; ++k) h[j][k] = 0.f;
+            for (int k = 0; k < NS; ++k) {
+                const int n = k * P + g;
+                h[j][k] = (dval[j] && n < N) ? ent[n] : 0.f;
+                grows |= Al2[j][k] > 0.f;
             }
+            if (dval[j]) grows |= p.seg_dmin[ch[j] * p.S + s] < 0.f;
         }
     }
+    const bool cut = CORR && !__syncthreads_or(grows);
     const bool scalar = __all_sync(FULL, uniform_rate);
-    // correction: the carry is followed until every state of the CTA has
-    // fallen below 2^-24 of its entry magnitude; the last segment's final
-    // state is the carry decayed over the segment plus its local end state
     float thr[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         float m = 0.f;
 #pragma unroll
         for (int k = 0; k < NS; ++k) m = fmaxf(m, fabsf(h[j][k]));
-        thr[j] = m * 0x1p-24f;
+        thr[j] = cut ? m * 0x1p-24f : 0.f;
+        // the last segment's final state: the entry state decayed over the
+        // segment plus the segment's local end state
         if (CORR && dval[j] && s == p.S - 1 && p.final_state != nullptr) {
             const float dsg = p.seg_dsum[ch[j] * p.S + s];
             const float* sst = p.seg_state + (ch[j] * p.S + s) * p.N;
@@ -577,9 +800,9 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     const bool dsum_on = !CORR && p.mode == MODE_LOCAL;
     // Kahan sums of delta per slot (a slot is the same channel row and 4-step
     // offset in both halves)
-    float dsum[Cfg::IPH], dcomp[Cfg::IPH];
+    float dsum[Cfg::IPH], dcomp[Cfg::IPH], dmin[Cfg::IPH];  // and min(0, smallest delta)
 #pragma unroll
-    for (int k = 0; k < Cfg::IPH; ++k) dsum[k] = dcomp[k] = 0.f;
+    for (int k = 0; k < Cfg::IPH; ++k) dsum[k] = dcomp[k] = dmin[k] = 0.f;
     float Dr[Cfg::IPH];
 #pragma unroll
     for (int k = 0; k < Cfg::IPH; ++k) {
@@ -588,6 +811,12 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     }
     T* gout = static_cast<T*>(p.out);
     float* work = reinterpret_cast<float*>(sbase + Cfg::OFF_WORK + w * Cfg::WORK_BYTES);
+    // shuffle kernels: the lane's kept channel rl[0], whose outputs it stores
+    // when it is the first of the channel's lanes that hold the full sums
+    float sh_dsum = 0.f, sh_dcomp = 0.f, sh_dmin = 0.f;
+    const bool sh_store = SH && (g & (P / 2 - 1)) == 0 && dval[0];
+    const float sh_D = (SH && p.D != nullptr && dval[0]) ? __ldg(p.D + (dw + rl[0])) : 0.f;
+    T* sh_orow = gout + ch[0] * p.L;
 
     // warp epilogue of one half chunk: sum the P partials, add D*u, store 4
     // steps per item (and the Kahan sums of delta of a local pass)
@@ -629,6 +858,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 const float tk = dsum[k] + yk;
                 dcomp[k] = (tk - dsum[k]) - yk;
                 dsum[k] = tk;
+                dmin[k] = fminf(dmin[k], fminf(fminf(dv[0], dv[1]), fminf(dv[2], dv[3])));
             }
             if (dd < p.dim && t < t_end) {  // t_end is a multiple of 4 on this path
                 T* o = gout + (b * p.dim + dd) * p.L + t;
@@ -649,8 +879,8 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     // ring (the calling warp is chunk c's widener), then refill the raw stage
     auto widen_bc = [&](int c) -> bool {
         const int st = c % STAGES, ws = c % Cfg::WB;
-        bool good = mbar_wait_bounded(barBC + st, (unsigned)(c / STAGES) & 1u);
-        if (c >= Cfg::WB) good = mbar_wait_bounded(bcw_empty + ws, (unsigned)((c - Cfg::WB) / Cfg::WB) & 1u) && good;
+        bool good = mbar_wait_bounded(barBC + st, (unsigned)(c / STAGES) & 1u, lim);
+        if (c >= Cfg::WB) good = mbar_wait_bounded(bcw_empty + ws, (unsigned)((c - Cfg::WB) / Cfg::WB) & 1u, lim) && good;
         good = __all_sync(FULL, good);
         if (!good) return false;
         float* dst = reinterpret_cast<float*>(sbase + Cfg::OFF_BCW + ws * Cfg::BCW_BYTES);
@@ -679,8 +909,8 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         const UT *su, *sd;
         const float *sz, *sB, *sC;
         if constexpr (Cfg::kF32) {
-            ok = mbar_wait_bounded(barU + w * STAGES + st, par);
-            ok = mbar_wait_bounded(barBC + st, par) && ok;
+            ok = mbar_wait_bounded(barU + w * STAGES + st, par, lim);
+            ok = mbar_wait_bounded(barBC + st, par, lim) && ok;
             ok = __all_sync(FULL, ok);
             if (!ok && !CORR) break;
             su = reinterpret_cast<const UT*>(u_slot(st));
@@ -710,12 +940,12 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
             }
             // the warp's raw u/delta rows, read in place; the stage is
             // refilled after the chunk
-            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par)) && ok;
+            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par, lim)) && ok;
             if (!ok && !CORR) break;
             su = reinterpret_cast<const UT*>(u_slot(st));
             sd = reinterpret_cast<const UT*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
             sz = nullptr;
-            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u)) && ok;
+            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u, lim)) && ok;
             if (!ok && !CORR) break;
             sB = reinterpret_cast<const float*>(sbase + Cfg::OFF_BCW + (i % Cfg::WB) * Cfg::BCW_BYTES);
             sC = sB + NSP * FROW;
@@ -727,7 +957,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
             }
             // the warp's own u/delta (z) rows, widened (delta transformed),
             // then the raw stage refilled
-            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par)) && ok;
+            ok = __all_sync(FULL, mbar_wait_bounded(barU + w * STAGES + st, par, lim)) && ok;
             if (!ok && !CORR) break;
             const bf16* ru = reinterpret_cast<const bf16*>(u_slot(st));
             widen_rows_warp<RROW, FROW, TC>(ru, work, CPW, lane);
@@ -742,7 +972,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                     work + 2 * CPW * FROW, CPW, lane);
             __syncwarp();
             if (lane == 0 && nx < nchunks) issue_u(nx, st);
-            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u)) && ok;
+            ok = __all_sync(FULL, mbar_wait_bounded(bcw_full + i % Cfg::WB, (unsigned)(i / Cfg::WB) & 1u, lim)) && ok;
             if (!ok && !CORR) break;
             su = work;
             sd = work + CPW * FROW;
@@ -760,7 +990,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 bool l = false;
 #pragma unroll
                 for (int j = 0; j < CPL; ++j) l |= fabsf(h[j][k]) > thr[j];
-                live[k] = scalar ? true : __any_sync(FULL, l);
+                live[k] = (scalar || !cut) ? true : __any_sync(FULL, l);
                 any |= l;
             }
             // a wait that gave up in any warp ends the CTA's correction; so
@@ -770,8 +1000,46 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 ok = false;
                 break;
             }
-            if (!__syncthreads_or(any)) break;
+            if (cut && !__syncthreads_or(any)) break;
         }
+        if constexpr (SH && CORR) {
+            const int nvalid = (int)min((long long)TC, t_end - t0);
+            if (scalar)
+                decay_chunk_shfl<T, UT, UROW, NS, P, FROW, TC, true>(su, sd, sC, rl, g, Al2, As, live, h,
+                                                                     sh_orow + t0, sh_store, nvalid);
+            else
+                decay_chunk_shfl<T, UT, UROW, NS, P, FROW, TC, false>(su, sd, sC, rl, g, Al2, As, live, h,
+                                                                      sh_orow + t0, sh_store, nvalid);
+            __syncwarp();
+            if (lane == 0) {  // C of this chunk is no longer read by this warp
+                if constexpr (Cfg::kF32) {
+                    const unsigned old = atomicAdd(bc_count + st, 1u);
+                    if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+                } else {
+                    mbar_arrive(bcw_empty + i % Cfg::WB);
+                }
+            }
+        } else if constexpr (SH) {
+            const int nvalid = (int)min((long long)TC, t_end - t0);
+            if (scalar)
+                compute_chunk_shfl<T, UT, UROW, NS, P, FROW, TC, true>(su, sd, sB, sC, rl, g, Al2, As, h, sh_D,
+                                                                       sh_orow + t0, sh_store, nvalid, dsum_on,
+                                                                       sh_dsum, sh_dcomp, sh_dmin);
+            else
+                compute_chunk_shfl<T, UT, UROW, NS, P, FROW, TC, false>(su, sd, sB, sC, rl, g, Al2, As, h, sh_D,
+                                                                        sh_orow + t0, sh_store, nvalid, dsum_on,
+                                                                        sh_dsum, sh_dcomp, sh_dmin);
+            __syncwarp();
+            // B/C of this chunk are no longer read by this warp
+            if (lane == 0) {
+                if constexpr (Cfg::kF32) {
+                    const unsigned old = atomicAdd(bc_count + st, 1u);
+                    if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
+                } else {
+                    mbar_arrive(bcw_empty + i % Cfg::WB);
+                }
+            }
+        } else {
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
             if constexpr (CORR) {
@@ -801,6 +1069,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
             epilogue(half, t0, su, sd, sz);
             __syncwarp();
         }
+        }
         if constexpr (Cfg::kF32 || kRawU) {
             // u/delta (z) of this stage are no longer read by this warp; the
             // delta transform wrote them, so order those writes before the copy
@@ -810,47 +1079,50 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
             }
         }
     }
-    if (!ok) {
-        // a wait gave up: record it, then wait (bounded) for the copies this
-        // warp may still have in flight before leaving
+    // Every warp leaves the chunk loop here (a local pass has no CTA barrier in
+    // the loop; a correction leaves it at the same chunk by CTA-wide votes).
+    // After this barrier no warp issues a copy, so a CTA that gave up on a
+    // wait, or a correction that stopped early, waits (bounded) for the last
+    // copy issued into every ring stage before it leaves: none may land in
+    // the shared memory of a CTA that has exited.
+    const bool failed = __syncthreads_or(!ok);
+    if (failed || (CORR && i < nchunks)) {
         if (lane == 0) {
-            atomicExch(p.status, (int)SSCAN_ERR_TIMEOUT);
-            for (int c = i; c < nchunks && c < i + STAGES; ++c) {
-                mbar_wait_bounded(barU + w * STAGES + c % STAGES, (unsigned)(c / STAGES) & 1u);
-                mbar_wait_bounded(barBC + c % STAGES, (unsigned)(c / STAGES) & 1u);
-            }
-        }
-        return;
-    }
-    if constexpr (CORR) {
-        // stopped early: wait (bounded) for the copies already issued for the
-        // chunks not consumed (chunk i's were), so that none lands in the
-        // shared memory of a CTA that has left
-        __syncthreads();  // no warp issues copies any more
-        if (lane == 0 && i < nchunks) {
-            // per ring slot, the last copy issued into it (earlier phases of
-            // the slot have completed); chunks up to i were consumed
             bool good = true;
-            const int bhi = *bc_hi;
             for (int st = 0; st < STAGES; ++st) {
+                // a warp issues its u/delta copies in chunk order; the B/C
+                // copies of a bf16 ring may be issued out of order, so their
+                // stages record their own last chunk
                 const int cu = u_hi - ((u_hi - st) % STAGES + STAGES) % STAGES;  // largest c <= u_hi, c = st
-                if (cu > i) good = mbar_wait_bounded(barU + w * STAGES + st, (unsigned)(cu / STAGES) & 1u) && good;
-                const int cb = bhi - ((bhi - st) % STAGES + STAGES) % STAGES;
-                if (w == 0 && cb > i) good = mbar_wait_bounded(barBC + st, (unsigned)(cb / STAGES) & 1u) && good;
+                if (cu >= 0) good = mbar_wait_bounded(barU + w * STAGES + st, (unsigned)(cu / STAGES) & 1u, lim) && good;
+                const int cb = bc_last[st];
+                if (w == 0 && cb >= 0)
+                    good = mbar_wait_bounded(barBC + st, (unsigned)(cb / STAGES) & 1u, lim) && good;
             }
-            if (!good) atomicExch(p.status, (int)SSCAN_ERR_TIMEOUT);
+            if (failed || !good) atomicExch(p.status, (int)SSCAN_ERR_TIMEOUT);
         }
         return;
     }
+    if constexpr (CORR) return;
 
-    if (dsum_on) {  // the segment's sum of delta per channel: 4 slots in 4 lanes
+    if (SH && dsum_on) {  // the kept channel's sum of delta
+        if (sh_store) {
+            p.seg_dsum[ch[0] * p.S + s] = sh_dsum;
+            p.seg_dmin[ch[0] * p.S + s] = sh_dmin;
+        }
+    } else if (dsum_on) {  // the segment's sum of delta per channel: 4 slots in 4 lanes
 #pragma unroll
         for (int k = 0; k < Cfg::IPH; ++k) {
-            float v = dsum[k];
+            float v = dsum[k], m = dmin[k];
             v += __shfl_xor_sync(FULL, v, 1);
             v += __shfl_xor_sync(FULL, v, 2);
+            m = fminf(m, __shfl_xor_sync(FULL, m, 1));
+            m = fminf(m, __shfl_xor_sync(FULL, m, 2));
             const long long dd = dw + (lane + 32 * k) / 4;
-            if ((lane & 3) == 0 && dd < p.dim) p.seg_dsum[(b * p.dim + dd) * p.S + s] = v;
+            if ((lane & 3) == 0 && dd < p.dim) {
+                p.seg_dsum[(b * p.dim + dd) * p.S + s] = v;
+                p.seg_dmin[(b * p.dim + dd) * p.S + s] = m;
+            }
         }
     }
 #pragma unroll
@@ -881,6 +1153,20 @@ template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
 __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
     sscan_fwd_tma_wide(const FwdParams p, const __grid_constant__ TmaMaps tm) {
     sscan_fwd_tma_body<T, NS, P, CPL, OPT, CORR>(p, tm);
+}
+
+// Shuffle kernels (the plain scan's single and local passes): outputs summed
+// across a channel's lanes by shuffles and stored by the lanes.
+template <typename T, int NS, int P, int CPL>
+__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, 0, true>::kThreads, TmaCfg<T, NS, P, CPL, 0, true>::SH_MIN_BLOCKS)
+    sscan_fwd_tma_shfl(const FwdParams p, const __grid_constant__ TmaMaps tm) {
+    sscan_fwd_tma_body<T, NS, P, CPL, 0, false, true>(p, tm);
+}
+// ... and their carry correction (MODE_CORR)
+template <typename T, int NS, int P, int CPL>
+__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, 0, true>::kThreads, TmaCfg<T, NS, P, CPL, 0, true>::SH_MIN_BLOCKS)
+    sscan_fwd_tma_shfl_corr(const FwdParams p, const __grid_constant__ TmaMaps tm) {
+    sscan_fwd_tma_body<T, NS, P, CPL, 0, true, true>(p, tm);
 }
 
 // The kernel of a shape and pass.
@@ -948,6 +1234,76 @@ int occupancy_tma_variant() {
         return 0;
     return n;
 }
+
+// The shuffle kernel of a shape (single and local passes of the plain scan).
+template <typename T, int NS, int P, int CPL>
+cudaError_t launch_tma_shfl_variant(const FwdParams& p, int grid, cudaStream_t stream) {
+    using Cfg = TmaCfg<T, NS, P, CPL, 0, true>;
+    if (p.N < 1 || p.N > (long long)Cfg::NSP || fwd_variant(p) != 0) return cudaErrorInvalidValue;
+    const bool corr = p.mode == MODE_CORR;
+    TmaMaps tm;
+    const bool f32 = Cfg::kF32;
+    // a correction stages the local outputs where a local pass stages u
+    if (!tma_encode_3d(&tm.u, corr ? p.out : p.u, f32, p.L, p.dim, p.batch, Cfg::RROW_U, Cfg::CPW) ||
+        !tma_encode_3d(&tm.delta, p.delta, f32, p.L, p.dim, p.batch, Cfg::RROW_U, Cfg::CPW) ||
+        !tma_encode_3d(&tm.B, p.B, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP) ||
+        !tma_encode_3d(&tm.C, p.C, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP))
+        return cudaErrorInvalidValue;
+    auto kern = corr ? sscan_fwd_tma_shfl_corr<T, NS, P, CPL> : sscan_fwd_tma_shfl<T, NS, P, CPL>;
+    static unsigned long long configured[2] = {0, 0};  // bit per device ordinal (< 64), per kernel
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured[corr ? 1 : 0], __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured[corr ? 1 : 0], bit, __ATOMIC_ACQ_REL);
+    }
+    if (!corr) {
+        kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p, tm);
+        return cudaGetLastError();
+    }
+    // the correction follows the fold pass as a programmatic dependent
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, tm);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <typename T, int NS, int P, int CPL>
+int occupancy_tma_shfl_variant() {
+    using Cfg = TmaCfg<T, NS, P, CPL, 0, true>;
+    auto kern = sscan_fwd_tma_shfl<T, NS, P, CPL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Cfg::kThreads, Cfg::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+#define SSCAN_SHFL_LAUNCH_CASE(P_, NS_, CPL_) \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return launch_tma_shfl_variant<UnitT, NS_, P_, CPL_>(p, grid, st);
+#define SSCAN_SHFL_OCC_CASE(P_, NS_, CPL_) \
+    if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return occupancy_tma_shfl_variant<UnitT, NS_, P_, CPL_>();
+#define SSCAN_DEFINE_SHFL_UNIT(SUFFIX)                                                               \
+    cudaError_t fwd_shfl_launch_##SUFFIX(const FwdParams& p, Shape sh, int grid, cudaStream_t st) { \
+        SSCAN_TMA_SHFL_SHAPES(SSCAN_SHFL_LAUNCH_CASE)                                                \
+        return cudaErrorInvalidValue;                                                                \
+    }                                                                                                \
+    int fwd_shfl_occupancy_##SUFFIX(Shape sh) {                                                      \
+        SSCAN_TMA_SHFL_SHAPES(SSCAN_SHFL_OCC_CASE)                                                   \
+        return 0;                                                                                    \
+    }
 
 #define SSCAN_TMA_LAUNCH_CASE(P_, NS_, CPL_) \
     if (sh.P == P_ && sh.NS == NS_ && sh.CPL == CPL_) return launch_tma_variant<UnitT, NS_, P_, CPL_, UnitOPT>(p, grid, st);

@@ -93,8 +93,9 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     const int esz = f32 ? 4 : 2;
     const bool vec = (seqlen % (16 / esz)) == 0 && is_aligned16(u) && is_aligned16(delta) &&
                      is_aligned16(B) && is_aligned16(C) && is_aligned16(out);
-    // carry scratch of a plan with S segments: batch*dim*S*(dstate+1) floats
-    const long long per_segment = batch * dim * (dstate + 1) * (long long)sizeof(float);
+    // carry scratch of a plan with S segments: batch*dim*S*(dstate+2) floats
+    const long long per_segment =
+        batch * dim * sscan::split_floats_per_segment(dstate) * (long long)sizeof(float);
     const long long max_segments = (long long)kScratchBytes / per_segment;  // may be 0 or 1
     sscan::FwdPlan pl;
     const int prc = sscan::plan_fwd(f32, batch, dim, seqlen, dstate, segments, 0,
@@ -123,12 +124,15 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     const size_t nseg = (size_t)(batch * dim) * (size_t)S;
     p.seg_state = static_cast<float*>(scratch);
     p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
+    p.seg_dmin = p.seg_dsum + nseg;
     // pass 1: every segment from its local start, writing y and its aggregate;
-    // pass 2: add the carried state's decaying contribution (bf16 outputs are
-    // rounded twice, the second time with the carry added)
+    // pass 2: fold the aggregates into the state entering each segment (and
+    // the final state); pass 3: add the carried state's decaying contribution
+    // (bf16 outputs are rounded twice, the second time with the carry added)
     p.mode = sscan::MODE_LOCAL;
     p.seg_count = (int)S;
     e = launch(f32, p, sh, tiles * S, st);
+    if (e == cudaSuccess && S > 2) e = sscan::fwd_fold_launch(p, st);
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);

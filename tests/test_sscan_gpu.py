@@ -9,6 +9,7 @@ final_state uses the same forms (it is always float32, but inherits the
 inputs' rounding; the bound for bf16 I/O is the bf16 one).
 """
 import ctypes
+import os
 
 import numpy as np
 import pytest
@@ -101,15 +102,94 @@ LANE_CASES = [(1, 4, (1, 4, 1)), (2, 7, (2, 4, 1)), (2, 13, (2, 8, 1)), (4, 13, 
               (8, 16, (8, 2, 1)), (8, 25, (8, 4, 1)), (8, 50, (8, 8, 1)), (16, 61, (16, 4, 1))]
 
 
-def test_two_channel_shape_for_few_channels(lr):
-    # few channels and a long sequence: the plan takes two channels per lane
-    w = workloads.WORKLOADS["dim512"].scaled(batch=1, dim=48, L=4096, N=16)
+def test_shuffle_kernel_for_long_sequences(lr):
+    # a long sequence over few channels, 16-byte aligned rows: the automatic
+    # plan runs the plain scan on the shuffle kernel (two lanes of 8 states,
+    # two channels per lane) in long time segments
+    w = workloads.WORKLOADS["long64k"].scaled(batch=1, dim=1536, L=32768, N=16)
     x = workloads.make_inputs(w)
     _compare(lr, w, x, TOL["f32"])
-    assert "P=8 NS=2 CPL=2 " in lr.last_plan(), lr.last_plan()
-    wb = workloads.Workload(**{**w.__dict__, "dtype": "bf16", "h0_std": 0.2})
-    _compare(lr, wb, workloads.make_inputs(wb), TOL["bf16"])
-    assert "P=8 NS=2 CPL=2 " in lr.last_plan(), lr.last_plan()
+    plan = lr.last_plan()
+    assert "P=2 NS=8 CPL=2 " in plan and " shfl " in plan and "S=1 " not in plan, plan
+    wb = workloads.WORKLOADS["dim512"].scaled(batch=1, dim=48, L=4096, N=16)
+    wb = workloads.Workload(**{**wb.__dict__, "dtype": "bf16", "h0_std": 0.2})
+    _compare(lr, wb, workloads.make_inputs(wb), TOL["bf16"], lanes=2)
+    assert "P=2 NS=8 CPL=2 " in lr.last_plan(), lr.last_plan()
+
+
+# the shuffle kernel (plain scan, aligned rows, 8 < N <= 16; lanes=2 selects
+# it): (batch, dim, L, N, segments, use_D, use_h0)
+SHFL_CASES = [
+    (3, 70, 1004, 16, 0, True, True),     # ragged channel tile, 12-step tail chunk
+    (2, 130, 2048, 12, 0, True, True),    # N < 16: box rows past N read zeros
+    (1, 33, 4096, 16, 5, False, True),    # time split, no skip term
+    (2, 64, 996, 9, 3, True, False),      # no h0, short last segment
+    (1, 300, 64, 16, 0, True, True),      # two chunks, warps wholly past dim
+    (4, 17, 8, 16, 0, True, True),        # a partial first chunk only
+    (1, 24, 3840, 16, 40, True, True),    # many short segments: the fold over 40 aggregates
+    (1, 20, 4000, 16, 125, True, True),   # one chunk per segment
+    (2, 300, 2048, 16, 1, True, True),    # unsplit, three tiles per batch
+]
+
+
+@pytest.mark.parametrize("case", SHFL_CASES, ids=lambda c: "x".join(map(str, c[:5])))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_shuffle_kernel(lr, case, dtype):
+    batch, dim, L, N, segments, use_D, use_h0 = case
+    if dtype == "bf16" and L % 8:
+        L += 8 - L % 8  # bf16 rows are 16-byte aligned when L is a multiple of 8
+    w = workloads.WORKLOADS["long64k"].scaled(batch=batch, dim=dim, L=L, N=N)
+    w = workloads.Workload(**{**w.__dict__, "dtype": dtype})
+    plan = _compare(lr, w, workloads.make_inputs(w), TOL[dtype], segments=segments, lanes=2,
+                    use_D=use_D, use_h0=use_h0)
+    assert " shfl " in plan and "P=2 NS=8 CPL=2 " in plan, plan
+    if segments:
+        assert f"S={segments} " in plan, plan
+
+
+def test_shuffle_kernel_scalar_rate(lr):
+    """One decay rate per channel (the wide workload's kind of A) on the
+    shuffle kernel."""
+    w = workloads.WORKLOADS["wide64"].scaled(batch=2, dim=72, L=1024, N=16)
+    x = workloads.make_inputs(w)
+    for segs in (1, 4):
+        plan = _compare(lr, w, x, TOL["bf16"], segments=segs, lanes=2)
+        assert " shfl " in plan, plan
+    wf = workloads.Workload(**{**w.__dict__, "dtype": "f32"})
+    plan = _compare(lr, wf, workloads.make_inputs(wf), TOL["f32"], segments=3, lanes=2)
+    assert " shfl " in plan, plan
+
+
+@pytest.mark.parametrize("lanes", [0, 2, 4, 8])
+def test_growing_states_split_matches_unsplit_and_oracle(lr, lanes):
+    """Decay factors above one: some rates A > 0 and a few negative steps.  The
+    carry correction must then follow every carried state to the end of its
+    segment (its cut-off assumes states that only decay), so time-split plans
+    compute what the unsplit plan and the oracle compute."""
+    w = workloads.WORKLOADS["dim512"].scaled(batch=2, dim=40, L=512, N=16)
+    x = workloads.make_inputs(w)
+    A = x["A"].clone()
+    A[::4, 3] = 0.02              # growing states in every fourth channel
+    x["A"] = A
+    d = x["delta"].clone()
+    d[1::5, :, 120:124] = -0.05   # negative steps in some channels
+    x["delta"] = d
+    x["u"] = x["u"] * 0.1
+    g = _dev(x)
+    y1, h1 = lr.sscan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["h0"],
+                          segments=1, lanes=lanes)
+    for segs in (4, 16):
+        plan = _compare(lr, w, x, TOL["f32"], lanes=lanes, segments=segs)
+        assert f"S={segs} " in plan, plan
+        y, hT = lr.sscan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["h0"],
+                             segments=segs, lanes=lanes)
+        torch.cuda.synchronize()
+        assert _rel_err(y.double().cpu().numpy(), y1.double().cpu().numpy()) <= TOL["f32"]
+        assert _rel_err(hT.double().cpu().numpy(), h1.double().cpu().numpy()) <= TOL["f32"]
+    # growth alone: mixed-sign A with positive delta
+    x2 = dict(x)
+    x2["delta"] = workloads.make_inputs(w)["delta"]
+    _compare(lr, w, x2, TOL["f32"], lanes=lanes, segments=4)
 
 
 @pytest.mark.parametrize("lanes,N,shape", LANE_CASES, ids=lambda v: str(v))
@@ -335,28 +415,30 @@ def test_output_guard_bands_untouched(lr):
 
 # --------------------------------------------------------------------------
 # full-size workloads in the automatic launch plan (the one the benchmark
-# times), checked on sampled channels the oracle computes one by one
+# times), every output element and every final state against the oracle
 
 FULL = ["dim512", "bf16_2k", "long64k", "wide64"]
 
 
+def _rel_err_rows(got, ref):
+    """max |got - ref| / (1 + |ref|) over [batch, dim, ...] arrays, one batch
+    row at a time (keeps the temporaries of the largest workloads small)."""
+    worst = 0.0
+    for b in range(got.shape[0]):
+        worst = max(worst, _rel_err(got[b], ref[b]))
+    return worst
+
+
 @pytest.mark.parametrize("name", FULL)
-def test_workload_full_size_sampled(lr, name):
+def test_workload_full_size_every_element(lr, name):
     w = workloads.WORKLOADS[name]
     x = workloads.make_inputs(w)
     y, hT, plan = _run(lr, x)
-    rng = np.random.default_rng(99)
-    chans = {(0, 0), (w.batch - 1, w.dim - 1)}
-    while len(chans) < 24:
-        chans.add((int(rng.integers(w.batch)), int(rng.integers(w.dim))))
-    chans = sorted(chans)
-    yr, hr = oracle.sscan_fwd_channels(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"],
-                                       x["h0"], chans)
-    ys = np.stack([y[b, d] for b, d in chans])
-    hs = np.stack([hT[b, d] for b, d in chans])
-    ey, eh = _rel_err(ys, yr), _rel_err(hs, hr)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(hT))
+    yr, hr = oracle.sscan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["h0"],
+                              nthreads=os.cpu_count() or 1)
+    ey, eh = _rel_err_rows(y, yr), _rel_err_rows(hT, hr)
     assert ey <= TOL[w.dtype] and eh <= TOL[w.dtype], f"{name} [{plan}]: {ey:.3e} {eh:.3e}"
-    assert np.all(np.isfinite(y))
 
 
 def test_pipelined_end_to_end_steps_return_the_scan(lr):
