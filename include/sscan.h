@@ -66,9 +66,19 @@ enum {
  * default stream).
  *
  * Scratch: long sequences with few channels are split in time; the split
- * needs batch*dim*segments*(dstate+1) floats of scratch, taken stream-ordered
+ * needs batch*dim*segments*(dstate+2) floats of scratch, taken stream-ordered
  * from the library's memory pool on the current device (which keeps up to
  * 1 GiB mapped while idle) and returned on the same stream.
+ *
+ * Time splits and the domain of delta: each segment after the first adds the
+ * decaying contribution of its entry state to the outputs, and stops once
+ * every carried state has decayed below 2^-24 of its entry magnitude.  That
+ * cut-off is exact (to float32 rounding) while every decay factor
+ * exp(delta*A) is at most 1, i.e. delta >= 0 (a step size, as softplus
+ * produces) and A <= 0.  Rates A > 0 are always detected and the carries are
+ * then followed to each segment's end; negative delta values lie outside the
+ * stated domain (delta >= 0), but are detected the same way by every pass
+ * except the 16-state-lane TMA-fed one (dstate > 32).
  */
 int sscan_fwd(const void *u, const void *delta, const float *A, const void *B,
               const void *C, const float *D, const float *h0, void *out,
@@ -79,8 +89,10 @@ int sscan_fwd(const void *u, const void *delta, const float *A, const void *B,
  * sscan_fwd_ex -- sscan_fwd with the launch plan pinned, for testing and
  * tuning.  segments: number of time segments per channel (0 = automatic; 1 =
  * no time split); lanes: lanes per channel sharing the state vector (0 =
- * automatic; 1, 2 or 4, subject to dstate <= 16*lanes).  Results are the same
- * computation under any plan (up to float32 rounding order).
+ * automatic; 1, 2, 4, 8 or 16, subject to dstate <= 16*lanes; with 16-byte
+ * aligned rows and 8 < dstate <= 16, lanes = 2 selects the kernel whose lanes
+ * sum their partial outputs by shuffles).  Results are the same computation
+ * under any plan (up to float32 rounding order).
  */
 int sscan_fwd_ex(const void *u, const void *delta, const float *A, const void *B,
                  const void *C, const float *D, const float *h0, void *out,
@@ -202,17 +214,20 @@ int sscan_step(const void *u, const void *delta, const float *A, const void *B,
  * caller still passes every input and output.
  *
  * Arguments are those of sscan_fwd plus segments: 0 picks the time split
- * automatically, shrunk so that its carry (batch*dim*segments*(dstate+1)
+ * automatically, shrunk so that its carry (batch*dim*segments*(dstate+2)
  * floats) fits the array; a positive value pins it, and a pinned split whose
  * carry does not fit is rejected with SSCAN_ERR_INVALID before anything is
- * launched.  The result equals sscan_fwd's under the same plan.
+ * launched.  The passes run on the library's cp.async-fed kernels (the
+ * general path of sscan_fwd, whatever the row alignment), so the results
+ * agree with sscan_fwd's up to float32 rounding order, and within the same
+ * tolerances against the definition.
  *
  * The first call on each device looks up the array's address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
  * first call before any stream capture.  All calls share the array and each
  * call writes everything it reads from it, so no clearing is needed, but
  * calls whose kernels may overlap on the GPU (unordered streams) race on it.
- * sscan_last_launch_count() and sscan_last_plan() do not describe these calls.
+ * sscan_last_launch_count() and sscan_last_plan() describe these calls too.
  */
 int sscan_fwd_noalloc(const void *u, const void *delta, const float *A, const void *B,
                       const void *C, const float *D, const float *h0, void *out,

@@ -139,6 +139,9 @@ void record_call(int launches, cudaStream_t stream, const char* plan) {
     snprintf(g_rec.plan, sizeof(g_rec.plan), "%s", plan);
 }
 void record_error(cudaError_t e) { fail_cuda(e); }
+// The device status word of the current device (nullptr if it cannot be
+// found); looking it up allocates nothing.
+int* device_status_word() { return device_status_ptr(); }
 
 // Warps per SM the automatic plan aims for when it splits time: about three
 // per scheduler, enough to cover the FMA/MUFU and shared-memory latencies of

@@ -64,6 +64,14 @@ struct TmaMaps {
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// Register ceiling of the 16-state-lane kernel without the zero-order hold
+// (two CTAs per SM fit in any case; left unbounded, the allocation drifted with
+// unrelated code changes from 167 to 215 registers and wide64 from 452 to 469
+// us; 176 is the lowest that spills nothing).
+#ifndef SSCAN_WIDE_MAXNREG
+#define SSCAN_WIDE_MAXNREG 176
+#endif
+
 // Steps per chunk of the shuffle kernels, and the most resident CTAs per SM
 // their register allocation is asked for (8 states per lane).
 #ifndef SSCAN_SHFL_CHUNK
@@ -447,10 +455,15 @@ __device__ __forceinline__ void compute_chunk_shfl(const TU* su, const TU* sd, c
 }
 
 // SH kernels, carry correction: one chunk of the homogeneous recurrence
-// h = exp(delta*A)*h from the carried state, its C-contraction summed over the
-// channel's lanes as in compute_chunk_shfl, added to the local outputs (staged
-// in the u rows, sy) and stored.  live[k] (warp-uniform) skips the state slots
-// whose carry has decayed below the threshold in every lane of the warp.
+// h = exp(delta*A)*h from the carried state, in closed form within the chunk:
+// with S_t the sum of delta from the chunk's start through step t (per
+// channel), h_t = 2^(A log2e S_t) h_start, so no step waits on the previous
+// one; h advances by the whole chunk's decay at its end.  The C-contraction is
+// summed over the channel's lanes as in compute_chunk_shfl, added to the local
+// outputs (staged in the u rows, sy) and stored.  live[k] (warp-uniform)
+// skips the quads of state slots whose carry has decayed below the threshold
+// in every lane of the warp (their states are not advanced: they stay below
+// it, decay factors being at most 1 whenever slots are skipped).
 template <typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
 __device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, const float* sC, const int (&rl)[2],
                                                  int g, const float (&Al2)[2][NS], const float (&As)[2],
@@ -460,41 +473,47 @@ __device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, con
     constexpr int NB = TC / 4, QS = 4, NQ = NS / QS;
     constexpr unsigned FULL = 0xffffffffu;
     const float* bC = sC + g * FROW;
+    bool lq[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        lq[q] = false;
+#pragma unroll
+        for (int kk = 0; kk < QS; ++kk) lq[q] |= live[q * QS + kk];
+    }
+    float sacc[CPL] = {0.f, 0.f};  // sum of delta since the chunk's start
 #pragma unroll 2
     for (int blk = 0; blk < NB; ++blk) {
         const int t4 = 4 * blk;
-        float dd[CPL][4], as[CPL][4], y[CPL][4], yl[4];
+        float sc[CPL][4], es[CPL][4], y[CPL][4], yl[4];
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            load4_smem(sd + rl[j] * UROW + t4, dd[j]);
+            float dv[4];
+            load4_smem(sd + rl[j] * UROW + t4, dv);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                as[j][s] = SCALAR ? ex2(dd[j][s] * As[j]) : 0.f;
+                sacc[j] += dv[s];
+                sc[j][s] = sacc[j];
+                es[j][s] = SCALAR ? ex2(sc[j][s] * As[j]) : 0.f;
                 y[j][s] = 0.f;
             }
         }
         load4_smem(sy + rl[0] * UROW + t4, yl);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            bool lq = false;
-#pragma unroll
-            for (int kk = 0; kk < QS; ++kk) lq |= live[q * QS + kk];
-            if (!lq) continue;
+            if (!lq[q]) continue;
             float cc[QS][4];
 #pragma unroll
             for (int kk = 0; kk < QS; ++kk) load4_smem(bC + (q * QS + kk) * P * FROW + t4, cc[kk]);
 #pragma unroll
-            for (int kk = 0; kk < QS; ++kk) {
-                const int k = q * QS + kk;
-                if (!live[k]) continue;
+            for (int s = 0; s < 4; ++s)
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
+                for (int j = 0; j < CPL; ++j)
 #pragma unroll
-                    for (int j = 0; j < CPL; ++j) {
-                        h[j][k] *= SCALAR ? as[j][s] : ex2(dd[j][s] * Al2[j][k]);
-                        y[j][s] = fmaf(cc[kk][s], h[j][k], y[j][s]);
+                    for (int kk = 0; kk < QS; ++kk) {
+                        const int k = q * QS + kk;
+                        const float e = SCALAR ? es[j][s] : ex2(sc[j][s] * Al2[j][k]);
+                        y[j][s] = fmaf(cc[kk][s], h[j][k] * e, y[j][s]);
                     }
-            }
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[1][s], P / 2);
@@ -516,6 +535,14 @@ __device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, con
                 *reinterpret_cast<uint2*>(orow + t4) = make_uint2(lo, hi);
             }
         }
+    }
+    // advance the live states over the chunk
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const float ech = SCALAR ? ex2(sacc[j] * As[j]) : 0.f;
+#pragma unroll
+        for (int k = 0; k < NS; ++k)
+            if (lq[k / QS]) h[j][k] *= SCALAR ? ech : ex2(sacc[j] * Al2[j][k]);
     }
 }
 
@@ -800,9 +827,17 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     const bool dsum_on = !CORR && p.mode == MODE_LOCAL;
     // Kahan sums of delta per slot (a slot is the same channel row and 4-step
     // offset in both halves)
-    float dsum[Cfg::IPH], dcomp[Cfg::IPH], dmin[Cfg::IPH];  // and min(0, smallest delta)
+    float dsum[Cfg::IPH], dcomp[Cfg::IPH];
 #pragma unroll
-    for (int k = 0; k < Cfg::IPH; ++k) dsum[k] = dcomp[k] = dmin[k] = 0.f;
+    for (int k = 0; k < Cfg::IPH; ++k) dsum[k] = dcomp[k] = 0.f;
+    // min(0, smallest delta) of the lane's item slots; the warp's minimum is
+    // recorded for all of its channels (negative steps are rare: a correction
+    // then follows its carries to the segment end).  Narrow lanes only: in
+    // the 16-state-lane kernel this tracking measured 4% slower (wide64 448 ->
+    // 470 us, the same with sign bits or in the compute loop), and its
+    // segments are recorded as free of negative steps, the domain the header
+    // states (delta >= 0).
+    float dmin = 0.f;
     float Dr[Cfg::IPH];
 #pragma unroll
     for (int k = 0; k < Cfg::IPH; ++k) {
@@ -858,7 +893,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 const float tk = dsum[k] + yk;
                 dcomp[k] = (tk - dsum[k]) - yk;
                 dsum[k] = tk;
-                dmin[k] = fminf(dmin[k], fminf(fminf(dv[0], dv[1]), fminf(dv[2], dv[3])));
+                if constexpr (NS <= 4) dmin = fminf(dmin, fminf(fminf(dv[0], dv[1]), fminf(dv[2], dv[3])));
             }
             if (dd < p.dim && t < t_end) {  // t_end is a multiple of 4 on this path
                 T* o = gout + (b * p.dim + dd) * p.L + t;
@@ -1111,13 +1146,12 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
             p.seg_dmin[ch[0] * p.S + s] = sh_dmin;
         }
     } else if (dsum_on) {  // the segment's sum of delta per channel: 4 slots in 4 lanes
+        const float m = __any_sync(FULL, dmin < 0.f) ? -1.f : 0.f;
 #pragma unroll
         for (int k = 0; k < Cfg::IPH; ++k) {
-            float v = dsum[k], m = dmin[k];
+            float v = dsum[k];
             v += __shfl_xor_sync(FULL, v, 1);
             v += __shfl_xor_sync(FULL, v, 2);
-            m = fminf(m, __shfl_xor_sync(FULL, m, 1));
-            m = fminf(m, __shfl_xor_sync(FULL, m, 2));
             const long long dd = dw + (lane + 32 * k) / 4;
             if ((lane & 3) == 0 && dd < p.dim) {
                 p.seg_dsum[(b * p.dim + dd) * p.S + s] = v;
@@ -1146,11 +1180,11 @@ __global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads, TmaCfg<T
     sscan_fwd_tma_body<T, NS, P, CPL, OPT, CORR>(p, tm);
 }
 
-// Wide lanes (16 states): no such request; every one tried (two or three
-// CTAs per SM) gave a slower schedule at the same or more registers
-// (wide64 458 / 462 us against 452 us).
+// Wide lanes (16 states): no request for resident CTAs (two or three CTAs per
+// SM gave slower schedules: wide64 458 / 462 us against 452 us), but a
+// register ceiling (its launches use kThreads = 128 threads per CTA).
 template <typename T, int NS, int P, int CPL, int OPT, bool CORR>
-__global__ void __launch_bounds__(TmaCfg<T, NS, P, CPL, OPT>::kThreads)
+__global__ void __maxnreg__(OPT == 2 ? 255 : SSCAN_WIDE_MAXNREG)
     sscan_fwd_tma_wide(const FwdParams p, const __grid_constant__ TmaMaps tm) {
     sscan_fwd_tma_body<T, NS, P, CPL, OPT, CORR>(p, tm);
 }

@@ -26,8 +26,16 @@
 #include <algorithm>
 #include <mutex>
 
+#include <stdio.h>
+
 #include "../../include/sscan.h"
 #include "sscan_dispatch.cuh"
+
+namespace sscan {
+// call record and device status word of the entry points (sscan_abi.cu)
+void record_call(int launches, cudaStream_t stream, const char* plan);
+int* device_status_word();
+}  // namespace sscan
 
 namespace {
 
@@ -69,6 +77,7 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
                                  float* final_state, int64_t batch, int64_t dim, int64_t seqlen,
                                  int64_t dstate, int dtype, int segments, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    sscan::record_call(0, st, "rejected");
     if (dtype != SSCAN_F32 && dtype != SSCAN_BF16) return SSCAN_ERR_INVALID;
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || dstate > sscan::kMaxDstate ||
         segments < 0)
@@ -77,8 +86,12 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     if (batch > big || dim > big || seqlen > big || (batch && dim > big / batch) ||
         (batch * dim && seqlen > big / (batch * dim)))
         return SSCAN_ERR_INVALID;
-    if (batch == 0 || dim == 0) return SSCAN_OK;
+    if (batch == 0 || dim == 0) {
+        sscan::record_call(0, st, "empty");
+        return SSCAN_OK;
+    }
     if (seqlen == 0) {
+        sscan::record_call(0, st, "seqlen 0: final_state = h0");
         if (final_state) {
             const size_t bytes = (size_t)(batch * dim * dstate) * sizeof(float);
             cudaError_t e = h0 ? cudaMemcpyAsync(final_state, h0, bytes, cudaMemcpyDeviceToDevice, st)
@@ -105,18 +118,26 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     const long long S = pl.S, tiles = pl.tiles, Tseg = pl.Tseg, tiles_per_batch = pl.tiles_per_batch;
     if (S > 1 && S > max_segments) return SSCAN_ERR_INVALID;  // would overflow the fixed scratch
 
+    int* status = sscan::device_status_word();
+    if (status == nullptr) return SSCAN_ERR_CUDA;
     sscan::FwdParams p{};
     p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.h0 = h0;
     p.out = out; p.final_state = final_state;
     p.batch = batch; p.dim = dim; p.L = seqlen; p.N = dstate;
     p.Tseg = Tseg; p.S = (int)S; p.tiles_per_batch = (int)tiles_per_batch;
     p.vec = vec ? 1 : 0;
+    p.status = status;
+    char plan[160];
+    snprintf(plan, sizeof(plan), "noalloc %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld cp.async %s",
+             f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, Tseg,
+             S == 1 ? "single" : S == 2 ? "local+correct" : "local+fold+correct");
 
     cudaError_t e;
     if (S == 1) {
         p.mode = sscan::MODE_SINGLE;
         p.seg_count = 1;
         e = launch(f32, p, sh, tiles, st);
+        sscan::record_call(1, st, plan);
         return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
     }
     void* scratch = nullptr;
@@ -138,5 +159,6 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
         p.seg_count = (int)(S - 1);
         e = launch(f32, p, sh, tiles * (S - 1), st);
     }
+    sscan::record_call(S > 2 ? 3 : 2, st, plan);
     return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
