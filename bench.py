@@ -1,14 +1,19 @@
 """Benchmark: selective-scan forward on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dim512] [--no-extra]
+                    [--workload long64k] [--no-extra]
 
 A step is one sscan_fwd call (load, discretise, recurrence, carry, output,
 final state) over the workload's whole batch, with inputs resident in HBM.
-Between timed steps a 512 MB buffer is written so the 51 MB working set starts
-from DRAM, not L2.  Each step is timed with CUDA events on the launch stream;
+The headline workload is the largest configuration, long64k (1536 channels x
+65536 steps, 16 states, fp32, 1.2 GB per call); the other configurations are
+timed the same way under ``per_workload``, each with its own clock record.
+Between timed steps a 512 MB buffer is written so that inputs smaller than L2
+start from DRAM.  Each step is timed with CUDA events on the launch stream;
 ``value`` is tokens*channels/s = batch*dim*L / (mean step time), summed over
-ranks (every rank runs its own copy of the workload: weak scaling).
+ranks (every rank runs its own copy of the workload: weak scaling).  The
+exponent unit's peak of the roofline is measured in the same run
+(``sscan_probe_ex2``); HBM bandwidth comes from MEASURED_PEAKS.json.
 
 ``e2e`` is the same metric through the public Python call with pinned host
 buffers: per step the inputs are copied host->device, the scan runs, and the
@@ -44,8 +49,8 @@ import workloads  # noqa: E402
 METRIC = ("selective-scan fwd tokens×channels/s, HBM GB/s and % of roofline on 1 GB300")
 UNIT = "tokens*channels/s"
 SM_COUNT = 152
-MUFU_PER_CLK_SM = 32     # ex2 lanes per clock per SM (GB300)
-FP32_PER_CLK_SM = 128    # FP32 lanes per clock per SM
+MUFU_PER_CLK_SM = 32     # ex2 lanes per clock per SM, nominal (used only if the probe fails)
+FP32_PER_CLK_SM = 128    # FP32 lanes per clock per SM (unit count)
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
@@ -85,12 +90,34 @@ def algorithmic(w: workloads.Workload):
     return {"bytes": nbytes, "exps": exps, "fp32": fp32, "tokens_channels": bdl, "elements": elems}
 
 
+def measure_ex2(dev, stream, reps=3):
+    """Exponentials per second of the MUFU unit on this GPU, from the
+    library's probe (every SM full: 8 CTAs of 256 threads per SM), best of
+    ``reps`` CUDA-event timings after a warm-up launch."""
+    import torch
+    import linear_recurrence_gb300 as lr
+    blocks, iters = SM_COUNT * 8, 2000
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    lr.probe_ex2(blocks, iters, sink=sink, stream=stream)
+    best = None
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        n = lr.probe_ex2(blocks, iters, sink=sink, stream=stream)
+        e.record(stream)
+        e.synchronize()
+        t = s.elapsed_time(e) * 1e-3
+        best = t if best is None else min(best, t)
+    return n / best
+
+
 def roofline(w, t_s, pk):
     a = algorithmic(w)
     clk = pk["sm_max_mhz"] * 1e6
     bw = pk["hbm_gbs"] * 1e9
+    ex2_rate = pk.get("ex2_per_s") or MUFU_PER_CLK_SM * SM_COUNT * clk
     t_hbm = a["bytes"] / bw
-    t_exp = a["exps"] / (MUFU_PER_CLK_SM * SM_COUNT * clk)
+    t_exp = a["exps"] / ex2_rate
     t_fp32 = a["fp32"] / (FP32_PER_CLK_SM * SM_COUNT * clk)
     t_roof = max(t_hbm, t_exp, t_fp32)
     achieved_gbs = a["bytes"] / t_s / 1e9
@@ -100,14 +127,15 @@ def roofline(w, t_s, pk):
     else:
         # an ALU-bound scan: express the rate in the binding unit's operations
         if t_exp >= t_fp32:
-            peak = MUFU_PER_CLK_SM * SM_COUNT * clk / 1e12
+            peak = ex2_rate / 1e12
             r = {"bound": "alu", "achieved": a["exps"] / t_s / 1e12, "peak": peak,
                  "unit": "Texp/s (MUFU ex2)", "frac": (a["exps"] / t_s / 1e12) / peak}
         else:
             peak = FP32_PER_CLK_SM * SM_COUNT * clk / 1e12
             r = {"bound": "alu", "achieved": a["fp32"] / t_s / 1e12, "peak": peak,
                  "unit": "T FP32 lane-ops/s", "frac": (a["fp32"] / t_s / 1e12) / peak}
-    r.update({"peak_source": pk["source"], "t_roofline_us": t_roof * 1e6,
+    r.update({"peak_source": pk["source"], "ex2_peak_source": pk.get("ex2_source", "nominal"),
+              "ex2_peak_texp_s": ex2_rate / 1e12, "t_roofline_us": t_roof * 1e6,
               "t_hbm_us": t_hbm * 1e6, "t_exp_us": t_exp * 1e6, "t_fp32_us": t_fp32 * 1e6,
               "hbm_gbs": achieved_gbs, "frac_of_roofline": t_roof / t_s})
     return r
@@ -511,7 +539,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dim512", choices=list(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="long64k", choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads, pscan and the CPU baseline")
     args = ap.parse_args()
@@ -555,6 +583,11 @@ def main():
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     pk = peaks()
+    try:
+        pk["ex2_per_s"] = measure_ex2(dev, stream)
+        pk["ex2_source"] = "measured in this run (sscan_probe_ex2)"
+    except Exception as exc:  # pragma: no cover - reported, nominal figure used
+        pk["ex2_source"] = f"nominal 32/clk/SM (probe failed: {exc})"
 
     barrier(ws, dev)
     torch.cuda.synchronize(dev)
@@ -573,23 +606,33 @@ def main():
     cpu = None
     if rank == 0 and not args.no_extra:
         per = {}
-        for name in ["bf16_2k", "long64k", "wide64"]:
+        for name in ["dim512", "bf16_2k", "long64k", "wide64"]:
             if name == w.name:
                 continue
             wx = workloads.WORKLOADS[name]
-            r = bench_workload(wx, max(5, args.steps // 2), 3, dev, stream, flush)
+            with ClockSampler(physical_gpu(dev.index or 0)) as ckx:
+                r = bench_workload(wx, max(5, args.steps // 2), 3, dev, stream, flush)
             rfx = roofline(wx, r["t"], pk)
             per[name] = {"ms": r["t"] * 1e3,
                          "value": wx.channels * wx.L / r["t"], "unit": UNIT,
                          "hbm_gbs": rfx["hbm_gbs"], "bound": rfx["bound"],
                          "frac": rfx["frac"], "frac_of_roofline": rfx["frac_of_roofline"],
-                         "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"]}
-        per["bf16_2k_bwd"] = bench_bwd(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3, dev,
-                                       stream, flush, pk, per.get("bf16_2k", {}).get("ms", 0) * 1e-3)
-        per["bf16_2k_fused"] = bench_fused(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3,
-                                           dev, stream, flush, pk)
-        per["pscan_8k"] = bench_pscan(max(5, args.steps // 2), 3, dev, stream, flush)
-        per["decode_step"] = bench_step(max(5, args.steps // 2), 3, dev, stream, flush, pk)
+                         "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"],
+                         "clocks": ckx.summary()}
+        with ClockSampler(physical_gpu(dev.index or 0)) as ckx:
+            per["bf16_2k_bwd"] = bench_bwd(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3, dev,
+                                           stream, flush, pk, per.get("bf16_2k", {}).get("ms", 0) * 1e-3)
+        per["bf16_2k_bwd"]["clocks"] = ckx.summary()
+        with ClockSampler(physical_gpu(dev.index or 0)) as ckx:
+            per["bf16_2k_fused"] = bench_fused(workloads.WORKLOADS["bf16_2k"], max(5, args.steps // 2), 3,
+                                               dev, stream, flush, pk)
+        per["bf16_2k_fused"]["clocks"] = ckx.summary()
+        with ClockSampler(physical_gpu(dev.index or 0)) as ckx:
+            per["pscan_8k"] = bench_pscan(max(5, args.steps // 2), 3, dev, stream, flush)
+        per["pscan_8k"]["clocks"] = ckx.summary()
+        with ClockSampler(physical_gpu(dev.index or 0)) as ckx:
+            per["decode_step"] = bench_step(max(5, args.steps // 2), 3, dev, stream, flush, pk)
+        per["decode_step"]["clocks"] = ckx.summary()
         extra["per_workload"] = per
         rate, cores, sample, _ = oracle_rate(w, budget_s=10.0)
         rate1, _, sample1, _ = oracle_rate(w, budget_s=3.0, nthreads=1)
@@ -600,7 +643,9 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-                "config": {"workload": wdesc, "l2": "512 MB buffer written before every step",
+                "config": {"workload": wdesc,
+                           "l2": ("inputs larger than L2; " if algorithmic(w)["bytes"] > (129 << 20) else "")
+                           + "a 512 MB buffer written before every step",
                            "plan": res["plan"], "parallelism": f"{ws} independent replicas"},
                 "roofline": rf,
                 "cpu_baseline": cpu,

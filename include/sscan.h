@@ -259,6 +259,22 @@ int sscan_get_last_error(void);
  */
 void sscan_debug_expire_next_wait(unsigned int wait_limit_us);
 
+/*
+ * sscan_probe_ex2 -- a measurement aid for the roofline of the scan; the
+ * pages have no counterpart.  It launches `blocks` CTAs of 256 threads on
+ * `stream`, each thread running 16 independent chains of `iters` exponentials
+ * 2^x on the MUFU unit -- the operation every element of the scan takes (one
+ * per channel and step for a channel with a single rate).  Timing the launch
+ * with CUDA events and dividing sscan_probe_ex2_count(blocks, iters) by the
+ * time gives the unit's throughput on this GPU.  sink: device float32
+ * [blocks*256], required (it keeps the work alive and is not written in
+ * practice).  Returns SSCAN_OK, SSCAN_ERR_INVALID (sink NULL, blocks or iters
+ * < 1) or SSCAN_ERR_CUDA (launch failure).
+ */
+int sscan_probe_ex2(float *sink, int blocks, int iters, void *stream);
+/* Exponentials one sscan_probe_ex2 launch computes. */
+long long sscan_probe_ex2_count(int blocks, int iters);
+
 /* Largest dstate that sscan_fwd accepts. */
 int sscan_max_dstate(void);
 

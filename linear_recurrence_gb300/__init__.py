@@ -50,6 +50,8 @@ SIGNATURES = {
     "sscan_get_last_error": (_int, []),
     "sscan_max_dstate": (_int, []),
     "sscan_debug_expire_next_wait": (None, [ctypes.c_uint]),
+    "sscan_probe_ex2": (_int, [_fp, _int, _int, _vp]),
+    "sscan_probe_ex2_count": (ctypes.c_longlong, [_int, _int]),
     "sscan_last_launch_count": (_int, []),
     "sscan_last_plan": (ctypes.c_char_p, []),
 }
@@ -99,6 +101,18 @@ def get_last_error() -> int:
 
 def max_dstate() -> int:
     return int(lib().sscan_max_dstate())
+
+
+def probe_ex2(blocks: int, iters: int, *, sink=None, stream=None) -> int:
+    """Launch the exponent-unit throughput probe (see include/sscan.h) on the
+    current device; returns the number of exponentials it computes.  Time it
+    with CUDA events on ``stream``."""
+    if sink is None:
+        sink = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    rc = lib().sscan_probe_ex2(_ptr(sink), int(blocks), int(iters), _stream_handle(stream))
+    if rc != SSCAN_OK:
+        raise SscanError(rc, "sscan_probe_ex2")
+    return int(lib().sscan_probe_ex2_count(int(blocks), int(iters)))
 
 
 def debug_expire_next_wait(wait_limit_us: int) -> None:

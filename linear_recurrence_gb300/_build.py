@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsscan.so")
-UNITS = ["sscan_abi.cu", "sscan_fold.cu", "sscan_noalloc.cu", "sscan_step.cu", "sscan_bwd.cu", "sscan_fwd_tma.cu"] + [
+UNITS = ["sscan_abi.cu", "sscan_fold.cu", "sscan_probe.cu", "sscan_noalloc.cu", "sscan_step.cu", "sscan_bwd.cu", "sscan_fwd_tma.cu"] + [
     f"sscan_fwd_tma_{dt}_{var}.cu" for dt in ("f32", "bf16") for var in "eoz"] + [
     f"sscan_fwd_shfl_{dt}.cu" for dt in ("f32", "bf16")] + [
     f"sscan_fwd_{dt}_{part}_{var}.cu" for dt in ("f32", "bf16") for part in "ab" for var in "eoz"]
