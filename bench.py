@@ -542,9 +542,15 @@ def main():
     ap.add_argument("--workload", default="long64k", choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads, pscan and the CPU baseline")
+    ap.add_argument("--size", default=None,
+                    help="BATCHxDIMxL: the workload's recipe at other sizes (smaller cases of the same "
+                         "kernels for profiler captures; not a bench line of the configuration)")
     args = ap.parse_args()
     ws, rank, local = _dist()
     w = workloads.WORKLOADS[args.workload]
+    if args.size:
+        b_, d_, l_ = (int(v) for v in args.size.lower().split("x"))
+        w = w.scaled(batch=b_, dim=d_, L=l_)
     wdesc = (f"{w.name}: batch={w.batch}, dim={w.dim}, L={w.L}, N={w.N}, {w.dtype} I/O, "
              f"delta=softplus(N({w.delta_mu},{w.delta_sigma})), A={w.A_kind}"
              + (f", h0~N(0,{w.h0_std}^2)" if w.h0_std > 0 else ""))
