@@ -148,7 +148,7 @@ def kernel_source_hash():
     csrc = os.path.join(_ROOT, "linear_recurrence_gb300", "csrc")
     files = [os.path.join(csrc, n) for n in ("device_utils.cuh", "sscan_fwd_kernel.cuh",
                                              "sscan_fwd_tma.cuh", "sscan_fwd_tma.cu",
-                                             "sscan_dispatch.cuh", "sscan_abi.cu")]
+                                             "sscan_dispatch.cuh", "sscan_abi.cu", "sscan_fold.cu")]
     files += glob.glob(os.path.join(csrc, "sscan_fwd_*_*.cu"))
     for p in sorted(files):
         with open(p, "rb") as f:
