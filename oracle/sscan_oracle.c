@@ -79,7 +79,9 @@ enum {
     MUT_GATE_BEFORE_D = 11,  /* gate y, then add D*u ungated                 */
     MUT_ZOH_NO_DIV = 12,     /* ZOH B-bar = expm1(delta*A) * B (1/A dropped) */
     MUT_ZOH_DELTA_TWICE = 13, /* ZOH B-bar = expm1(delta*A)/A * delta*B      */
-    MUT_COUNT = 14
+    MUT_COUNT = 14,
+    MUT_COPY = 100           /* no mistake, but through the copy that carries
+                                them: it must equal the definition exactly    */
 };
 
 enum { FLAG_SOFTPLUS = 1, FLAG_ZOH = 2 };
@@ -97,7 +99,52 @@ typedef struct {
     int flags;                     /* FLAG_SOFTPLUS | FLAG_ZOH           */
 } sscan_job;
 
+/* The definition, one channel at a time and one step at a time (the
+ * pseudocode of section 2.3 with the options listed above). */
 static void sscan_channels(const sscan_job *j)
+{
+    const int64_t L = j->L, N = j->N, dim = j->dim;
+    double *h = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    for (int64_t ch = j->first; ch < j->last; ++ch) {
+        const int64_t b = ch / dim, d = ch % dim;
+        const double *u = j->u + ch * L;      /* u[b, d, :]     */
+        const double *dl = j->delta + ch * L; /* delta[b, d, :] */
+        const double *Ad = j->A + d * N;      /* A[d, :]        */
+        const double *Bb = j->B + b * N * L;  /* B[b, :, :]     */
+        const double *Cb = j->C + b * N * L;  /* C[b, :, :]     */
+        double *y = j->out + ch * L;
+        for (int64_t n = 0; n < N; ++n) h[n] = j->h0 ? j->h0[ch * N + n] : 0.0;
+        const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double dt = dl[t] + bias;
+            if (j->flags & FLAG_SOFTPLUS) dt = softplus(dt);
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = exp(dt * Ad[n]); /* A-bar */
+                double bbar = dt;                 /* B-bar per unit B: delta (Euler) ... */
+                if ((j->flags & FLAG_ZOH) && Ad[n] != 0.0) bbar = expm1(dt * Ad[n]) / Ad[n]; /* ... or ZOH */
+                h[n] = a * h[n] + bbar * Bb[n * L + t] * u[t];
+            }
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) acc += Cb[n * L + t] * h[n];
+            const double skip = j->D ? j->D[d] * u[t] : 0.0;
+            if (j->z) {
+                const double zv = j->z[ch * L + t];
+                acc = (acc + skip) * (zv * (1.0 / (1.0 + exp(-zv)))); /* (y + D u) silu(z) */
+            } else {
+                acc += skip;
+            }
+            y[t] = acc;
+        }
+        if (j->final_state)
+            for (int64_t n = 0; n < N; ++n) j->final_state[ch * N + n] = h[n];
+    }
+    free(h);
+}
+
+/* A copy of sscan_channels carrying the planted mistakes of the pin tests
+ * (which check that every plausible slip fails at least one pin); with
+ * MUT_NONE it computes exactly what sscan_channels computes. */
+static void sscan_channels_mutant(const sscan_job *j)
 {
     const int64_t L = j->L, N = j->N, dim = j->dim;
     double *h = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
@@ -171,9 +218,17 @@ static void sscan_channels(const sscan_job *j)
     free(hprev);
 }
 
+static void sscan_run(const sscan_job *j)
+{
+    if (j->mutation == MUT_NONE)
+        sscan_channels(j);
+    else
+        sscan_channels_mutant(j);
+}
+
 static void *sscan_thread(void *arg)
 {
-    sscan_channels((const sscan_job *)arg);
+    sscan_run((const sscan_job *)arg);
     return NULL;
 }
 
@@ -188,14 +243,14 @@ int oracle_sscan_fwd_full_mutant(const double *u, const double *delta, const dou
                                  int flags, int nthreads, int mutation)
 {
     if (batch < 0 || dim < 0 || L < 0 || N < 0) return -1;
-    if (mutation < 0 || mutation >= MUT_COUNT) return -1;
+    if ((mutation < 0 || mutation >= MUT_COUNT) && mutation != MUT_COPY) return -1;
     if (flags & ~(FLAG_SOFTPLUS | FLAG_ZOH)) return -1;
     const int64_t nch = batch * dim;
     if (nch == 0) return 0;
     sscan_job base = {u, delta, A, B, C, D, h0, out, final_state,
                       batch, dim, L, N, 0, nch, mutation, z, delta_bias, flags};
     if (nthreads <= 1 || nch == 1) {
-        sscan_channels(&base);
+        sscan_run(&base);
         return 0;
     }
     if (nthreads > nch) nthreads = (int)nch;
@@ -215,7 +270,7 @@ int oracle_sscan_fwd_full_mutant(const double *u, const double *delta, const dou
     if (started < nthreads) {
         sscan_job rest = base;
         rest.first = jobs[started].first;
-        sscan_channels(&rest);
+        sscan_run(&rest);
     }
     for (int i = 0; i < started; ++i) pthread_join(tid[i], NULL);
     free(tid);

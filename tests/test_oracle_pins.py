@@ -458,6 +458,29 @@ def test_every_planted_option_mistake_is_caught():
         assert failed, f"planted option mistake {m} passed every pin"
 
 
+def test_the_copy_carrying_the_planted_mistakes_equals_the_definition():
+    """The planted-mistake tests run on a copy of the definition, so that the
+    definition itself carries no mistake switches; with no mistake planted
+    (code 100) that copy computes exactly what the definition computes, with
+    every option on and off, threaded or not."""
+    u, delta, A, B, C, D, h0 = _rand_problem(41)
+    r = _rng(42)
+    z = r.normal(size=u.shape)
+    bias = r.normal(size=A.shape[0]) * 0.3
+    A = A.copy()
+    A[0, 1] = 0.0  # the zero-order hold's A = 0 branch
+    for softplus in (False, True):
+        for zoh in (False, True):
+            for gate in (None, z):
+                for nth in (1, 3):
+                    ref = oracle.sscan_fwd_full(u, delta, A, B, C, D, gate, bias, h0,
+                                                delta_softplus=softplus, zoh=zoh, nthreads=nth)
+                    cp = oracle.sscan_fwd_full(u, delta, A, B, C, D, gate, bias, h0,
+                                               delta_softplus=softplus, zoh=zoh, nthreads=nth,
+                                               mutation=100)
+                    assert np.array_equal(ref[0], cp[0]) and np.array_equal(ref[1], cp[1])
+
+
 def test_options_off_is_the_plain_scan():
     u, delta, A, B, C, D, h0 = _rand_problem(37)
     y0, h0r = oracle.sscan_fwd(u, delta, A, B, C, D, h0)
