@@ -569,7 +569,8 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     snprintf(g_rec.plan, sizeof(g_rec.plan),
              "sscan %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld %s%s%s%s%s%s%s",
              f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, pl.Tseg,
-             use_shfl ? "tma shfl " : use_tma ? "tma " : "", S == 1 ? "single" : S == 2 ? "local+correct" : "local+fold+correct",
+             use_shfl ? "tma shfl " : use_tma ? "tma " : "",
+             S == 1 ? "single" : S <= sscan::kFoldInCorrectionMaxSegments ? "local+correct" : "local+fold+correct",
              delta_bias ? " bias" : "",
              p.delta_softplus ? " softplus" : "", p.zoh ? " zoh" : "", z ? " gate" : "",
              S == 1 ? "" : pl.corr_shfl ? " corr=tma shfl" : pl.corr_tma ? " corr=tma" : " corr=cp.async");
@@ -609,7 +610,8 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
                   : launch_fwd(f32, p, sh, tiles * S, st);
     p.wait_ns = 0;
     p.expire_wait = 0;
-    if (e == cudaSuccess && S > 2) e = launch_fold(p, st);
+    p.fold_in_corr = S <= sscan::kFoldInCorrectionMaxSegments ? 1 : 0;
+    if (e == cudaSuccess && S > 2 && !p.fold_in_corr) e = launch_fold(p, st);
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);

@@ -125,6 +125,11 @@ bool tma_encode_3d(CUtensorMap* map, const void* base, bool f32, long long L, lo
 // written over aggregate slot s - 1; launched as a programmatic dependent of
 // the local pass.
 cudaError_t fwd_fold_launch(const FwdParams& p, cudaStream_t stream);
+// Splits of up to this many segments skip the fold pass: each correction CTA
+// folds the earlier segments' aggregates itself (O(S) per CTA, a few loads in
+// flight at a time), which costs less than one more launch on the critical
+// path (512 channels x 8192 steps in 19 segments: 47.1 us with the fold pass).
+constexpr long long kFoldInCorrectionMaxSegments = 24;
 // Scratch floats per (channel, segment) of a time split: the end state (N),
 // the sum of delta and min(0, smallest delta).
 inline long long split_floats_per_segment(long long N) { return N + 2; }

@@ -74,6 +74,7 @@ struct FwdParams {
     int zoh;                  // zero-order-hold B-bar (the kernel's ZOH variant)
     int* status;              // device status word: a bounded wait that gives up
                               // stores SSCAN_ERR_TIMEOUT there
+    int fold_in_corr;  // the correction folds the aggregates itself (few segments; no fold pass)
     // test aid (TMA-fed kernels): when set, each bounded wait gives up after
     // wait_ns, and the first B/C stage's barrier expects 16 bytes that no copy
     // delivers, so that its waits run out and the timeout path runs
@@ -180,6 +181,45 @@ struct FwdCfg {
     static_assert((DT * TC / 4) % kThreads == 0 || (DT * TC / 4) < kThreads, "epilogue items");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
+
+// State entering segment s (s >= 1) for the lane's states n = k*P + g of one
+// channel, when a split has few segments and the fold pass is not launched
+// (FwdParams::fold_in_corr): the fold of the aggregates of segments 0 .. s-1
+// (segment 0's entry holds its true end state because it started from h0),
+// the same composition in the same order as the fold pass.  FB segments'
+// loads are issued before their folds so the chain waits on memory once per FB.
+template <int NS, int P>
+__device__ __forceinline__ void fold_segments(const FwdParams& p, long long ch, int s, int g,
+                                              const float (&Al2)[NS], float (&h)[NS]) {
+    constexpr int FB = NS <= 2 ? 16 : NS <= 4 ? 8 : 4;
+    const float* st = p.seg_state + ch * p.S * p.N;
+    const float* ds = p.seg_dsum + ch * p.S;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        const long long n = (long long)k * P + g;
+        h[k] = n < p.N ? st[n] : 0.f;
+    }
+    for (int sp = 1; sp < s; sp += FB) {
+        float dv[FB], bv[FB][NS];
+#pragma unroll
+        for (int q = 0; q < FB; ++q) {
+            const bool on = sp + q < s;
+            dv[q] = on ? ds[sp + q] : 0.f;
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const long long n = (long long)k * P + g;
+                bv[q][k] = (on && n < p.N) ? st[(long long)(sp + q) * p.N + n] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < FB; ++q) {
+            if (sp + q < s) {
+#pragma unroll
+                for (int k = 0; k < NS; ++k) h[k] = fmaf(ex2(Al2[k] * dv[q]), h[k], bv[q][k]);
+            }
+        }
+    }
+}
 
 // Shared memory: raw ring [STAGES][ROWS][RROW] (T, cp.async targets), then the
 // fp32 work rows [ROWS][FROW] (bf16 only), then the partial outputs [DT][RS].
@@ -660,11 +700,19 @@ __global__ void __launch_bounds__(FwdCfg<T, NS, P, CPL, OPT>::kThreads) sscan_fw
             // the state entering segment s, folded from the aggregates of the
             // segments before it by the fold pass (slot s - 1; with two
             // segments slot 0 holds it already: segment 0 started from h0)
-            const float* ent = p.seg_state + (ch[j] * p.S + (s - 1)) * p.N;
+            if (p.fold_in_corr) {
+                fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
+            } else {
+                const float* ent = p.seg_state + (ch[j] * p.S + (s - 1)) * p.N;
+#pragma unroll
+                for (int k = 0; k < NS; ++k) {
+                    const int n = k * P + g;
+                    h[j][k] = n < N ? ent[n] : 0.f;
+                }
+            }
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
-                const int n = k * P + g;
-                h[j][k] = (dval[j] && n < N) ? ent[n] : 0.f;
+                if (!dval[j]) h[j][k] = 0.f;
                 grows |= Al2[j][k] > 0.f;
             }
             if (dval[j]) grows |= p.seg_dmin[ch[j] * p.S + s] < 0.f;

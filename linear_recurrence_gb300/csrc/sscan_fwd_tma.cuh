@@ -781,7 +781,8 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     }
     // correction: the carried state entering segment s, folded from the
     // aggregates of the segments before it by the fold pass (slot s - 1;
-    // with two segments slot 0 holds it already: segment 0 started from h0); it
+    // with two segments slot 0 holds it already: segment 0 started from h0),
+    // or here when the split has few segments (fold_in_corr); it
     // is followed until every state of the CTA has fallen below 2^-24 of its
     // entry magnitude, a cut-off taken only while every decay factor
     // exp(delta*A) of the CTA's channels in this segment is at most 1 (every
@@ -790,11 +791,19 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     if constexpr (CORR) {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            const float* ent = p.seg_state + (ch[j] * p.S + (s - 1)) * p.N;
+            if (p.fold_in_corr) {
+                fold_segments<NS, P>(p, ch[j], s, g, Al2[j], h[j]);
+            } else {
+                const float* ent = p.seg_state + (ch[j] * p.S + (s - 1)) * p.N;
+#pragma unroll
+                for (int k = 0; k < NS; ++k) {
+                    const int n = k * P + g;
+                    h[j][k] = n < N ? ent[n] : 0.f;
+                }
+            }
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
-                const int n = k * P + g;
-                h[j][k] = (dval[j] && n < N) ? ent[n] : 0.f;
+                if (!dval[j]) h[j][k] = 0.f;
                 grows |= Al2[j][k] > 0.f;
             }
             if (dval[j]) grows |= p.seg_dmin[ch[j] * p.S + s] < 0.f;

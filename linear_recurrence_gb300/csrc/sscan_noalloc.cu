@@ -130,7 +130,7 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     char plan[160];
     snprintf(plan, sizeof(plan), "noalloc %s P=%d NS=%d CPL=%d vec=%d tiles=%lld S=%lld Tseg=%lld cp.async %s",
              f32 ? "f32" : "bf16", sh.P, sh.NS, sh.CPL, (int)vec, tiles, S, Tseg,
-             S == 1 ? "single" : S == 2 ? "local+correct" : "local+fold+correct");
+             S == 1 ? "single" : S <= sscan::kFoldInCorrectionMaxSegments ? "local+correct" : "local+fold+correct");
 
     cudaError_t e;
     if (S == 1) {
@@ -153,12 +153,13 @@ extern "C" int sscan_fwd_noalloc(const void* u, const void* delta, const float* 
     p.mode = sscan::MODE_LOCAL;
     p.seg_count = (int)S;
     e = launch(f32, p, sh, tiles * S, st);
-    if (e == cudaSuccess && S > 2) e = sscan::fwd_fold_launch(p, st);
+    p.fold_in_corr = S <= sscan::kFoldInCorrectionMaxSegments ? 1 : 0;
+    if (e == cudaSuccess && S > 2 && !p.fold_in_corr) e = sscan::fwd_fold_launch(p, st);
     if (e == cudaSuccess) {
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
         e = launch(f32, p, sh, tiles * (S - 1), st);
     }
-    sscan::record_call(S > 2 ? 3 : 2, st, plan);
+    sscan::record_call(S > sscan::kFoldInCorrectionMaxSegments ? 3 : 2, st, plan);
     return e == cudaSuccess ? SSCAN_OK : SSCAN_ERR_CUDA;
 }
