@@ -111,7 +111,38 @@ def measure_ex2(dev, stream, reps=3):
     return n / best
 
 
+def measure_element(dev, stream, shared_rate, reps=3):
+    """Elements per second of the scan's arithmetic at its peak on this GPU,
+    from the library's element probe: per element one 2^x and four FP32
+    operations (three FP32 when a channel's states share one decay rate and
+    the 2^x is taken once per step), independent chains on every SM (two
+    resident CTAs of 256 threads, four waves); best of ``reps`` CUDA-event
+    timings after a warm-up launch.  The exponent and the FP32 operations draw
+    on the same issue slots, so this is the rate that bounds the scan's
+    arithmetic, below both units' separate peaks."""
+    import torch
+    import linear_recurrence_gb300 as lr
+    blocks, iters = SM_COUNT * 8, 2000
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    lr.probe_element(blocks, iters, shared_rate=shared_rate, sink=sink, stream=stream)
+    best = None
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        n = lr.probe_element(blocks, iters, shared_rate=shared_rate, sink=sink, stream=stream)
+        e.record(stream)
+        e.synchronize()
+        t = s.elapsed_time(e) * 1e-3
+        best = t if best is None else min(best, t)
+    return n / best
+
+
 def roofline(w, t_s, pk):
+    """The slower of the HBM bound (algorithmic bytes at the measured copy
+    bandwidth) and the arithmetic bound (the elements at the measured peak
+    element rate of the scan's exponent/FP32 mix, sscan_probe_element).  The
+    separate MUFU and FP32-pipe bounds, and the fraction of the HBM bound
+    alone, are reported beside it."""
     a = algorithmic(w)
     clk = pk["sm_max_mhz"] * 1e6
     bw = pk["hbm_gbs"] * 1e9
@@ -119,25 +150,31 @@ def roofline(w, t_s, pk):
     t_hbm = a["bytes"] / bw
     t_exp = a["exps"] / ex2_rate
     t_fp32 = a["fp32"] / (FP32_PER_CLK_SM * SM_COUNT * clk)
-    t_roof = max(t_hbm, t_exp, t_fp32)
+    shared = a["exps"] < a["elements"]
+    elem_rate = pk.get("elem_shared_per_s" if shared else "elem_per_s")
+    if elem_rate:
+        t_alu, alu_src = a["elements"] / elem_rate, "measured in this run (sscan_probe_element)"
+    else:
+        t_alu, alu_src = max(t_exp, t_fp32), "separate unit peaks (element probe failed)"
+        elem_rate = a["elements"] / t_alu
+    t_roof = max(t_hbm, t_alu)
     achieved_gbs = a["bytes"] / t_s / 1e9
-    if t_hbm >= max(t_exp, t_fp32):
+    if t_hbm >= t_alu:
         r = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
              "frac": achieved_gbs / pk["hbm_gbs"]}
     else:
-        # an ALU-bound scan: express the rate in the binding unit's operations
-        if t_exp >= t_fp32:
-            peak = ex2_rate / 1e12
-            r = {"bound": "alu", "achieved": a["exps"] / t_s / 1e12, "peak": peak,
-                 "unit": "Texp/s (MUFU ex2)", "frac": (a["exps"] / t_s / 1e12) / peak}
-        else:
-            peak = FP32_PER_CLK_SM * SM_COUNT * clk / 1e12
-            r = {"bound": "alu", "achieved": a["fp32"] / t_s / 1e12, "peak": peak,
-                 "unit": "T FP32 lane-ops/s", "frac": (a["fp32"] / t_s / 1e12) / peak}
-    r.update({"peak_source": pk["source"], "ex2_peak_source": pk.get("ex2_source", "nominal"),
-              "ex2_peak_texp_s": ex2_rate / 1e12, "t_roofline_us": t_roof * 1e6,
-              "t_hbm_us": t_hbm * 1e6, "t_exp_us": t_exp * 1e6, "t_fp32_us": t_fp32 * 1e6,
-              "hbm_gbs": achieved_gbs, "frac_of_roofline": t_roof / t_s})
+        # an arithmetic-bound scan: the rate in elements (b, d, t, n)
+        peak = elem_rate / 1e12
+        r = {"bound": "alu", "achieved": a["elements"] / t_s / 1e12, "peak": peak,
+             "unit": "T elements/s (" + ("three FP32 per element, one 2^x per step" if shared
+                                        else "one 2^x and four FP32 per element") + ")",
+             "frac": (a["elements"] / t_s / 1e12) / peak}
+    r.update({"peak_source": pk["source"], "alu_peak_source": alu_src,
+              "elem_peak_t_s": elem_rate / 1e12, "t_roofline_us": t_roof * 1e6,
+              "t_hbm_us": t_hbm * 1e6, "t_alu_us": t_alu * 1e6,
+              "ex2_peak_source": pk.get("ex2_source", "nominal"), "ex2_peak_texp_s": ex2_rate / 1e12,
+              "t_exp_us": t_exp * 1e6, "t_fp32_us": t_fp32 * 1e6,
+              "hbm_gbs": achieved_gbs, "frac_of_roofline": t_roof / t_s, "frac_of_hbm": t_hbm / t_s})
     return r
 
 
@@ -594,6 +631,11 @@ def main():
         pk["ex2_source"] = "measured in this run (sscan_probe_ex2)"
     except Exception as exc:  # pragma: no cover - reported, nominal figure used
         pk["ex2_source"] = f"nominal 32/clk/SM (probe failed: {exc})"
+    try:
+        pk["elem_per_s"] = measure_element(dev, stream, False)
+        pk["elem_shared_per_s"] = measure_element(dev, stream, True)
+    except Exception as exc:  # pragma: no cover - reported, the separate unit peaks used
+        print(f"element probe failed: {exc}", file=sys.stderr)
 
     barrier(ws, dev)
     torch.cuda.synchronize(dev)
@@ -623,6 +665,7 @@ def main():
                          "value": wx.channels * wx.L / r["t"], "unit": UNIT,
                          "hbm_gbs": rfx["hbm_gbs"], "bound": rfx["bound"],
                          "frac": rfx["frac"], "frac_of_roofline": rfx["frac_of_roofline"],
+                         "frac_of_hbm": rfx["frac_of_hbm"],
                          "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"],
                          "clocks": ckx.summary()}
         with ClockSampler(physical_gpu(dev.index or 0)) as ckx:

@@ -275,6 +275,26 @@ int sscan_probe_ex2(float *sink, int blocks, int iters, void *stream);
 /* Exponentials one sscan_probe_ex2 launch computes. */
 long long sscan_probe_ex2_count(int blocks, int iters);
 
+/*
+ * sscan_probe_element -- a measurement aid for the roofline of the scan; the
+ * pages have no counterpart.  It launches `blocks` CTAs of 256 threads on
+ * `stream` (two resident per SM); each thread runs 16 independent state
+ * chains (32 when shared_rate != 0) for `iters` steps of the element
+ * arithmetic of "Mamba 状态空间模型：从理论到生产级推理的 CUDA 内核优化实战"
+ * section 2.3: a = 2^(delta*A*log2 e), h = a*h + (delta*u)*B, y += C*h --
+ * one exponent per element, or one per step shared by all chains when
+ * shared_rate != 0 (a channel with a single decay rate).  Timing the launch
+ * with CUDA events and dividing sscan_probe_element_count(blocks, iters,
+ * shared_rate) by the time gives the peak element rate of the arithmetic on
+ * this GPU: the exponent and the FP32 operations share the SMs' issue slots,
+ * so it lies below both units' separate peaks.  sink: device float32
+ * [blocks*256], required (not written in practice).  Returns SSCAN_OK,
+ * SSCAN_ERR_INVALID (sink NULL, blocks or iters < 1) or SSCAN_ERR_CUDA.
+ */
+int sscan_probe_element(float *sink, int blocks, int iters, int shared_rate, void *stream);
+/* Elements one sscan_probe_element launch computes. */
+long long sscan_probe_element_count(int blocks, int iters, int shared_rate);
+
 /* Largest dstate that sscan_fwd accepts. */
 int sscan_max_dstate(void);
 

@@ -52,6 +52,8 @@ SIGNATURES = {
     "sscan_debug_expire_next_wait": (None, [ctypes.c_uint]),
     "sscan_probe_ex2": (_int, [_fp, _int, _int, _vp]),
     "sscan_probe_ex2_count": (ctypes.c_longlong, [_int, _int]),
+    "sscan_probe_element": (_int, [_fp, _int, _int, _int, _vp]),
+    "sscan_probe_element_count": (ctypes.c_longlong, [_int, _int, _int]),
     "sscan_last_launch_count": (_int, []),
     "sscan_last_plan": (ctypes.c_char_p, []),
 }
@@ -113,6 +115,19 @@ def probe_ex2(blocks: int, iters: int, *, sink=None, stream=None) -> int:
     if rc != SSCAN_OK:
         raise SscanError(rc, "sscan_probe_ex2")
     return int(lib().sscan_probe_ex2_count(int(blocks), int(iters)))
+
+
+def probe_element(blocks: int, iters: int, *, shared_rate: bool = False, sink=None, stream=None) -> int:
+    """Launch the element-arithmetic throughput probe (see include/sscan.h) on
+    the current device; returns the number of elements it computes.  Time it
+    with CUDA events on ``stream``."""
+    if sink is None:
+        sink = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    rc = lib().sscan_probe_element(_ptr(sink), int(blocks), int(iters), int(bool(shared_rate)),
+                                   _stream_handle(stream))
+    if rc != SSCAN_OK:
+        raise SscanError(rc, "sscan_probe_element")
+    return int(lib().sscan_probe_element_count(int(blocks), int(iters), int(bool(shared_rate))))
 
 
 def debug_expire_next_wait(wait_limit_us: int) -> None:

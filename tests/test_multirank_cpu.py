@@ -82,6 +82,20 @@ def test_roofline_arithmetic():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(a["bytes"] / 1e-5 / 1e9)
     assert r["frac"] == pytest.approx(r["achieved"] / 6788.3)
-    # the bf16 workload is bound by the exponentials; the wide one by FP32
-    assert bench.roofline(bench.workloads.WORKLOADS["bf16_2k"], 1e-4, pk)["unit"].startswith("Texp")
-    assert "FP32" in bench.roofline(bench.workloads.WORKLOADS["wide64"], 1e-3, pk)["unit"]
+    assert r["frac_of_hbm"] == pytest.approx(r["frac"])
+    # without the element probe the arithmetic bound is the slower of the
+    # separate unit peaks: the bf16 and the wide workloads are bound by it
+    rb = bench.roofline(bench.workloads.WORKLOADS["bf16_2k"], 1e-4, pk)
+    assert rb["bound"] == "alu" and rb["t_alu_us"] == pytest.approx(max(rb["t_exp_us"], rb["t_fp32_us"]))
+    # with measured element rates (one 2^x and four FP32 per element; three
+    # FP32 with a shared rate) the bound is the elements at that rate
+    pk.update({"elem_per_s": 5.8e12, "elem_shared_per_s": 9.7e12})
+    r = bench.roofline(w, 1e-5, pk)
+    assert r["bound"] == "alu" and r["t_alu_us"] == pytest.approx(a["elements"] / 5.8e12 * 1e6)
+    assert r["frac"] == pytest.approx(a["elements"] / 1e-5 / 5.8e12)
+    assert r["frac_of_roofline"] == pytest.approx(r["t_alu_us"] * 1e-6 / 1e-5)
+    assert r["frac_of_hbm"] == pytest.approx(a["bytes"] / (6788.3e9 * 1e-5))
+    ww = bench.workloads.WORKLOADS["wide64"]
+    rw = bench.roofline(ww, 1e-3, pk)
+    assert rw["t_alu_us"] == pytest.approx(bench.algorithmic(ww)["elements"] / 9.7e12 * 1e6)
+    assert "three FP32" in rw["unit"]
