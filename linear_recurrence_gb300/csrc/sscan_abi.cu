@@ -355,21 +355,20 @@ int plan_fwd_tma(bool f32, int variant, long long batch, long long dim, long lon
 
 // The carry correction of a TMA-fed plan: for long segments (long sequences,
 // where long memories make long decay horizons) on the TMA-fed kernel, shape
-// (4,4,2) (64 state slots: (4,16,2)); for short ones on the cp.async kernel,
-// shape (8,2,1), whose smaller CTAs start and stop sooner.
+// (4,4,2); for short ones, and for 64 state slots, on the cp.async kernel,
+// shapes (8,2,1) and (8,8,1), whose smaller CTAs start and stop sooner.
 void choose_correction(FwdPlan& best, bool wide, long long batch, long long dim) {
     const long long TC = kChunkSteps;
-    // the correction: for long segments (long sequences, where long memories
-    // make long decay horizons) on the TMA-fed kernel, shape (4,4,2); for short
-    // ones on the cp.async kernel, shape (8,2,1), whose smaller CTAs start and
-    // stop sooner (measured on GB300: 512 channels x 8192 steps in 19 segments
-    // 47.1 / 49.2 / 53.2 us with (8,2,1) / TMA (8,2,2) / TMA (4,4,2), and
-    // 46.9 / 49.0 / 51.0 us with (8,2,1) / (4,4,1) / (2,8,1), whose fewer
-    // lanes per channel let decayed states drop out sooner but give fewer
-    // warps; 1536 x 65536 in 19 segments 554 / 548 / 509 us with the first
-    // three, 531 / 557 us with (4,4,1) / (2,8,1))
-    best.corr_tma = best.S > 1 && (wide || best.Tseg >= 32 * TC);
-    best.corr_sh = wide ? Shape{4, 16, 2} : best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
+    // measured on GB300: 512 channels x 8192 steps in 19 segments 47.1 / 49.2 /
+    // 53.2 us with (8,2,1) / TMA (8,2,2) / TMA (4,4,2), and 46.9 / 49.0 / 51.0 us
+    // with (8,2,1) / (4,4,1) / (2,8,1), whose fewer lanes per channel let
+    // decayed states drop out sooner but give fewer warps; 1536 x 65536 in 19
+    // segments 554 / 548 / 509 us with the first three, 531 / 557 us with
+    // (4,4,1) / (2,8,1).  64 state slots (8 x 1024 channels x 4096 steps in 2
+    // segments): 449 us with TMA (4,16,2), whose 128 CTAs leave a quarter of
+    // the SMs idle, 427 / 426 us with cp.async (8,8,1) / (16,4,1)
+    best.corr_tma = best.S > 1 && !wide && best.Tseg >= 32 * TC;
+    best.corr_sh = wide ? Shape{8, 8, 1} : best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
     best.corr_tiles_per_batch = ceil_div(dim, best.corr_tma ? tma_channels(best.corr_sh) : shape_channels(best.corr_sh));
     best.corr_tiles = batch * best.corr_tiles_per_batch;
     best.corr_shfl = false;
