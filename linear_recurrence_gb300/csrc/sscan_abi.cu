@@ -365,7 +365,7 @@ void choose_correction(FwdPlan& best, bool wide, long long batch, long long dim)
     // decayed states drop out sooner but give fewer warps; 1536 x 65536 in 19
     // segments 554 / 548 / 509 us with the first three, 531 / 557 us with
     // (4,4,1) / (2,8,1).  64 state slots (8 x 1024 channels x 4096 steps in 2
-    // segments): 449 us with TMA (4,16,2), whose 128 CTAs leave a quarter of
+    // segments): 449 us with TMA (4,16,2), whose 128 CTAs leave a sixth of
     // the SMs idle, 427 / 426 us with cp.async (8,8,1) / (16,4,1)
     best.corr_tma = best.S > 1 && !wide && best.Tseg >= 32 * TC;
     best.corr_sh = wide ? Shape{8, 8, 1} : best.corr_tma ? Shape{4, 4, 2} : Shape{8, 2, 1};
@@ -430,12 +430,15 @@ int plan_fwd_shfl(bool f32, long long batch, long long dim, long long seqlen, lo
     pl.Tseg = ceil_div(ceil_div(seqlen, S), TC) * TC;
     pl.S = ceil_div(seqlen, pl.Tseg);
     if (pl.tiles * pl.S > (1LL << 30)) return SSCAN_ERR_INVALID;
-    // the correction runs on the same kernel's correction instantiation
+    // the correction runs on the same kernel's correction instantiation, with
+    // one channel per lane: twice the warps of the local pass's shape, so that
+    // its latency-bound chunks overlap more (1536 channels x 65536 steps in 25
+    // segments: correction 105.6 -> 99 us)
     pl.corr_tma = pl.S > 1;
     pl.corr_shfl = pl.S > 1;
-    pl.corr_sh = sh;
-    pl.corr_tiles_per_batch = pl.tiles_per_batch;
-    pl.corr_tiles = pl.tiles;
+    pl.corr_sh = Shape{2, 8, 1};
+    pl.corr_tiles_per_batch = ceil_div(dim, tma_channels(pl.corr_sh));
+    pl.corr_tiles = batch * pl.corr_tiles_per_batch;
     *out = pl;
     return SSCAN_OK;
 }

@@ -90,9 +90,9 @@ inline int fwd_occupancy(bool f32, Shape sh) {
 inline int tma_channels(Shape sh) { return 4 * (32 / sh.P) * sh.CPL; }
 // Shapes of the shuffle kernels (the TMA-fed kernel's plain scan with
 // outputs summed by shuffles): 16 state slots as 2 lanes x 8 states, two
-// channels per lane.
+// channels per lane; with one channel per lane for the carry correction only.
 #ifndef SSCAN_TMA_SHFL_SHAPES
-#define SSCAN_TMA_SHFL_SHAPES(X) X(2, 8, 2)
+#define SSCAN_TMA_SHFL_SHAPES(X) X(2, 8, 2) X(2, 8, 1)
 #endif
 bool shfl_has_shape(Shape sh);
 cudaError_t fwd_shfl_launch(bool f32, const FwdParams& p, Shape sh, int grid, cudaStream_t stream);

@@ -454,22 +454,22 @@ __device__ __forceinline__ void compute_chunk_shfl(const TU* su, const TU* sd, c
     }
 }
 
-// SH kernels, carry correction: one chunk of the homogeneous recurrence
-// h = exp(delta*A)*h from the carried state, in closed form within the chunk:
-// with S_t the sum of delta from the chunk's start through step t (per
-// channel), h_t = 2^(A log2e S_t) h_start, so no step waits on the previous
-// one; h advances by the whole chunk's decay at its end.  The C-contraction is
-// summed over the channel's lanes as in compute_chunk_shfl, added to the local
-// outputs (staged in the u rows, sy) and stored.  live[k] (warp-uniform)
+// SH kernels, carry correction (one channel per lane): one chunk of the
+// homogeneous recurrence h = exp(delta*A)*h from the carried state, in closed
+// form within the chunk: with S_t the sum of delta from the chunk's start
+// through step t, h_t = 2^(A log2e S_t) h_start, so no step waits on the
+// previous one; h advances by the whole chunk's decay at its end.  The
+// C-contraction is summed over the channel's P lanes by a butterfly (every
+// lane then holds the full sum), added to the local outputs (staged in the u
+// rows, sy) and stored by the channel's first lane.  live[k] (warp-uniform)
 // skips the quads of state slots whose carry has decayed below the threshold
 // in every lane of the warp (their states are not advanced: they stay below
 // it, decay factors being at most 1 whenever slots are skipped).
 template <typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
-__device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, const float* sC, const int (&rl)[2],
-                                                 int g, const float (&Al2)[2][NS], const float (&As)[2],
-                                                 const bool (&live)[NS], float (&h)[2][NS], T* orow, bool store,
-                                                 int nvalid) {
-    constexpr int CPL = 2;
+__device__ __forceinline__ void decay_chunk_shfl1(const TU* sy, const TU* sd, const float* sC, const int (&rl)[1],
+                                                  int g, const float (&Al2)[1][NS], const float (&As)[1],
+                                                  const bool (&live)[NS], float (&h)[1][NS], T* orow, bool store,
+                                                  int nvalid) {
     constexpr int NB = TC / 4, QS = 4, NQ = NS / QS;
     constexpr unsigned FULL = 0xffffffffu;
     const float* bC = sC + g * FROW;
@@ -480,22 +480,18 @@ __device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, con
 #pragma unroll
         for (int kk = 0; kk < QS; ++kk) lq[q] |= live[q * QS + kk];
     }
-    float sacc[CPL] = {0.f, 0.f};  // sum of delta since the chunk's start
+    float sacc = 0.f;  // sum of delta since the chunk's start
 #pragma unroll 2
     for (int blk = 0; blk < NB; ++blk) {
         const int t4 = 4 * blk;
-        float sc[CPL][4], es[CPL][4], y[CPL][4], yl[4];
+        float sc[4], es[4], y[4], yl[4], dv[4];
+        load4_smem(sd + rl[0] * UROW + t4, dv);
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            float dv[4];
-            load4_smem(sd + rl[j] * UROW + t4, dv);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                sacc[j] += dv[s];
-                sc[j][s] = sacc[j];
-                es[j][s] = SCALAR ? ex2(sc[j][s] * As[j]) : 0.f;
-                y[j][s] = 0.f;
-            }
+        for (int s = 0; s < 4; ++s) {
+            sacc += dv[s];
+            sc[s] = sacc;
+            es[s] = SCALAR ? ex2(sc[s] * As[0]) : 0.f;
+            y[s] = 0.f;
         }
         load4_smem(sy + rl[0] * UROW + t4, yl);
 #pragma unroll
@@ -507,24 +503,20 @@ __device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, con
 #pragma unroll
             for (int s = 0; s < 4; ++s)
 #pragma unroll
-                for (int j = 0; j < CPL; ++j)
-#pragma unroll
-                    for (int kk = 0; kk < QS; ++kk) {
-                        const int k = q * QS + kk;
-                        const float e = SCALAR ? es[j][s] : ex2(sc[j][s] * Al2[j][k]);
-                        y[j][s] = fmaf(cc[kk][s], h[j][k] * e, y[j][s]);
-                    }
+                for (int kk = 0; kk < QS; ++kk) {
+                    const int k = q * QS + kk;
+                    const float e = SCALAR ? es[s] : ex2(sc[s] * Al2[0][k]);
+                    y[s] = fmaf(cc[kk][s], h[0][k] * e, y[s]);
+                }
         }
 #pragma unroll
-        for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[1][s], P / 2);
+        for (int m = P / 2; m >= 1; m /= 2)
 #pragma unroll
-        for (int m = P / 4; m >= 1; m /= 2)
-#pragma unroll
-            for (int s = 0; s < 4; ++s) y[0][s] += __shfl_xor_sync(FULL, y[0][s], m);
+            for (int s = 0; s < 4; ++s) y[s] += __shfl_xor_sync(FULL, y[s], m);
         if (store && t4 < nvalid) {
             float v[4];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) v[s] = yl[s] + y[0][s];
+            for (int s = 0; s < 4; ++s) v[s] = yl[s] + y[s];
             if constexpr (sizeof(T) == 4) {
                 *reinterpret_cast<float4*>(orow + t4) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
@@ -537,13 +529,10 @@ __device__ __forceinline__ void decay_chunk_shfl(const TU* sy, const TU* sd, con
         }
     }
     // advance the live states over the chunk
+    const float ech = SCALAR ? ex2(sacc * As[0]) : 0.f;
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        const float ech = SCALAR ? ex2(sacc[j] * As[j]) : 0.f;
-#pragma unroll
-        for (int k = 0; k < NS; ++k)
-            if (lq[k / QS]) h[j][k] *= SCALAR ? ech : ex2(sacc[j] * Al2[j][k]);
-    }
+    for (int k = 0; k < NS; ++k)
+        if (lq[k / QS]) h[0][k] *= SCALAR ? ech : ex2(sacc * Al2[0][k]);
 }
 
 // Steps [T0, T0 + TS) of the carry correction for the calling lane: the
@@ -629,7 +618,8 @@ __device__ __forceinline__ void widen_delta_rows_warp(const bf16* src, float* ds
 template <typename T, int NS, int P, int CPL, int OPT, bool CORR, bool SH = false>
 __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const TmaMaps& tm) {
     using Cfg = TmaCfg<T, NS, P, CPL, OPT, SH>;
-    static_assert(!SH || (CPL == 2 && P >= 2 && OPT == 0), "shuffle kernels: plain scan, lane pairs");
+    static_assert(!SH || ((CORR ? CPL == 1 : CPL == 2) && P >= 2 && OPT == 0),
+                  "shuffle kernels: plain scan; lane pairs, one channel per lane in the correction");
     constexpr int NUR = Cfg::NUR;
     constexpr int kWarps = Cfg::kWarps, CPW = Cfg::CPW, GPW = Cfg::GPW, NSP = Cfg::NSP, TC = Cfg::TC;
     constexpr int RROW = Cfg::RROW, FROW = Cfg::FROW, RS = Cfg::RS, STAGES = Cfg::STAGES;
@@ -752,7 +742,8 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         // 2gi + 1 (the eight lanes of a quarter-warp then read eight distinct
         // padded rows, in distinct banks), and the lanes in the upper half of
         // the channel's lanes hold the pair in the opposite order
-        if constexpr (SH) rl[j] = 2 * gi + (j ^ ((g & (P / 2)) ? 1 : 0));
+        if constexpr (SH && CPL == 1) rl[j] = gi;
+        else if constexpr (SH) rl[j] = 2 * gi + (j ^ ((g & (P / 2)) ? 1 : 0));
         else rl[j] = j * GPW + gi;
         const long long dch = dw + rl[j];
         dval[j] = dch < p.dim;
@@ -858,7 +849,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     // shuffle kernels: the lane's kept channel rl[0], whose outputs it stores
     // when it is the first of the channel's lanes that hold the full sums
     float sh_dsum = 0.f, sh_dcomp = 0.f, sh_dmin = 0.f;
-    const bool sh_store = SH && (g & (P / 2 - 1)) == 0 && dval[0];
+    const bool sh_store = SH && (CPL == 1 ? g == 0 : (g & (P / 2 - 1)) == 0) && dval[0];
     const float sh_D = (SH && p.D != nullptr && dval[0]) ? __ldg(p.D + (dw + rl[0])) : 0.f;
     T* sh_orow = gout + ch[0] * p.L;
 
@@ -1049,11 +1040,11 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         if constexpr (SH && CORR) {
             const int nvalid = (int)min((long long)TC, t_end - t0);
             if (scalar)
-                decay_chunk_shfl<T, UT, UROW, NS, P, FROW, TC, true>(su, sd, sC, rl, g, Al2, As, live, h,
-                                                                     sh_orow + t0, sh_store, nvalid);
-            else
-                decay_chunk_shfl<T, UT, UROW, NS, P, FROW, TC, false>(su, sd, sC, rl, g, Al2, As, live, h,
+                decay_chunk_shfl1<T, UT, UROW, NS, P, FROW, TC, true>(su, sd, sC, rl, g, Al2, As, live, h,
                                                                       sh_orow + t0, sh_store, nvalid);
+            else
+                decay_chunk_shfl1<T, UT, UROW, NS, P, FROW, TC, false>(su, sd, sC, rl, g, Al2, As, live, h,
+                                                                       sh_orow + t0, sh_store, nvalid);
             __syncwarp();
             if (lane == 0) {  // C of this chunk is no longer read by this warp
                 if constexpr (Cfg::kF32) {
@@ -1278,7 +1269,15 @@ int occupancy_tma_variant() {
     return n;
 }
 
-// The shuffle kernel of a shape (single and local passes of the plain scan).
+// The shuffle kernel of a shape: the carry correction for one channel per
+// lane, the single and local passes for two.
+template <typename T, int NS, int P, int CPL>
+constexpr auto shfl_kernel() {
+    if constexpr (CPL == 1) return sscan_fwd_tma_shfl_corr<T, NS, P, CPL>;
+    else return sscan_fwd_tma_shfl<T, NS, P, CPL>;
+}
+
+// Launch of a shuffle-kernel shape's pass.
 template <typename T, int NS, int P, int CPL>
 cudaError_t launch_tma_shfl_variant(const FwdParams& p, int grid, cudaStream_t stream) {
     using Cfg = TmaCfg<T, NS, P, CPL, 0, true>;
@@ -1292,7 +1291,8 @@ cudaError_t launch_tma_shfl_variant(const FwdParams& p, int grid, cudaStream_t s
         !tma_encode_3d(&tm.B, p.B, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP) ||
         !tma_encode_3d(&tm.C, p.C, f32, p.L, p.N, p.batch, Cfg::RROW, Cfg::NSP))
         return cudaErrorInvalidValue;
-    auto kern = corr ? sscan_fwd_tma_shfl_corr<T, NS, P, CPL> : sscan_fwd_tma_shfl<T, NS, P, CPL>;
+    if (corr != (CPL == 1)) return cudaErrorInvalidValue;  // a shape runs its own pass only
+    auto kern = shfl_kernel<T, NS, P, CPL>();
     static unsigned long long configured[2] = {0, 0};  // bit per device ordinal (< 64), per kernel
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1307,7 +1307,7 @@ cudaError_t launch_tma_shfl_variant(const FwdParams& p, int grid, cudaStream_t s
         kern<<<grid, Cfg::kThreads, Cfg::SMEM_BYTES, stream>>>(p, tm);
         return cudaGetLastError();
     }
-    // the correction follows the fold pass as a programmatic dependent
+    // the correction follows the local (or fold) pass as a programmatic dependent
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(Cfg::kThreads);
@@ -1325,7 +1325,7 @@ cudaError_t launch_tma_shfl_variant(const FwdParams& p, int grid, cudaStream_t s
 template <typename T, int NS, int P, int CPL>
 int occupancy_tma_shfl_variant() {
     using Cfg = TmaCfg<T, NS, P, CPL, 0, true>;
-    auto kern = sscan_fwd_tma_shfl<T, NS, P, CPL>;
+    auto kern = shfl_kernel<T, NS, P, CPL>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;
