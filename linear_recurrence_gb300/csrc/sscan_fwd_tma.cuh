@@ -462,30 +462,25 @@ __device__ __forceinline__ void compute_chunk_shfl(const TU* su, const TU* sd, c
 // C-contraction is summed over the channel's P lanes by a butterfly (every
 // lane then holds the full sum), added to the local outputs (staged in the u
 // rows, sy) and stored by the channel's first lane.  live[k] (warp-uniform)
-// skips the quads of state slots whose carry has decayed below the threshold
-// in every lane of the warp (their states are not advanced: they stay below
-// it, decay factors being at most 1 whenever slots are skipped).
-template <typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
-__device__ __forceinline__ void decay_chunk_shfl1(const TU* sy, const TU* sd, const float* sC, const int (&rl)[1],
-                                                  int g, const float (&Al2)[1][NS], const float (&As)[1],
-                                                  const bool (&live)[NS], float (&h)[1][NS], T* orow, bool store,
-                                                  int nvalid) {
-    constexpr int NB = TC / 4, QS = 4, NQ = NS / QS;
+// marks the state slots whose carry is still above the threshold in some
+// lane of the warp: the chunk runs over the quads of slots up to the last
+// live one (the ones past it are not advanced: they stay below the threshold,
+// decay factors being at most 1 whenever slots are skipped), and a chunk
+// with no live slot leaves the outputs as they are.  The count of quads is a
+// template parameter, so that the step loop has no branch and the compiler
+// can overlap its 4-step blocks (long64k: 462 -> 457 us).
+template <int NQL, typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
+__device__ __forceinline__ void decay_blocks_shfl1(const TU* sy, const TU* sd, const float* bC, int r,
+                                                   const float (&Al2)[1][NS], const float (&As)[1],
+                                                   float (&h)[1][NS], T* orow, bool store, int nvalid) {
+    constexpr int NB = TC / 4, QS = 4;
     constexpr unsigned FULL = 0xffffffffu;
-    const float* bC = sC + g * FROW;
-    bool lq[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        lq[q] = false;
-#pragma unroll
-        for (int kk = 0; kk < QS; ++kk) lq[q] |= live[q * QS + kk];
-    }
     float sacc = 0.f;  // sum of delta since the chunk's start
 #pragma unroll 2
     for (int blk = 0; blk < NB; ++blk) {
         const int t4 = 4 * blk;
         float sc[4], es[4], y[4], yl[4], dv[4];
-        load4_smem(sd + rl[0] * UROW + t4, dv);
+        load4_smem(sd + r * UROW + t4, dv);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             sacc += dv[s];
@@ -493,10 +488,9 @@ __device__ __forceinline__ void decay_chunk_shfl1(const TU* sy, const TU* sd, co
             es[s] = SCALAR ? ex2(sc[s] * As[0]) : 0.f;
             y[s] = 0.f;
         }
-        load4_smem(sy + rl[0] * UROW + t4, yl);
+        load4_smem(sy + r * UROW + t4, yl);
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            if (!lq[q]) continue;
+        for (int q = 0; q < NQL; ++q) {
             float cc[QS][4];
 #pragma unroll
             for (int kk = 0; kk < QS; ++kk) load4_smem(bC + (q * QS + kk) * P * FROW + t4, cc[kk]);
@@ -531,8 +525,30 @@ __device__ __forceinline__ void decay_chunk_shfl1(const TU* sy, const TU* sd, co
     // advance the live states over the chunk
     const float ech = SCALAR ? ex2(sacc * As[0]) : 0.f;
 #pragma unroll
+    for (int k = 0; k < NQL * QS; ++k) h[0][k] *= SCALAR ? ech : ex2(sacc * Al2[0][k]);
+}
+
+template <typename T, typename TU, int UROW, int NS, int P, int FROW, int TC, bool SCALAR>
+__device__ __forceinline__ void decay_chunk_shfl1(const TU* sy, const TU* sd, const float* sC, const int (&rl)[1],
+                                                  int g, const float (&Al2)[1][NS], const float (&As)[1],
+                                                  const bool (&live)[NS], float (&h)[1][NS], T* orow, bool store,
+                                                  int nvalid) {
+    constexpr int QS = 4, NQ = NS / QS;
+    static_assert(NQ >= 1 && NQ <= 4, "one to four quads of state slots");
+    const float* bC = sC + g * FROW;
+    int nql = 0;  // quads up to the last one with a live slot
+#pragma unroll
     for (int k = 0; k < NS; ++k)
-        if (lq[k / QS]) h[0][k] *= SCALAR ? ech : ex2(sacc * Al2[0][k]);
+        if (live[k]) nql = k / QS + 1;
+    // no live slot: the carry adds nothing to this chunk's outputs
+    if (nql == 0) return;
+    if constexpr (NQ >= 4)
+        if (nql == 4) return decay_blocks_shfl1<4, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
+    if constexpr (NQ >= 3)
+        if (nql == 3) return decay_blocks_shfl1<3, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
+    if constexpr (NQ >= 2)
+        if (nql == 2) return decay_blocks_shfl1<2, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
+    decay_blocks_shfl1<1, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
 }
 
 // Steps [T0, T0 + TS) of the carry correction for the calling lane: the
