@@ -96,7 +96,12 @@ struct TmaCfg {
     // SH: the lanes sum a channel's P partial outputs by warp shuffles and
     // store the outputs themselves (no partial-output buffer, no epilogue)
     static constexpr bool SH = SH_;
-    static constexpr int NUR = OPT > 0 ? 3 : 2;  // row sets of a warp's slot: u, delta (, z)
+    // the shuffle kernels' fp32 carry correction (one channel per lane) stages
+    // the C rows per warp, with the warp's local outputs and delta: every warp
+    // runs on its own, without a CTA-shared ring or CTA-wide votes
+    static constexpr bool kWarpC = SH_ && CPL == 1 && std::is_same<T, float>::value;
+    // row sets of a warp's slot: u (or the local outputs), delta (, z, or C)
+    static constexpr int NUR = OPT > 0 || kWarpC ? 3 : 2;
     static constexpr int kWarps = 4;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int GPW = Base::GPW, CPW = Base::CPW, NSP = Base::NSP;
@@ -153,7 +158,7 @@ struct TmaCfg {
     static constexpr int OFF_BAR = 0;
     static constexpr int OFF_U = 1024;  // [STAGES][kWarps][u, delta (, z)] slots
     static constexpr int OFF_BC = OFF_U + STAGES * kWarps * NUR * U_SLOT;  // [STAGES][B, C] slots
-    static constexpr int OFF_BCW = OFF_BC + STAGES * 2 * BC_SLOT;
+    static constexpr int OFF_BCW = OFF_BC + (kWarpC ? 0 : STAGES * 2 * BC_SLOT);
     static constexpr int OFF_WORK = OFF_BCW + WB * BCW_BYTES;
     static constexpr int WORK_BYTES = kF32 || kRawU ? 0 : WORK_ROWS * FROW * 4;  // per warp
     static constexpr int OFF_YP = OFF_WORK + kWarps * WORK_BYTES;
@@ -175,6 +180,7 @@ struct TmaCfg {
     static_assert(RROW * ESZ % 16 == 0 && RROW_U * ESZ % 16 == 0 && FROW % 4 == 0, "16-byte rows");
     static_assert(CPW <= 256 && NSP <= 256 && RROW <= 256 && RROW_U <= 256, "tensor-map box limits");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(!kWarpC || BC_BOX <= U_SLOT, "a warp's C box fits a row-set slot");
 };
 
 // Steps [T0, T0 + TS) of a chunk of the recurrence for the calling lane, from
@@ -644,6 +650,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
     using UT = typename std::conditional<kRawU, bf16, float>::type;
     constexpr int UROW = kRawU ? Cfg::RROW_U : FROW;
     constexpr unsigned FULL = 0xffffffffu;
+    constexpr bool WC = Cfg::kWarpC;  // C per warp: no CTA-shared ring, no CTA-wide votes
     extern __shared__ __align__(16) unsigned char smem_dyn[];
     // 128-byte aligned base, offset from the shared array itself so that the
     // compiler keeps every derived pointer in the shared address space
@@ -706,8 +713,9 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         u_hi = c;
         T* dst = u_slot(st);
         uint64_t* bar = barU + w * STAGES + st;
-        mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX);
+        mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX + (WC ? Cfg::BC_BOX : 0));
         const int t0 = (int)(t_begin + (long long)c * TC);
+        if constexpr (WC) tma_load_3d(reinterpret_cast<unsigned char*>(dst) + 2 * Cfg::U_SLOT, &tm.C, t0, 0, (int)b, bar);
         tma_load_3d(dst, &tm.u, t0, (int)dw, (int)b, bar);
         tma_load_3d(reinterpret_cast<unsigned char*>(dst) + Cfg::U_SLOT, &tm.delta, t0, (int)dw, (int)b, bar);
         if (gated)
@@ -736,12 +744,13 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         for (int c = 0; c < STAGES && c < nchunks; ++c) {
             u_hi = c;
             uint64_t* bar = barU + w * STAGES + c;
-            mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX);
+            mbar_arrive_expect_tx(bar, (gated ? 3 : 2) * Cfg::U_BOX + (WC ? Cfg::BC_BOX : 0));
             const int t0 = (int)(t_begin + (long long)c * TC);
             unsigned char* dst = reinterpret_cast<unsigned char*>(u_slot(c));
             tma_load_3d(dst + Cfg::U_SLOT, &tm.delta, t0, (int)dw, (int)b, bar);
             if (gated) tma_load_3d(dst + 2 * Cfg::U_SLOT, &tm.z, t0, (int)dw, (int)b, bar);
-            if (w == 0) issue_bc(c, c);
+            if constexpr (WC) tma_load_3d(dst + 2 * Cfg::U_SLOT, &tm.C, t0, 0, (int)b, bar);
+            else if (w == 0) issue_bc(c, c);
         }
     }
 
@@ -961,14 +970,14 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         const float *sz, *sB, *sC;
         if constexpr (Cfg::kF32) {
             ok = mbar_wait_bounded(barU + w * STAGES + st, par, lim);
-            ok = mbar_wait_bounded(barBC + st, par, lim) && ok;
+            if constexpr (!WC) ok = mbar_wait_bounded(barBC + st, par, lim) && ok;
             ok = __all_sync(FULL, ok);
             if (!ok && !CORR) break;
             su = reinterpret_cast<const UT*>(u_slot(st));
             sd = reinterpret_cast<const UT*>(reinterpret_cast<const unsigned char*>(su) + Cfg::U_SLOT);
             sz = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(su) + 2 * Cfg::U_SLOT);
             sB = reinterpret_cast<const float*>(bc_slot(st));
-            sC = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(sB) + Cfg::BC_SLOT);
+            sC = WC ? sz : reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(sB) + Cfg::BC_SLOT);
             if (OPT > 0 && xform) {
                 // delta transform in place on the warp's rows: lane = step;
                 // padding (channels past dim, steps past the segment) keeps 0
@@ -1044,14 +1053,21 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 live[k] = (scalar || !cut) ? true : __any_sync(FULL, l);
                 any |= l;
             }
-            // a wait that gave up in any warp ends the CTA's correction; so
-            // does the decay of every state of every lane (CTA-wide votes, so
-            // that every warp leaves the loop at the same chunk)
-            if (__syncthreads_or(!ok)) {
-                ok = false;
-                break;
+            if constexpr (WC) {
+                // every warp on its own: a wait that gave up, or the decay of
+                // every state of its lanes, ends its correction
+                if (!ok) break;
+                if (cut && !__any_sync(FULL, any)) break;
+            } else {
+                // a wait that gave up in any warp ends the CTA's correction; so
+                // does the decay of every state of every lane (CTA-wide votes, so
+                // that every warp leaves the loop at the same chunk)
+                if (__syncthreads_or(!ok)) {
+                    ok = false;
+                    break;
+                }
+                if (cut && !__syncthreads_or(any)) break;
             }
-            if (cut && !__syncthreads_or(any)) break;
         }
         if constexpr (SH && CORR) {
             const int nvalid = (int)min((long long)TC, t_end - t0);
@@ -1062,7 +1078,7 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 decay_chunk_shfl1<T, UT, UROW, NS, P, FROW, TC, false>(su, sd, sC, rl, g, Al2, As, live, h,
                                                                        sh_orow + t0, sh_store, nvalid);
             __syncwarp();
-            if (lane == 0) {  // C of this chunk is no longer read by this warp
+            if (!WC && lane == 0) {  // C of this chunk is no longer read by this warp
                 if constexpr (Cfg::kF32) {
                     const unsigned old = atomicAdd(bc_count + st, 1u);
                     if ((old + 1) % kWarps == 0 && nx < nchunks) issue_bc(nx, st);
@@ -1131,7 +1147,8 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
         }
     }
     // Every warp leaves the chunk loop here (a local pass has no CTA barrier in
-    // the loop; a correction leaves it at the same chunk by CTA-wide votes).
+    // the loop; a correction leaves it at the same chunk by CTA-wide votes,
+    // except the shuffle kernels' fp32 one, whose warps each leave on their own).
     // After this barrier no warp issues a copy, so a CTA that gave up on a
     // wait, or a correction that stopped early, waits (bounded) for the last
     // copy issued into every ring stage before it leaves: none may land in
