@@ -132,6 +132,33 @@ SHFL_CASES = [
 ]
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_shuffle_correction_warps_with_different_horizons(lr, dtype):
+    """The shuffle kernel's carry correction follows each warp's carries for as
+    long as they live: here the first 16 channels of every 64 decay a thousand
+    times more slowly than the rest (whose states die within a few chunks), so the
+    warps of one correction CTA stop at very different chunks (with their last
+    copies still in flight when they stop).
+    The split plan must compute what the unsplit plan and the oracle compute."""
+    w = workloads.WORKLOADS["long64k"].scaled(batch=1, dim=136, L=4096, N=16)
+    w = workloads.Workload(**{**w.__dict__, "dtype": dtype})
+    x = workloads.make_inputs(w)
+    A = x["A"].clone()
+    slow = (torch.arange(w.dim) % 64) < 16
+    A[slow] = A[slow] * 0.01
+    A[~slow] = A[~slow] * 10.0
+    x["A"] = A
+    g = _dev(x)
+    y1, h1 = lr.sscan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["h0"], segments=1, lanes=2)
+    plan = _compare(lr, w, x, TOL[dtype], lanes=2, segments=8)
+    assert " shfl " in plan and "S=8 " in plan, plan
+    y, hT = lr.sscan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["h0"], segments=8, lanes=2)
+    torch.cuda.synchronize()
+    assert lr.get_last_error() == 0
+    assert _rel_err(y.double().cpu().numpy(), y1.double().cpu().numpy()) <= TOL[dtype]
+    assert _rel_err(hT.double().cpu().numpy(), h1.double().cpu().numpy()) <= TOL[dtype]
+
+
 @pytest.mark.parametrize("case", SHFL_CASES, ids=lambda c: "x".join(map(str, c[:5])))
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_shuffle_kernel(lr, case, dtype):
