@@ -29,7 +29,12 @@
 //     warp c mod 4, one chunk ahead), into an fp32 ring of WB slots with a
 //     full mbarrier (the widening warp's lanes arrive) and an empty one (every
 //     warp arrives when it is done with the slot); only the widening warp
-//     reads the raw B/C stage, so it refills that stage itself.
+//     reads the raw B/C stage, so it refills that stage itself;
+//   * the shuffle kernels (SH): the lanes of a channel sum its partial outputs
+//     by warp shuffles and store them (no partial-output buffer, no epilogue);
+//     their fp32 carry correction, one channel per lane, stages the C rows per
+//     warp with the warp's local outputs and delta, so its warps run on their
+//     own (no CTA-shared ring, no CTA-wide votes).
 // fp32 boxes (and the raw bf16 u/delta boxes read in place) are TC + 16 bytes
 // wide: the extra columns (the next chunk's first steps, or zeros past the
 // end) pad every shared-memory row exactly as the cp.async ring does, so the
@@ -548,13 +553,26 @@ __device__ __forceinline__ void decay_chunk_shfl1(const TU* sy, const TU* sd, co
         if (live[k]) nql = k / QS + 1;
     // no live slot: the carry adds nothing to this chunk's outputs
     if (nql == 0) return;
-    if constexpr (NQ >= 4)
-        if (nql == 4) return decay_blocks_shfl1<4, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
-    if constexpr (NQ >= 3)
-        if (nql == 3) return decay_blocks_shfl1<3, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
-    if constexpr (NQ >= 2)
-        if (nql == 2) return decay_blocks_shfl1<2, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
-    decay_blocks_shfl1<1, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, rl[0], Al2, As, h, orow, store, nvalid);
+    const int r = rl[0];
+    if constexpr (NQ >= 4) {
+        if (nql == 4) {
+            decay_blocks_shfl1<4, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, r, Al2, As, h, orow, store, nvalid);
+            return;
+        }
+    }
+    if constexpr (NQ >= 3) {
+        if (nql == 3) {
+            decay_blocks_shfl1<3, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, r, Al2, As, h, orow, store, nvalid);
+            return;
+        }
+    }
+    if constexpr (NQ >= 2) {
+        if (nql == 2) {
+            decay_blocks_shfl1<2, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, r, Al2, As, h, orow, store, nvalid);
+            return;
+        }
+    }
+    decay_blocks_shfl1<1, T, TU, UROW, NS, P, FROW, TC, SCALAR>(sy, sd, bC, r, Al2, As, h, orow, store, nvalid);
 }
 
 // Steps [T0, T0 + TS) of the carry correction for the calling lane: the
