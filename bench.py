@@ -51,6 +51,7 @@ UNIT = "tokens*channels/s"
 SM_COUNT = 152
 MUFU_PER_CLK_SM = 32     # ex2 lanes per clock per SM, nominal (used only if the probe fails)
 FP32_PER_CLK_SM = 128    # FP32 lanes per clock per SM (unit count)
+ISSUE_LANES_PER_CLK_SM = 128  # 4 schedulers x one 32-lane warp instruction per clock
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
@@ -112,14 +113,13 @@ def measure_ex2(dev, stream, reps=3):
 
 
 def measure_element(dev, stream, shared_rate, reps=3):
-    """Elements per second of the scan's arithmetic at its peak on this GPU,
+    """Elements per second that this GPU reaches with the scan's arithmetic,
     from the library's element probe: per element one 2^x and four FP32
     operations (three FP32 when a channel's states share one decay rate and
     the 2^x is taken once per step), independent chains on every SM (two
     resident CTAs of 256 threads, four waves); best of ``reps`` CUDA-event
-    timings after a warm-up launch.  The exponent and the FP32 operations draw
-    on the same issue slots, so this is the rate that bounds the scan's
-    arithmetic, below both units' separate peaks."""
+    timings after a warm-up launch.  Reported beside the roofline: the mix
+    issues at about three quarters of the issue slots' peak (dispatch stalls)."""
     import torch
     import linear_recurrence_gb300 as lr
     blocks, iters = SM_COUNT * 8, 2000
@@ -139,10 +139,14 @@ def measure_element(dev, stream, shared_rate, reps=3):
 
 def roofline(w, t_s, pk):
     """The slower of the HBM bound (algorithmic bytes at the measured copy
-    bandwidth) and the arithmetic bound (the elements at the measured peak
-    element rate of the scan's exponent/FP32 mix, sscan_probe_element).  The
-    separate MUFU and FP32-pipe bounds, and the fraction of the HBM bound
-    alone, are reported beside it."""
+    bandwidth) and the issue bound of the arithmetic, derived from unit counts
+    and the clock: every exponent and every FP32 operation of the scan takes
+    one lane of an issue slot, and an SM issues one 32-lane warp instruction
+    per scheduler and clock (four schedulers, 152 SMs, the maximum SM clock).
+    Beside it: the exponent unit's and the FP32 pipe's separate bounds, the
+    elements at the rate the element probe reaches with this exact mix
+    (sscan_probe_element, measured in the run) and the fraction of the HBM
+    bound alone."""
     a = algorithmic(w)
     clk = pk["sm_max_mhz"] * 1e6
     bw = pk["hbm_gbs"] * 1e9
@@ -150,28 +154,30 @@ def roofline(w, t_s, pk):
     t_hbm = a["bytes"] / bw
     t_exp = a["exps"] / ex2_rate
     t_fp32 = a["fp32"] / (FP32_PER_CLK_SM * SM_COUNT * clk)
-    shared = a["exps"] < a["elements"]
-    elem_rate = pk.get("elem_shared_per_s" if shared else "elem_per_s")
-    if elem_rate:
-        t_alu, alu_src = a["elements"] / elem_rate, "measured in this run (sscan_probe_element)"
-    else:
-        t_alu, alu_src = max(t_exp, t_fp32), "separate unit peaks (element probe failed)"
-        elem_rate = a["elements"] / t_alu
-    t_roof = max(t_hbm, t_alu)
+    lane_ops = a["exps"] + a["fp32"]
+    issue_peak = ISSUE_LANES_PER_CLK_SM * SM_COUNT * clk  # lane operations per second
+    t_issue = lane_ops / issue_peak
+    t_roof = max(t_hbm, t_issue)
     achieved_gbs = a["bytes"] / t_s / 1e9
-    if t_hbm >= t_alu:
+    if t_hbm >= t_issue:
         r = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
              "frac": achieved_gbs / pk["hbm_gbs"]}
     else:
-        # an arithmetic-bound scan: the rate in elements (b, d, t, n)
-        peak = elem_rate / 1e12
-        r = {"bound": "alu", "achieved": a["elements"] / t_s / 1e12, "peak": peak,
-             "unit": "T elements/s (" + ("three FP32 per element, one 2^x per step" if shared
-                                        else "one 2^x and four FP32 per element") + ")",
-             "frac": (a["elements"] / t_s / 1e12) / peak}
-    r.update({"peak_source": pk["source"], "alu_peak_source": alu_src,
-              "elem_peak_t_s": elem_rate / 1e12, "t_roofline_us": t_roof * 1e6,
-              "t_hbm_us": t_hbm * 1e6, "t_alu_us": t_alu * 1e6,
+        # an arithmetic-bound scan: exponents and FP32 operations per second
+        r = {"bound": "alu", "achieved": lane_ops / t_s / 1e12, "peak": issue_peak / 1e12,
+             "unit": "T lane-ops/s (exponents + FP32 operations, one issue-slot lane each)",
+             "frac": (lane_ops / t_s) / issue_peak,
+             "peak_derivation": f"{SM_COUNT} SMs x {ISSUE_LANES_PER_CLK_SM} lanes (4 schedulers x one 32-lane "
+                                f"warp instruction) per clock x {pk['sm_max_mhz']:.0f} MHz"}
+    shared = a["exps"] < a["elements"]
+    elem_rate = pk.get("elem_shared_per_s" if shared else "elem_per_s")
+    if elem_rate:
+        t_meas = a["elements"] / elem_rate
+        r.update({"alu_measured_t_elem_s": elem_rate / 1e12, "t_alu_measured_us": t_meas * 1e6,
+                  "frac_of_measured_alu": t_meas / t_s,
+                  "alu_measured_source": "sscan_probe_element in this run (the same exponent/FP32 mix)"})
+    r.update({"peak_source": pk["source"], "t_roofline_us": t_roof * 1e6,
+              "t_hbm_us": t_hbm * 1e6, "t_issue_us": t_issue * 1e6,
               "ex2_peak_source": pk.get("ex2_source", "nominal"), "ex2_peak_texp_s": ex2_rate / 1e12,
               "t_exp_us": t_exp * 1e6, "t_fp32_us": t_fp32 * 1e6,
               "hbm_gbs": achieved_gbs, "frac_of_roofline": t_roof / t_s, "frac_of_hbm": t_hbm / t_s})
@@ -666,6 +672,7 @@ def main():
                          "hbm_gbs": rfx["hbm_gbs"], "bound": rfx["bound"],
                          "frac": rfx["frac"], "frac_of_roofline": rfx["frac_of_roofline"],
                          "frac_of_hbm": rfx["frac_of_hbm"],
+                         "frac_of_measured_alu": rfx.get("frac_of_measured_alu"),
                          "t_roofline_us": rfx["t_roofline_us"], "plan": r["plan"],
                          "clocks": ckx.summary()}
         with ClockSampler(physical_gpu(dev.index or 0)) as ckx:

@@ -78,24 +78,36 @@ def test_roofline_arithmetic():
     w = bench.workloads.WORKLOADS["dim512"]
     a = bench.algorithmic(w)
     assert a["bytes"] == 3 * 512 * 8192 * 4 + 2 * 16 * 8192 * 4 + 512 * 16 * 4 + 512 * 4 + 512 * 16 * 4
-    r = bench.roofline(w, 1e-5, pk)
+    # one state per channel: the bytes bind
+    w1 = w.scaled(N=1)
+    a1 = bench.algorithmic(w1)
+    r = bench.roofline(w1, 1e-5, pk)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
-    assert r["achieved"] == pytest.approx(a["bytes"] / 1e-5 / 1e9)
+    assert r["achieved"] == pytest.approx(a1["bytes"] / 1e-5 / 1e9)
     assert r["frac"] == pytest.approx(r["achieved"] / 6788.3)
     assert r["frac_of_hbm"] == pytest.approx(r["frac"])
-    # without the element probe the arithmetic bound is the slower of the
-    # separate unit peaks: the bf16 and the wide workloads are bound by it
+    # the arithmetic bound: every exponent and FP32 operation one issue-slot
+    # lane, 128 lanes per clock per SM at the maximum clock
+    issue = 128 * 152 * 2070e6
     rb = bench.roofline(bench.workloads.WORKLOADS["bf16_2k"], 1e-4, pk)
-    assert rb["bound"] == "alu" and rb["t_alu_us"] == pytest.approx(max(rb["t_exp_us"], rb["t_fp32_us"]))
-    # with measured element rates (one 2^x and four FP32 per element; three
-    # FP32 with a shared rate) the bound is the elements at that rate
-    pk.update({"elem_per_s": 5.8e12, "elem_shared_per_s": 9.7e12})
+    ab = bench.algorithmic(bench.workloads.WORKLOADS["bf16_2k"])
+    assert ab["exps"] == ab["elements"] and ab["fp32"] == 4 * ab["elements"]
+    assert rb["bound"] == "alu" and rb["peak"] == pytest.approx(issue / 1e12)
+    assert rb["t_issue_us"] == pytest.approx(5 * ab["elements"] / issue * 1e6)
+    assert rb["frac"] == pytest.approx(5 * ab["elements"] / 1e-4 / issue)
+    assert rb["frac_of_roofline"] == pytest.approx(rb["t_issue_us"] * 1e-6 / 1e-4)
+    # dim512: the issue bound (8.3 us) is above the HBM bound (7.6 us)
     r = bench.roofline(w, 1e-5, pk)
-    assert r["bound"] == "alu" and r["t_alu_us"] == pytest.approx(a["elements"] / 5.8e12 * 1e6)
-    assert r["frac"] == pytest.approx(a["elements"] / 1e-5 / 5.8e12)
-    assert r["frac_of_roofline"] == pytest.approx(r["t_alu_us"] * 1e-6 / 1e-5)
+    assert r["bound"] == "alu" and r["t_issue_us"] > r["t_hbm_us"]
     assert r["frac_of_hbm"] == pytest.approx(a["bytes"] / (6788.3e9 * 1e-5))
+    # one rate per channel: one exponent per (b, d, t), three FP32 per element
     ww = bench.workloads.WORKLOADS["wide64"]
+    aw = bench.algorithmic(ww)
+    assert aw["exps"] == aw["tokens_channels"] and aw["fp32"] == 3 * aw["elements"]
     rw = bench.roofline(ww, 1e-3, pk)
-    assert rw["t_alu_us"] == pytest.approx(bench.algorithmic(ww)["elements"] / 9.7e12 * 1e6)
-    assert "three FP32" in rw["unit"]
+    assert rw["t_issue_us"] == pytest.approx((aw["exps"] + aw["fp32"]) / issue * 1e6)
+    # the element probe's measured rates are reported beside the bound
+    pk.update({"elem_per_s": 5.8e12, "elem_shared_per_s": 9.7e12})
+    rw = bench.roofline(ww, 1e-3, pk)
+    assert rw["t_alu_measured_us"] == pytest.approx(aw["elements"] / 9.7e12 * 1e6)
+    assert rw["frac_of_measured_alu"] == pytest.approx(aw["elements"] / 9.7e12 / 1e-3)
