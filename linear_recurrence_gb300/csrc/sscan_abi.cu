@@ -602,8 +602,10 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     p.seg_dsum = p.seg_state + nseg * (size_t)dstate;
     p.seg_dmin = p.seg_dsum + nseg;
     // pass 1: every segment from its local start, writing y and its aggregate;
-    // pass 2: fold the aggregates into the state entering each segment (and
-    // the final state); pass 3: add the carried state's decaying contribution
+    // pass 2 (more than kFoldInCorrectionMaxSegments segments): fold the
+    // aggregates into the state entering each segment; pass 3: add the carried
+    // state's decaying contribution (folding the aggregates itself when pass 2
+    // did not run) and compose the final state
     // (bf16 outputs are rounded twice, the second time with the carry added)
     p.mode = sscan::MODE_LOCAL;
     p.seg_count = (int)S;

@@ -120,15 +120,17 @@ SSCAN_DECLARE_TMA_UNIT(bf16_z)
 bool tma_encode_3d(CUtensorMap* map, const void* base, bool f32, long long L, long long rows, long long batch,
                    int box_l, int box_rows);
 
-// The fold pass of a time split into three or more segments (sscan_fold.cu):
-// from the local pass's aggregates, the state entering each segment s >= 1,
-// written over aggregate slot s - 1; launched as a programmatic dependent of
-// the local pass.
+// The fold pass of a time split into more than kFoldInCorrectionMaxSegments
+// segments (sscan_fold.cu): from the local pass's aggregates, the state
+// entering each segment s >= 1, written over aggregate slot s - 1; launched as
+// a programmatic dependent of the local pass.
 cudaError_t fwd_fold_launch(const FwdParams& p, cudaStream_t stream);
 // Splits of up to this many segments skip the fold pass: each correction CTA
 // folds the earlier segments' aggregates itself (O(S) per CTA, a few loads in
-// flight at a time), which costs less than one more launch on the critical
-// path (512 channels x 8192 steps in 19 segments: 47.1 us with the fold pass).
+// flight at a time), which saves one launch on the critical path (512
+// channels x 8192 steps in 19 segments: 47.1 us either way, one launch fewer).
+// Beyond it the pass is cheaper (1536 x 65536 in 25 segments: 453 us with the
+// pass, 464 us with the fold in the correction).
 constexpr long long kFoldInCorrectionMaxSegments = 24;
 // Scratch floats per (channel, segment) of a time split: the end state (N),
 // the sum of delta and min(0, smallest delta).
