@@ -260,6 +260,20 @@ int sscan_get_last_error(void);
 void sscan_debug_expire_next_wait(unsigned int wait_limit_us);
 
 /*
+ * sscan_debug_expire_next_correction_wait -- the same test aid for the carry
+ * correction of a time split; the pages have no counterpart.  It arms the
+ * calling thread's next sscan_fwd / sscan_fwd_ex / sscan_fwd_fused call: if
+ * that call splits time and its correction runs on the TMA-fed kernels, one
+ * ring stage of each correction CTA (the first B/C stage, or the first warp's
+ * first stage where the warps stage C themselves) is made to expect 16 bytes
+ * that no copy delivers, and the correction's bounded waits give up after
+ * wait_limit_us microseconds; the outcome is as above (SSCAN_ERR_TIMEOUT,
+ * outputs undefined, context usable).  The next call consumes the setting
+ * whichever plan it runs; 0 disarms it.
+ */
+void sscan_debug_expire_next_correction_wait(unsigned int wait_limit_us);
+
+/*
  * sscan_probe_ex2 -- a measurement aid for the roofline of the scan; the
  * pages have no counterpart.  It launches `blocks` CTAs of 256 threads on
  * `stream`, each thread running 16 independent chains of `iters` exponentials

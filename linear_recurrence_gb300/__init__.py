@@ -50,6 +50,7 @@ SIGNATURES = {
     "sscan_get_last_error": (_int, []),
     "sscan_max_dstate": (_int, []),
     "sscan_debug_expire_next_wait": (None, [ctypes.c_uint]),
+    "sscan_debug_expire_next_correction_wait": (None, [ctypes.c_uint]),
     "sscan_probe_ex2": (_int, [_fp, _int, _int, _vp]),
     "sscan_probe_ex2_count": (ctypes.c_longlong, [_int, _int]),
     "sscan_probe_element": (_int, [_fp, _int, _int, _int, _vp]),
@@ -134,6 +135,13 @@ def debug_expire_next_wait(wait_limit_us: int) -> None:
     """Test aid: make the bounded waits of this thread's next forward call
     run out after ``wait_limit_us`` (see include/sscan.h)."""
     lib().sscan_debug_expire_next_wait(int(wait_limit_us))
+
+
+def debug_expire_next_correction_wait(wait_limit_us: int) -> None:
+    """Test aid: make the bounded waits of the carry correction of this
+    thread's next forward call run out after ``wait_limit_us`` (see
+    include/sscan.h)."""
+    lib().sscan_debug_expire_next_correction_wait(int(wait_limit_us))
 
 
 def last_launch_count() -> int:

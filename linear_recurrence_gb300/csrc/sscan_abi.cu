@@ -31,6 +31,9 @@ thread_local CallRecord g_rec;
 // thread's next forward call, whose first B/C stage is made to never complete
 // (0: not armed)
 thread_local unsigned g_expire_wait_us = 0;
+// sscan_debug_expire_next_correction_wait: the same for the carry correction
+// of this thread's next forward call (0: not armed)
+thread_local unsigned g_expire_corr_us = 0;
 
 int sm_count() {
     static std::atomic<int> cached[64] = {};  // per device ordinal; host threads may race
@@ -459,6 +462,7 @@ const char* sscan_status_string(int status) {
 int sscan_max_dstate(void) { return sscan::kMaxDstate; }
 
 void sscan_debug_expire_next_wait(unsigned int wait_limit_us) { g_expire_wait_us = wait_limit_us; }
+void sscan_debug_expire_next_correction_wait(unsigned int wait_limit_us) { g_expire_corr_us = wait_limit_us; }
 
 int sscan_last_launch_count(void) { return g_rec.launches; }
 
@@ -562,9 +566,12 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     p.delta_softplus = (flags & SSCAN_DELTA_SOFTPLUS) ? 1 : 0;
     p.zoh = (flags & SSCAN_ZOH) ? 1 : 0;
     p.status = status;
-    // the test aid applies to the first pass of this call only
+    // the test aids apply to the first pass, or to the carry correction, of
+    // this call only
     const unsigned expire_us = g_expire_wait_us;
     g_expire_wait_us = 0;
+    const unsigned expire_corr_us = g_expire_corr_us;
+    g_expire_corr_us = 0;
     p.wait_ns = (unsigned long long)expire_us * 1000ull;
     p.expire_wait = expire_us != 0 ? 1 : 0;
 
@@ -617,6 +624,8 @@ int sscan_fwd_fused(const void* u, const void* delta, const float* A, const void
     p.fold_in_corr = S <= sscan::kFoldInCorrectionMaxSegments ? 1 : 0;
     if (e == cudaSuccess && S > 2 && !p.fold_in_corr) e = launch_fold(p, st);
     if (e == cudaSuccess) {
+        p.wait_ns = (unsigned long long)expire_corr_us * 1000ull;
+        p.expire_wait = expire_corr_us != 0 ? 1 : 0;
         p.mode = sscan::MODE_CORR;
         p.seg_count = (int)(S - 1);
         p.tiles_per_batch = (int)pl.corr_tiles_per_batch;

@@ -717,9 +717,10 @@ __device__ __forceinline__ void sscan_fwd_tma_body(const FwdParams& p, const Tma
                 mbar_init(bcw_empty + i, kWarps);
             }
         }
-        // test aid: bytes that no copy delivers keep the first B/C stage
-        // from completing, so that the waits on it run out
-        if (p.expire_wait) mbar_expect_tx(barBC, 16);
+        // test aid: bytes that no copy delivers keep the first B/C stage (the
+        // first warp's first ring stage where C comes per warp) from
+        // completing, so that the waits on it run out
+        if (p.expire_wait) mbar_expect_tx(WC ? barU : barBC, 16);
         mbar_fence_init();
     }
     __syncthreads();
